@@ -1,0 +1,237 @@
+"""Pins for the oracle's verify (accept / resample / bonus / commit).
+
+Sources: "DFlash to DSpark in SGLang", section "Background" (accepted prefix
+plus one bonus token) and section "Serving DeepSeek-V4 with SGLang" (the
+target's output distribution is unchanged); "SGLang Integrates DSpark ...",
+section "The Old Problem with Speculative Decoding: It Breaks Down at Scale"
+(speculative sampling, Chen et al. 2023).
+
+The statistical tests replicate one request over many batch slots; each slot
+has its own Philox counter (b, k), so the slots are independent draws.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+from scipy import special, stats
+
+import oracle
+
+GOLDEN = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "worked_examples.json")))
+ALPHA = 1e-3
+
+
+def test_greedy_worked_example():
+    g = GOLDEN["verify_greedy"]
+    tgt = np.array(g["target"], np.float32)
+    for case in g["cases"]:
+        a, tok, _, _, tie = oracle.verify_request(3, case["drafts"], tgt, None, 0.0,
+                                                  np.zeros(4), np.zeros(4))
+        assert (a, tok) == (case["a"], case["token"]), case
+        assert tie == 0
+
+
+def test_sampling_worked_examples():
+    for case in GOLDEN["verify_sampling"]["cases"]:
+        Tm = case["Tm"]
+        tgt = np.array([np.log(case["p"]), np.log(case["p1"])], np.float64) * Tm
+        dft = np.array([np.log(case["q"])], np.float64) * Tm
+        a, tok, p, q, _ = oracle.verify_request(1, [case["draft"]], tgt.astype(np.float32),
+                                                dft.astype(np.float32), Tm,
+                                                np.array(case["u"]), np.array(case["u2"]))
+        assert (a, tok) == (case["a"], case["token"]), case["name"]
+        np.testing.assert_allclose(p[0], case["p_tok"], atol=1e-6)
+        np.testing.assert_allclose(q[0], case["q_tok"], atol=1e-6)
+
+
+def _ragged(tgt_rows_per_req, L):
+    return np.concatenate(tgt_rows_per_req, axis=0)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_greedy_is_longest_argmax_prefix(seed):
+    rng = np.random.default_rng(seed)
+    B, gamma, V = 12, 5, 40
+    tgt_dense = rng.integers(-3, 4, (B, gamma + 1, V)).astype(np.float32)  # many ties
+    argm = np.argmax(tgt_dense, axis=-1)                                    # first max
+    drafts = argm[:, :gamma].copy().astype(np.int32)
+    # break the agreement at a random position in some requests
+    for b in range(B):
+        if rng.random() < 0.7:
+            k = rng.integers(0, gamma)
+            drafts[b, k] = (drafts[b, k] + 1 + rng.integers(0, V - 1)) % V
+    L = rng.integers(0, gamma + 1, B).astype(np.int32)
+    cpt = oracle.compact(L, drafts)
+    tgt = oracle.ragged_target(tgt_dense, L, cpt["row_off"])
+    out = oracle.verify(drafts, np.zeros((B, gamma, V), np.float32), tgt, L, cpt["row_off"],
+                        cpt["draft_off"], 0.0, 0)
+    for b in range(B):
+        a = 0
+        while a < L[b] and drafts[b, a] == argm[b, a]:
+            a += 1
+        assert out["accept_len"][b] == a
+        assert out["num_emitted"][b] == a + 1
+        assert list(out["out_tokens"][b, :a]) == list(drafts[b, :a])
+        assert out["out_tokens"][b, a] == argm[b, a]
+        assert np.all(out["out_tokens"][b, a + 1:] == -1)
+
+
+def test_greedy_drafts_equal_to_argmax_accept_everything():
+    rng = np.random.default_rng(1)
+    B, gamma, V = 6, 8, 64
+    tgt_dense = rng.standard_normal((B, gamma + 1, V)).astype(np.float32)
+    drafts = np.argmax(tgt_dense[:, :gamma], axis=-1).astype(np.int32)
+    L = np.array([0, 1, 3, 8, 8, 5], np.int32)
+    cpt = oracle.compact(L, drafts)
+    tgt = oracle.ragged_target(tgt_dense, L, cpt["row_off"])
+    out = oracle.verify(drafts, np.zeros((B, gamma, V), np.float32), tgt, L, cpt["row_off"],
+                        cpt["draft_off"], 0.0, 0, seq_lens=np.full(B, 10, np.int32))
+    np.testing.assert_array_equal(out["accept_len"], L)
+    np.testing.assert_array_equal(out["seq_lens"], 10 + L + 1)
+
+
+@pytest.mark.parametrize("Tm", [1.0, 0.7])
+def test_probabilities_are_library_softmax(Tm):
+    rng = np.random.default_rng(2)
+    B, gamma, V = 5, 4, 50
+    tgt_dense = rng.normal(0, 2, (B, gamma + 1, V)).astype(np.float32)
+    dft = (tgt_dense[:, :gamma] + rng.normal(0, 0.5, (B, gamma, V))).astype(np.float32)
+    drafts = rng.integers(0, V, (B, gamma)).astype(np.int32)
+    L = np.array([4, 0, 2, 3, 1], np.int32)
+    cpt = oracle.compact(L, drafts)
+    tgt = oracle.ragged_target(tgt_dense, L, cpt["row_off"])
+    out = oracle.verify(drafts, dft, tgt, L, cpt["row_off"], cpt["draft_off"], Tm, 11)
+    for b in range(B):
+        for k in range(L[b]):
+            P = special.softmax(tgt_dense[b, k].astype(np.float64) / np.float32(Tm))
+            Q = special.softmax(dft[b, k].astype(np.float64) / np.float32(Tm))
+            j = cpt["draft_off"][b] + k
+            np.testing.assert_allclose(out["p_tok"][j], P[drafts[b, k]], rtol=1e-12)
+            np.testing.assert_allclose(out["q_tok"][j], Q[drafts[b, k]], rtol=1e-12)
+
+
+def test_identical_draft_and_target_accept_everything():
+    rng = np.random.default_rng(3)
+    B, gamma, V = 40, 6, 30
+    tgt_dense = rng.normal(0, 2, (B, gamma + 1, V)).astype(np.float32)
+    dft = tgt_dense[:, :gamma].copy()
+    drafts = rng.integers(0, V, (B, gamma)).astype(np.int32)
+    L = rng.integers(0, gamma + 1, B).astype(np.int32)
+    cpt = oracle.compact(L, drafts)
+    tgt = oracle.ragged_target(tgt_dense, L, cpt["row_off"])
+    out = oracle.verify(drafts, dft, tgt, L, cpt["row_off"], cpt["draft_off"], 1.0, 4)
+    np.testing.assert_array_equal(out["accept_len"], L)
+
+
+def _replicate(p_logits, q_logits, bonus_logits, drafts, n, seed, Tm=1.0):
+    """n slots of one L=1 request: row 0 holds (p, q), row 1 the bonus p1."""
+    V = p_logits.shape[0]
+    L = np.ones(n, np.int32)
+    tgt = np.empty((2 * n, V), np.float32)
+    tgt[0::2] = p_logits
+    tgt[1::2] = bonus_logits
+    dft = np.broadcast_to(q_logits, (n, 1, V)).astype(np.float32)
+    row_off = (2 * np.arange(n + 1)).astype(np.int32)
+    draft_off = np.arange(n + 1).astype(np.int32)
+    return oracle.verify(np.asarray(drafts, np.int32).reshape(n, 1), dft, tgt, L, row_off,
+                         draft_off, Tm, seed)
+
+
+@pytest.mark.parametrize("V,seed", [(4, 0), (8, 1), (16, 2)])
+def test_accept_frequency_is_min_one_p_over_q(V, seed):
+    rng = np.random.default_rng(100 + seed)
+    zp = rng.normal(0, 1.5, V).astype(np.float32)
+    zq = (zp + rng.normal(0, 1.0, V)).astype(np.float32)
+    P, Q = special.softmax(zp.astype(np.float64)), special.softmax(zq.astype(np.float64))
+    d = int(np.argmax(Q / P))                     # a draft with r < 1
+    r = min(1.0, P[d] / Q[d])
+    n = 100_000
+    out = _replicate(zp, zq, zp, np.full(n, d), n, seed)
+    acc = int(np.sum(out["accept_len"] == 1))
+    assert stats.binomtest(acc, n, r).pvalue > ALPHA
+
+
+@pytest.mark.parametrize("V,seed", [(4, 0), (8, 1), (16, 2)])
+def test_resampled_tokens_follow_the_normalised_residual(V, seed):
+    rng = np.random.default_rng(200 + seed)
+    zp = rng.normal(0, 1.5, V).astype(np.float32)
+    zq = (zp + rng.normal(0, 1.5, V)).astype(np.float32)
+    P, Q = special.softmax(zp.astype(np.float64)), special.softmax(zq.astype(np.float64))
+    d = int(np.argmax(Q / P))
+    n = 100_000
+    out = _replicate(zp, zq, zp, np.full(n, d), n, seed)
+    rej = out["accept_len"] == 0
+    toks = out["out_tokens"][rej, 0]
+    resid = np.maximum(0.0, P - Q)
+    resid /= resid.sum()
+    support = resid > 0
+    assert np.all(support[toks])                 # never a token with zero residual
+    counts = np.bincount(toks, minlength=V)[support]
+    assert stats.chisquare(counts, resid[support] * counts.sum()).pvalue > ALPHA
+
+
+@pytest.mark.parametrize("V,seed,Tm", [(4, 0, 1.0), (8, 1, 1.0), (16, 2, 0.7)])
+def test_first_emitted_token_follows_the_target(V, seed, Tm):
+    """Speculative-sampling theorem: with the draft drawn from q, the first
+    emitted token (accepted draft or resample) is distributed as p."""
+    rng = np.random.default_rng(300 + seed)
+    zp = rng.normal(0, 1.5, V).astype(np.float32)
+    zq = (zp + rng.normal(0, 1.5, V)).astype(np.float32)
+    Tm32 = np.float32(Tm)
+    P = special.softmax(zp.astype(np.float64) / Tm32)
+    Q = special.softmax(zq.astype(np.float64) / Tm32)
+    n = 100_000
+    drafts = rng.choice(V, size=n, p=Q / Q.sum())
+    out = _replicate(zp, zq, zp, drafts, n, seed, Tm=Tm)
+    first = out["out_tokens"][:, 0]
+    counts = np.bincount(first, minlength=V)
+    assert stats.chisquare(counts, P * n).pvalue > ALPHA
+
+
+@pytest.mark.parametrize("V,seed", [(4, 3), (16, 4)])
+def test_bonus_token_follows_the_target(V, seed):
+    rng = np.random.default_rng(400 + seed)
+    zp = rng.normal(0, 1.5, V).astype(np.float32)
+    z1 = rng.normal(0, 1.5, V).astype(np.float32)
+    P1 = special.softmax(z1.astype(np.float64))
+    n = 100_000
+    # the draft is the argmax of p/q with q == p: ratio 1, always accepted
+    out = _replicate(zp, zp, z1, np.zeros(n, np.int32), n, seed)
+    assert np.all(out["accept_len"] == 1)
+    counts = np.bincount(out["out_tokens"][:, 1], minlength=V)
+    assert stats.chisquare(counts, P1 * n).pvalue > ALPHA
+
+
+def test_commit_and_padding():
+    rng = np.random.default_rng(5)
+    B, gamma, V = 8, 5, 20
+    tgt_dense = rng.normal(0, 1, (B, gamma + 1, V)).astype(np.float32)
+    dft = (tgt_dense[:, :gamma] + rng.normal(0, 1, (B, gamma, V))).astype(np.float32)
+    drafts = rng.integers(0, V, (B, gamma)).astype(np.int32)
+    L = rng.integers(0, gamma + 1, B).astype(np.int32)
+    cpt = oracle.compact(L, drafts)
+    tgt = oracle.ragged_target(tgt_dense, L, cpt["row_off"])
+    sl = rng.integers(10, 100, B).astype(np.int32)
+    out = oracle.verify(drafts, dft, tgt, L, cpt["row_off"], cpt["draft_off"], 1.0, 6,
+                        seq_lens=sl)
+    a = out["accept_len"]
+    assert np.all((a >= 0) & (a <= L))
+    np.testing.assert_array_equal(out["num_emitted"], a + 1)
+    np.testing.assert_array_equal(out["seq_lens"], sl + a + 1)
+    for b in range(B):
+        row = out["out_tokens"][b]
+        assert list(row[:a[b]]) == list(drafts[b, :a[b]])
+        assert 0 <= row[a[b]] < V
+        assert np.all(row[a[b] + 1:] == -1)
+
+
+def test_oracle_step_on_the_tiny_workload():
+    import torch  # noqa: F401  (the generators draw with torch)
+    from confidence_driven_speculative_gb300 import workloads
+    for Tm in (0.0, 1.0):
+        inp = workloads.to_numpy(workloads.make_inputs(workloads.TINY, 0, temperature=Tm))
+        res = oracle.step(inp)
+        assert res["L"].sum() <= inp["cap_T"]
+        assert np.all(res["accept_len"] <= res["L"])
+        assert np.all(np.diff(res["surv"], axis=1) <= 0)
