@@ -160,7 +160,8 @@ def test_resampled_tokens_follow_the_normalised_residual(V, seed):
     P, Q = special.softmax(zp.astype(np.float64)), special.softmax(zq.astype(np.float64))
     d = int(np.argmax(Q / P))
     n = 100_000
-    out = _replicate(zp, zq, zp, np.full(n, d), n, seed)
+    z1 = rng.normal(0, 1.5, V).astype(np.float32)   # a different bonus row
+    out = _replicate(zp, zq, z1, np.full(n, d), n, seed)
     rej = out["accept_len"] == 0
     toks = out["out_tokens"][rej, 0]
     resid = np.maximum(0.0, P - Q)
@@ -235,3 +236,46 @@ def test_oracle_step_on_the_tiny_workload():
         assert res["L"].sum() <= inp["cap_T"]
         assert np.all(res["accept_len"] <= res["L"])
         assert np.all(np.diff(res["surv"], axis=1) <= 0)
+
+
+def test_inverse_cdf_uses_strict_crossing():
+    """The sampled token is the smallest x with C(x) > u' * Z: a target that
+    lands exactly on a cumulative sum moves past it, and u' = 0 never picks a
+    token of zero weight."""
+    V = 4
+    zero = np.zeros(V, np.float32)                   # uniform: C = [.25, .5, .75, 1]
+    tgt = np.stack([zero, zero])
+    for u2, want in [(0.0, 0), (0.25, 1), (0.5, 2), (0.75, 3), (0.99, 3)]:
+        a, tok, _, _, _ = oracle.verify_request(1, [0], tgt, zero[None], 1.0,
+                                                np.array([0.0, 0.0]), np.array([0.0, u2]))
+        assert (a, tok) == (1, want), u2
+    # residual max(0, p - q) = [0, 0.4, 0, 0], u' = 0: the first positive weight
+    p = np.array([0.1, 0.5, 0.2, 0.2])
+    q = np.array([0.2, 0.1, 0.4, 0.3])
+    tgt = np.stack([np.log(p), np.log(p)]).astype(np.float32)
+    a, tok, _, _, _ = oracle.verify_request(1, [2], tgt, np.log(q)[None].astype(np.float32), 1.0,
+                                            np.array([0.9, 0.0]), np.array([0.0, 0.0]))
+    assert (a, tok) == (0, 1)
+
+
+def test_uniforms_are_wired_to_philox_words():
+    """Per slot b the accept test uses word 0 of Philox((b, k, 0, 0), (seed, 0))
+    and the resample uses word 1: r = 1/2 at every slot, so slot b accepts iff
+    u_b < 1/2; after a rejection the residual [0.3, 0, 0.1, 0] (Z = 0.4) gives
+    token 0 iff u'_b * 0.4 < 0.3."""
+    from tests.test_oracle_philox import numpy_block
+    seed, n = 77, 300
+    p = np.array([0.4, 0.1, 0.3, 0.2])
+    q = np.array([0.1, 0.2, 0.2, 0.5])                # p(1)/q(1) = 1/2
+    zp = np.log(p).astype(np.float32)
+    zq = np.log(q).astype(np.float32)
+    out = _replicate(zp, zq, zp, np.ones(n, np.int32), n, seed)
+    for b in range(n):
+        w0, w1 = numpy_block((b, 0, 0, 0), (seed, 0))[:2]
+        u = int(w0 >> np.uint64(40)) / 2.0**24
+        u2 = int(w1 >> np.uint64(40)) / 2.0**24
+        if abs(u - 0.5) < 1e-6:
+            continue
+        assert out["accept_len"][b] == (1 if u < 0.5 else 0), b
+        if u >= 0.5 and abs(u2 * 0.4 - 0.3) > 1e-6:
+            assert out["out_tokens"][b, 0] == (0 if u2 * 0.4 < 0.3 else 2), b
