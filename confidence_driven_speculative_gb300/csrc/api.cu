@@ -1,0 +1,283 @@
+// api.cu -- the C ABI of libdspark.so (declared in include/dspark.h):
+// argument validation, workspace carving, per-device launch configuration.
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "dspark_internal.cuh"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+dspark_status fail(dspark_status s, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+dspark_status cuda_fail(cudaError_t e, const char *what) {
+    return fail(DSPARK_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned(const void *p, size_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
+
+size_t dtype_size(int32_t dt) { return dt == DSPARK_BF16 ? 2 : 4; }
+
+// Per-device facts and one-time kernel attributes.
+struct DeviceInfo {
+    bool ready = false;
+    int sms = 0;
+    int verify_blocks[2] = {0, 0};  // per logit dtype (0 = fp32, 1 = bf16)
+};
+constexpr int kMaxDevices = 64;
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+dspark_status device_info(DeviceInfo **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(DSPARK_EDEVICE, "device index %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    DeviceInfo &d = g_dev[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0;
+        if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute");
+        if (major != 10 || minor != 3)
+            return fail(DSPARK_EDEVICE, "libdspark is built for sm_103a; device %d is sm_%d%d", dev,
+                        major, minor);
+        for (int bf = 0; bf < 2; ++bf) {
+            d.verify_blocks[bf] = dspark::verify_blocks_per_sm(bf);
+            if (d.verify_blocks[bf] <= 0)
+                return fail(DSPARK_ECUDA, "verify kernel cannot be resident (smem %zu bytes)",
+                            dspark::verify_smem_bytes());
+        }
+        d.ready = true;
+    }
+    *out = &d;
+    return DSPARK_OK;
+}
+
+dspark_status check_shape(const dspark_step *s) {
+    if (!s) return fail(DSPARK_EINVAL, "step is NULL");
+    if (s->B < 0 || s->B > DSPARK_MAX_B) return fail(DSPARK_EINVAL, "B=%d outside [0, %d]", s->B, DSPARK_MAX_B);
+    if (s->gamma < 1 || s->gamma > DSPARK_MAX_GAMMA)
+        return fail(DSPARK_EINVAL, "gamma=%d outside [1, %d]", s->gamma, DSPARK_MAX_GAMMA);
+    if (s->V < 1 || s->V > DSPARK_MAX_V) return fail(DSPARK_EINVAL, "V=%d outside [1, %d]", s->V, DSPARK_MAX_V);
+    if (s->d < 1 || s->d > DSPARK_MAX_D) return fail(DSPARK_EINVAL, "d=%d outside [1, %d]", s->d, DSPARK_MAX_D);
+    if (s->logit_dtype != DSPARK_F32 && s->logit_dtype != DSPARK_BF16)
+        return fail(DSPARK_EDTYPE, "logit_dtype=%d", s->logit_dtype);
+    if (s->hidden_dtype != DSPARK_F32 && s->hidden_dtype != DSPARK_BF16)
+        return fail(DSPARK_EDTYPE, "hidden_dtype=%d", s->hidden_dtype);
+    return DSPARK_OK;
+}
+
+dspark_status check_workspace(const dspark_step *s, dspark::WorkspaceLayout *lay) {
+    *lay = dspark::workspace_layout(s->B, s->gamma, s->V);
+    if (!s->workspace) return fail(DSPARK_EWORKSPACE, "workspace is NULL");
+    if (!aligned(s->workspace, 256)) return fail(DSPARK_EWORKSPACE, "workspace is not 256-byte aligned");
+    if (s->workspace_bytes < lay->total)
+        return fail(DSPARK_EWORKSPACE, "workspace has %zu bytes, needs %zu", s->workspace_bytes, lay->total);
+    return DSPARK_OK;
+}
+
+template <typename T>
+T *ws_at(const dspark_step *s, size_t off) {
+    return reinterpret_cast<T *>(static_cast<char *>(s->workspace) + off);
+}
+
+#define REQUIRE(ptr)                                                             \
+    do {                                                                         \
+        if (!(ptr)) return fail(DSPARK_EINVAL, "%s: " #ptr " is NULL", fn);     \
+    } while (0)
+#define REQUIRE_ALIGNED(ptr, n)                                                  \
+    do {                                                                         \
+        if (!aligned((ptr), (n)))                                                \
+            return fail(DSPARK_EALIGN, "%s: " #ptr " is not %d-byte aligned", fn, int(n)); \
+    } while (0)
+
+}  // namespace
+
+extern "C" {
+
+size_t dspark_workspace_size(int32_t B, int32_t gamma, int32_t V, int32_t d) {
+    if (B < 0 || B > DSPARK_MAX_B || gamma < 1 || gamma > DSPARK_MAX_GAMMA || V < 1 ||
+        V > DSPARK_MAX_V || d < 1 || d > DSPARK_MAX_D)
+        return 0;
+    return dspark::workspace_layout(B, gamma, V).total;
+}
+
+dspark_status dspark_workspace_init(void *workspace, size_t workspace_bytes, dspark_stream_t stream) {
+    if (!workspace) return fail(DSPARK_EWORKSPACE, "workspace is NULL");
+    cudaError_t e = cudaMemsetAsync(workspace, 0, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(workspace)");
+    g_err[0] = 0;
+    return DSPARK_OK;
+}
+
+dspark_status dspark_score_budget(const dspark_step *s, dspark_stream_t stream) {
+    const char *fn = "dspark_score_budget";
+    dspark_status st = check_shape(s);
+    if (st) return st;
+    if (s->B == 0) return DSPARK_OK;
+    REQUIRE(s->L);
+    REQUIRE(s->draft_off);
+    REQUIRE(s->row_off);
+    const bool fixed = s->fixed_budget >= 0;
+    if (fixed && s->cap_T >= 0)
+        return fail(DSPARK_EINVAL, "%s: a fixed budget (%d) cannot be combined with a cap (%d)", fn,
+                    s->fixed_budget, s->cap_T);
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    DeviceInfo *dev;
+    if (fixed) {
+        if ((st = device_info(&dev))) return st;
+        dspark::FixedArgs a{s->B, s->gamma, s->fixed_budget, s->L, s->draft_off, s->row_off};
+        cudaError_t e = dspark::launch_fixed_budget(a, cs);
+        if (e != cudaSuccess) return cuda_fail(e, "fixed_budget_kernel launch");
+        return DSPARK_OK;
+    }
+    REQUIRE(s->hidden);
+    REQUIRE(s->head_w);
+    REQUIRE(s->head_bias);
+    REQUIRE(s->sts_tau);
+    REQUIRE(s->conf);
+    REQUIRE(s->survival);
+    REQUIRE(s->L0);
+    if (std::isnan(s->cost_c)) return fail(DSPARK_EINVAL, "%s: cost_c is NaN", fn);
+    const size_t hs = dtype_size(s->hidden_dtype);
+    REQUIRE_ALIGNED(s->hidden, 16);
+    REQUIRE_ALIGNED(s->head_w, 16);
+    if ((size_t(s->d) * hs) % 16 != 0)
+        return fail(DSPARK_EALIGN, "%s: a hidden row (d=%d) is not a multiple of 16 bytes", fn, s->d);
+    dspark::WorkspaceLayout lay;
+    if ((st = check_workspace(s, &lay))) return st;
+    if ((st = device_info(&dev))) return st;
+
+    const int nvec = int(size_t(s->d) * hs / 16);
+    int splits = (2 * dev->sms + s->B - 1) / s->B;
+    splits = std::min(splits, dspark::kMaxScoreSplits);
+    splits = std::min(splits, std::max(1, nvec / 32));
+    splits = std::max(splits, 1);
+    dspark::ScoreArgs a{};
+    a.B = s->B; a.gamma = s->gamma; a.d = s->d; a.splits = splits;
+    a.hidden_bf16 = s->hidden_dtype == DSPARK_BF16;
+    a.hidden = s->hidden; a.head_w = s->head_w; a.head_bias = s->head_bias; a.sts_tau = s->sts_tau;
+    a.cost_c = s->cost_c; a.cap_T = s->cap_T;
+    a.conf = s->conf; a.survival = s->survival; a.L0 = s->L0; a.L = s->L;
+    a.draft_off = s->draft_off; a.row_off = s->row_off;
+    a.dot_part = ws_at<float>(s, lay.dot_part);
+    a.req_cnt = ws_at<int32_t>(s, lay.score_cnt);
+    a.done_cnt = ws_at<int32_t>(s, lay.score_done);
+    a.status = ws_at<int32_t>(s, lay.status);
+    cudaError_t e = dspark::launch_score_budget(a, s->B * splits, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "score_budget_kernel launch");
+    return DSPARK_OK;
+}
+
+dspark_status dspark_compact(const dspark_step *s, dspark_stream_t stream) {
+    const char *fn = "dspark_compact";
+    dspark_status st = check_shape(s);
+    if (st) return st;
+    if (s->B == 0) return DSPARK_OK;
+    REQUIRE(s->L);
+    REQUIRE(s->row_off);
+    REQUIRE(s->draft_tokens);
+    REQUIRE(s->packed_ids);
+    REQUIRE(s->packed_pos);
+    REQUIRE(s->row_req);
+    REQUIRE(s->row_k);
+    DeviceInfo *dev;
+    if ((st = device_info(&dev))) return st;
+    dspark::CompactArgs a{s->B, s->gamma, s->L, s->row_off, s->draft_tokens, s->last_tokens,
+                          s->seq_lens_in, s->packed_ids, s->packed_pos, s->row_req, s->row_k};
+    cudaError_t e = dspark::launch_compact(a, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "compact_kernel launch");
+    return DSPARK_OK;
+}
+
+dspark_status dspark_verify(const dspark_step *s, dspark_stream_t stream) {
+    const char *fn = "dspark_verify";
+    dspark_status st = check_shape(s);
+    if (st) return st;
+    if (s->B == 0) return DSPARK_OK;
+    const bool greedy = s->temperature == 0.0f;
+    if (!(s->temperature >= 0.0f) || std::isinf(s->temperature))
+        return fail(DSPARK_EINVAL, "%s: temperature must be finite and >= 0", fn);
+    REQUIRE(s->draft_tokens);
+    REQUIRE(s->target_logits);
+    if (!greedy) REQUIRE(s->draft_logits);
+    REQUIRE(s->L);
+    REQUIRE(s->draft_off);
+    REQUIRE(s->row_off);
+    REQUIRE(s->row_req);
+    REQUIRE(s->row_k);
+    REQUIRE(s->accept_len);
+    REQUIRE(s->num_emitted);
+    REQUIRE(s->out_tokens);
+    REQUIRE(s->p_tok);
+    REQUIRE(s->q_tok);
+    const size_t ls = dtype_size(s->logit_dtype);
+    REQUIRE_ALIGNED(s->target_logits, 16);
+    if (!greedy) REQUIRE_ALIGNED(s->draft_logits, 16);
+    if ((size_t(s->V) * ls) % 16 != 0)
+        return fail(DSPARK_EALIGN, "%s: a logit row (V=%d) is not a multiple of 16 bytes", fn, s->V);
+    if (size_t(s->V) * ls > size_t(INT32_MAX))
+        return fail(DSPARK_EINVAL, "%s: a logit row is too large", fn);
+    dspark::WorkspaceLayout lay;
+    if ((st = check_workspace(s, &lay))) return st;
+    DeviceInfo *dev;
+    if ((st = device_info(&dev))) return st;
+
+    const int bf = s->logit_dtype == DSPARK_BF16;
+    dspark::VerifyArgs a{};
+    a.B = s->B; a.gamma = s->gamma; a.V = s->V;
+    a.row_bytes = int(size_t(s->V) * ls);
+    a.nc = (a.row_bytes + dspark::kChunkBytes - 1) / dspark::kChunkBytes;
+    a.chunk_elems = int(dspark::kChunkBytes / ls);
+    a.greedy = greedy;
+    a.scale = greedy ? 0.f : float(1.4426950408889634 / double(s->temperature));
+    a.seed = s->seed;
+    a.draft_tokens = s->draft_tokens;
+    a.draft_logits = s->draft_logits;
+    a.target_logits = s->target_logits;
+    a.L = s->L; a.draft_off = s->draft_off; a.row_off = s->row_off;
+    a.row_req = s->row_req; a.row_k = s->row_k;
+    a.accept_len = s->accept_len; a.num_emitted = s->num_emitted; a.out_tokens = s->out_tokens;
+    a.p_tok = s->p_tok; a.q_tok = s->q_tok; a.seq_lens_commit = s->seq_lens_commit;
+    a.part = ws_at<float4>(s, lay.part);
+    a.gath = ws_at<float2>(s, lay.gath);
+    a.req_cnt = ws_at<int32_t>(s, lay.verify_cnt);
+    a.status = ws_at<int32_t>(s, lay.status);
+    const long long max_tasks = (long long)s->B * (s->gamma + 1) * a.nc;
+    const long long resident = (long long)dev->sms * dev->verify_blocks[bf];
+    const int grid = int(std::min(max_tasks, resident));
+    cudaError_t e = dspark::launch_verify(a, bf, grid, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "verify_kernel launch");
+    return DSPARK_OK;
+}
+
+dspark_status dspark_read_device_status(const void *workspace, int32_t *status_out,
+                                        dspark_stream_t stream) {
+    if (!workspace) return fail(DSPARK_EWORKSPACE, "workspace is NULL");
+    if (!status_out) return fail(DSPARK_EINVAL, "status_out is NULL");
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(status_out, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost, cs);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device status");
+    return DSPARK_OK;
+}
+
+const char *dspark_last_error(void) { return g_err; }
+
+const char *dspark_version(void) { return "dspark-gb300 0.1.0 (sm_103a)"; }
+
+}  // extern "C"

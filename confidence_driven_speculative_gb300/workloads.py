@@ -134,7 +134,9 @@ def make_inputs(w: Workload, step: int = 0, device="cpu", temperature: Optional[
     cap_T, temperature, seed, fixed_budget.
     """
     if B is not None or V is not None or d is not None or gamma is not None:
-        w = dataclasses.replace(w, B=B or w.B, V=V or w.V, d=d or w.d, gamma=gamma or w.gamma)
+        w = dataclasses.replace(w, B=w.B if B is None else B, V=w.V if V is None else V,
+                                d=w.d if d is None else d,
+                                gamma=w.gamma if gamma is None else gamma)
     Tm = w.temperature if temperature is None else float(temperature)
     dt = torch.float32 if w.dtype == "f32" else torch.bfloat16
     gen = torch.Generator(device=device)
@@ -203,3 +205,12 @@ def to_numpy(inp: dict) -> dict:
         else:
             out[k] = v
     return out
+
+
+def ragged_target_rows(target_dense, row_req, row_k, n_rows: int):
+    """Stand-in for the target forward over the packed rows: row r of the
+    result is the target row (row_req[r], row_k[r]) of a dense
+    [B, gamma+1, V] tensor.  A plain gather (torch), not part of the step."""
+    B, g1, V = target_dense.shape
+    idx = row_req[:n_rows].long() * g1 + row_k[:n_rows].long()
+    return target_dense.reshape(B * g1, V).index_select(0, idx)

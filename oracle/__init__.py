@@ -69,16 +69,16 @@ def _load():
             i32, f64, u64, i64 = ctypes.c_int, ctypes.c_double, ctypes.c_uint64, ctypes.c_int64
             lib.orc_philox4x64_10.argtypes = [P, P, P]
             lib.orc_philox4x64_10.restype = None
-            lib.orc_uniforms.argtypes = [u64, i64, i64, P, P]
+            lib.orc_uniforms.argtypes = [u64, i64, i64, P, P, P]
             lib.orc_uniforms.restype = None
             lib.orc_score.argtypes = [i32, i32, i32, i32, P, P, P, P, f64, f64, P, P, P, P]
             lib.orc_fixed_budget.argtypes = [i32, i32, i32, P]
             lib.orc_cap.argtypes = [i32, i32, P, P, i32, f64, P, P]
             lib.orc_compact.argtypes = [i32, i32, P, P, P, P, P, P, P, P, P, P]
-            lib.orc_verify_request.argtypes = [i32, i32, i32, P, P, P, f64, P, P, f64,
-                                               P, P, P, P, P]
-            lib.orc_verify.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, f64, u64, f64,
-                                       P, P, P, P, P, P, P]
+            lib.orc_verify_request.argtypes = [i32, i32, i32, P, P, P, f64, P, P, P, f64, f64,
+                                               f64, P, P, P, P, P]
+            lib.orc_verify.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, f64, u64, f64, f64,
+                                       f64, P, P, P, P, P, P, P]
             for name in ("orc_score", "orc_fixed_budget", "orc_cap", "orc_compact",
                          "orc_verify_request", "orc_verify"):
                 getattr(lib, name).restype = ctypes.c_int
@@ -117,13 +117,16 @@ def philox4x64_10(ctr, key) -> np.ndarray:
     return out
 
 
-def uniforms(seed: int, b: int, k: int) -> tuple[float, float]:
-    """(u, u') of draft position ``k`` of request ``b``: Philox counter (b,k,0,0), key (seed,0)."""
+def uniforms(seed: int, b: int, k: int) -> tuple[float, float, float]:
+    """(u, u', u'') of draft position ``k`` of request ``b``: words 0, 1, 2 of
+    Philox counter (b,k,0,0), key (seed,0)."""
     lib = _load()
     u = ctypes.c_double()
     u2 = ctypes.c_double()
-    lib.orc_uniforms(ctypes.c_uint64(seed), b, k, ctypes.byref(u), ctypes.byref(u2))
-    return u.value, u2.value
+    u3 = ctypes.c_double()
+    lib.orc_uniforms(ctypes.c_uint64(seed), b, k, ctypes.byref(u), ctypes.byref(u2),
+                     ctypes.byref(u3))
+    return u.value, u2.value, u3.value
 
 
 def score(hidden, w, bias, tau, c: float, eps: float = 1e-5):
@@ -194,12 +197,16 @@ def compact(L, draft_tokens, last_tokens=None, seq_lens=None) -> dict:
     return out
 
 
-def verify_request(L: int, drafts, tgt, dft, Tm: float, u, u2, eps: float = 1e-5):
+EPS_U, EPS_BLK, EPS_TOK = 1e-5, 1e-6, 5e-7
+
+
+def verify_request(L: int, drafts, tgt, dft, Tm: float, u, u2, u3, eps: float = EPS_U,
+                   eps_blk: float = EPS_BLK, eps_tok: float = EPS_TOK):
     """Verify one request with explicit uniforms.
 
     ``tgt`` [L+1, V] target rows (root first), ``dft`` [L, V] draft rows (may be
-    ``None`` when ``Tm == 0``), ``u``/``u2`` [L+1].  Returns
-    ``(a, token, p[L], q[L], tie)``.
+    ``None`` when ``Tm == 0``), ``u``/``u2``/``u3`` [L+1] (accept, block,
+    in-block).  Returns ``(a, token, p[L], q[L], tie)``.
     """
     lib = _load()
     tgt = np.ascontiguousarray(tgt)
@@ -210,20 +217,23 @@ def verify_request(L: int, drafts, tgt, dft, Tm: float, u, u2, eps: float = 1e-5
     drafts = _c(drafts, np.int32) if L > 0 else np.zeros(1, np.int32)
     u = _c(u, np.float64)
     u2 = _c(u2, np.float64)
+    u3 = _c(u3, np.float64)
     a = ctypes.c_int32()
     tok = ctypes.c_int32()
     tie = ctypes.c_int32()
     p = np.zeros(max(L, 1), np.float64)
     q = np.zeros(max(L, 1), np.float64)
     rc = lib.orc_verify_request(L, V, _logit_dtype(tgt), _ptr(drafts), _ptr(tgt), _ptr(dft),
-                                float(np.float32(Tm)), _ptr(u), _ptr(u2), eps, ctypes.byref(a),
+                                float(np.float32(Tm)), _ptr(u), _ptr(u2), _ptr(u3), eps,
+                                eps_blk, eps_tok, ctypes.byref(a),
                                 ctypes.byref(tok), _ptr(p), _ptr(q), ctypes.byref(tie))
     _check(rc, "verify_request")
     return int(a.value), int(tok.value), p[:L], q[:L], int(tie.value)
 
 
 def verify(draft_tokens, draft_logits, target_ragged, L, row_off, draft_off, Tm: float,
-           seed: int, eps: float = 1e-5, seq_lens=None) -> dict:
+           seed: int, eps: float = EPS_U, seq_lens=None, eps_blk: float = EPS_BLK,
+           eps_tok: float = EPS_TOK) -> dict:
     """Verify the batch.
 
     ``draft_logits`` [B, gamma, V]; ``target_ragged`` [N_rows, V] with request
@@ -251,7 +261,7 @@ def verify(draft_tokens, draft_logits, target_ragged, L, row_off, draft_off, Tm:
     sl = None if seq_lens is None else _c(seq_lens, np.int32).copy()
     rc = lib.orc_verify(B, gamma, V, dt, _ptr(draft_tokens), _ptr(draft_logits),
                         _ptr(target_ragged), _ptr(L), _ptr(row_off), _ptr(draft_off),
-                        float(np.float32(Tm)), ctypes.c_uint64(seed), eps,
+                        float(np.float32(Tm)), ctypes.c_uint64(seed), eps, eps_blk, eps_tok,
                         _ptr(out["accept_len"]), _ptr(out["num_emitted"]), _ptr(out["out_tokens"]),
                         _ptr(out["p_tok"]), _ptr(out["q_tok"]), _ptr(sl), _ptr(out["tie"]))
     _check(rc, "verify")
@@ -275,7 +285,7 @@ def ragged_target(target_dense, L, row_off) -> np.ndarray:
     return out[:n] if n > 0 else out[:0]
 
 
-def step(inp: dict, eps_s: float = 1e-5, eps_cap: float = 2e-5, eps_u: float = 1e-5,
+def step(inp: dict, eps_s: float = 1e-5, eps_cap: float = 2e-5, eps_u: float = EPS_U,
          L_override=None) -> dict:
     """The whole step a1..a6 on one input dict (keys as produced by the
     workload generators): score, cap (or fixed budget), compact, the

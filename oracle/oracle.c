@@ -82,9 +82,10 @@ double orc_uniform24(uint64_t word)
     return (double)(word >> 40) * (1.0 / 16777216.0);
 }
 
-/* The two uniforms of draft position k of request b: counter (b, k, 0, 0),
- * key (seed, 0); word 0 is the accept uniform u, word 1 the resample u'. */
-void orc_uniforms(uint64_t seed, int64_t b, int64_t k, double *u, double *u2)
+/* The uniforms of draft position k of request b: counter (b, k, 0, 0), key
+ * (seed, 0); word 0 is the accept uniform u, word 1 the block uniform u' and
+ * word 2 the in-block uniform u'' of a draw at that position. */
+void orc_uniforms(uint64_t seed, int64_t b, int64_t k, double *u, double *u2, double *u3)
 {
     uint64_t ctr[4] = {(uint64_t)b, (uint64_t)k, 0, 0};
     uint64_t key[2] = {seed, 0};
@@ -92,6 +93,7 @@ void orc_uniforms(uint64_t seed, int64_t b, int64_t k, double *u, double *u2)
     orc_philox4x64_10(ctr, key, out);
     *u = orc_uniform24(out[0]);
     *u2 = orc_uniform24(out[1]);
+    *u3 = orc_uniform24(out[2]);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -280,7 +282,8 @@ int orc_compact(int B, int gamma, const int32_t *L, const int32_t *draft_tokens,
 /* (lowest index on ties) and the emitted token is that argmax.             */
 /*                                                                           */
 /* tgt: L+1 contiguous rows of V logits; dft: L contiguous rows (unused when */
-/* Tm == 0).  u[k], u2[k] for k = 0..L.  Returns the accepted count in *a,   */
+/* Tm == 0).  u[k], u2[k], u3[k] (u, u', u'') for k = 0..L.  Returns the    */
+/* accepted count in *a,                                                     */
 /* the correction/bonus token in *tok, p(d_k), q(d_k) for k < L, and in      */
 /* *tie the number of near-tie decisions that the outcome depends on.        */
 /* ------------------------------------------------------------------------ */
@@ -311,29 +314,74 @@ static void softmax_row(const void *row, int dtype, int V, double Tm, double *pr
     for (int64_t y = 0; y < V; ++y) prob[y] /= s;
 }
 
-/* Inverse-CDF draw from nonnegative weights wt[0..V-1] with total Z > 0. */
-static int32_t inverse_cdf(const double *wt, int V, double Z, double u2, double eps, int32_t *tie)
+/* Tokens per sampling block of the two-level draw (reading, see below). */
+#define ORC_SAMPLE_BLOCK 8192
+
+/* Two-level inverse-CDF draw from nonnegative weights wt[0..V-1].
+ * Reading taken (the pages do not fix how a token is drawn): ids are split
+ * into consecutive blocks of ORC_SAMPLE_BLOCK; the block is the smallest j
+ * whose running block mass exceeds u_blk * Z (Z the total), and the token is
+ * the smallest x of that block whose running in-block weight exceeds
+ * u_tok * (the block's mass).  By the chain rule this draws x with
+ * probability wt[x] / Z.  When rounding leaves no crossing, the last block or
+ * token with positive weight is taken.  *tie counts draws whose margin to a
+ * crossing is below eps_blk * Z (block level) or eps_tok * mass (token level).
+ * Returns -1 when every weight is zero. */
+static int32_t draw_two_level(const double *wt, int V, double u_blk, double u_tok,
+                              double eps_blk, double eps_tok, int32_t *tie)
 {
-    const double target = u2 * Z;
+    const int nb = (V + ORC_SAMPLE_BLOCK - 1) / ORC_SAMPLE_BLOCK;
+    double *mass = (double *)malloc(sizeof(double) * (size_t)nb);
+    if (!mass) return -2;
+    double Z = 0.0;
+    for (int j = 0; j < nb; ++j) {
+        mass[j] = 0.0;
+        const int64_t y1 = (int64_t)(j + 1) * ORC_SAMPLE_BLOCK < V ? (int64_t)(j + 1) * ORC_SAMPLE_BLOCK : V;
+        for (int64_t y = (int64_t)j * ORC_SAMPLE_BLOCK; y < y1; ++y) mass[j] += wt[y];
+        Z += mass[j];
+    }
+    if (!(Z > 0.0)) { free(mass); return -1; }
+    const double t = u_blk * Z;
+    int jsel = -1;
     double before = 0.0;
-    for (int64_t x = 0; x < V; ++x) {
-        double after = before + wt[x];
-        if (after > target) {
-            if (target - before < eps * Z || after - target < eps * Z) (*tie)++;
-            return (int32_t)x;
+    for (int j = 0; j < nb; ++j) {
+        const double after = before + mass[j];
+        if (after > t) {
+            if (t - before < eps_blk * Z || after - t < eps_blk * Z) (*tie)++;
+            jsel = j;
+            break;
         }
         before = after;
     }
-    (*tie)++;
-    for (int64_t x = (int64_t)V - 1; x >= 0; --x) {
-        if (wt[x] > 0.0) return (int32_t)x;
+    if (jsel < 0) {
+        (*tie)++;
+        for (int j = nb - 1; j >= 0; --j)
+            if (mass[j] > 0.0) { jsel = j; break; }
     }
-    return 0;
+    const double m = mass[jsel];
+    free(mass);
+    const int64_t y0 = (int64_t)jsel * ORC_SAMPLE_BLOCK;
+    const int64_t y1 = y0 + ORC_SAMPLE_BLOCK < V ? y0 + ORC_SAMPLE_BLOCK : V;
+    const double t2 = u_tok * m;
+    double cum = 0.0;
+    for (int64_t x = y0; x < y1; ++x) {
+        const double after = cum + wt[x];
+        if (after > t2) {
+            if (t2 - cum < eps_tok * m || after - t2 < eps_tok * m) (*tie)++;
+            return (int32_t)x;
+        }
+        cum = after;
+    }
+    (*tie)++;
+    for (int64_t x = y1 - 1; x >= y0; --x)
+        if (wt[x] > 0.0) return (int32_t)x;
+    return (int32_t)y0;
 }
 
 int orc_verify_request(int L, int V, int dtype, const int32_t *drafts,
                        const void *tgt, const void *dft, double Tm,
-                       const double *u, const double *u2, double eps,
+                       const double *u, const double *u2, const double *u3,
+                       double eps, double eps_blk, double eps_tok,
                        int32_t *a_out, int32_t *tok_out, double *p_out,
                        double *q_out, int32_t *tie)
 {
@@ -392,14 +440,13 @@ int orc_verify_request(int L, int V, int dtype, const int32_t *drafts,
             Z += W[y];
         }
         if (Z < eps) (*tie)++;
-        if (Z > 0.0) tok = inverse_cdf(W, V, Z, u2[a], eps, tie);
-        else tok = inverse_cdf(P, V, 1.0, u2[a], eps, tie);
+        tok = draw_two_level(W, V, u2[a], u3[a], eps_blk, eps_tok, tie);
+        if (tok == -1) tok = draw_two_level(P, V, u2[a], u3[a], eps_blk, eps_tok, tie);
     } else {
         softmax_row(tbase + (size_t)L * V * es, dtype, V, Tm, P);
-        double Z = 0.0;
-        for (int64_t y = 0; y < V; ++y) Z += P[y];
-        tok = inverse_cdf(P, V, Z, u2[L], eps, tie);
+        tok = draw_two_level(P, V, u2[L], u3[L], eps_blk, eps_tok, tie);
     }
+    if (tok < 0) { free(P); free(Q); free(W); return -2; }
     *a_out = a;
     *tok_out = tok;
     free(P); free(Q); free(W);
@@ -415,25 +462,26 @@ int orc_verify_request(int L, int V, int dtype, const int32_t *drafts,
 int orc_verify(int B, int gamma, int V, int dtype, const int32_t *draft_tokens,
                const void *draft_logits, const void *target_logits,
                const int32_t *L, const int32_t *row_off, const int32_t *draft_off,
-               double Tm, uint64_t seed, double eps, int32_t *accept_len,
-               int32_t *num_emitted, int32_t *out_tokens, double *p_tok,
-               double *q_tok, int32_t *seq_lens, int32_t *tie)
+               double Tm, uint64_t seed, double eps, double eps_blk, double eps_tok,
+               int32_t *accept_len, int32_t *num_emitted, int32_t *out_tokens,
+               double *p_tok, double *q_tok, int32_t *seq_lens, int32_t *tie)
 {
     if (B < 0 || gamma < 1 || V < 1) return -1;
     const size_t es = dtype == 0 ? 4 : 2;
     double *u = (double *)malloc(sizeof(double) * (size_t)(gamma + 1));
     double *u2 = (double *)malloc(sizeof(double) * (size_t)(gamma + 1));
-    if (!u || !u2) { free(u); free(u2); return -2; }
+    double *u3 = (double *)malloc(sizeof(double) * (size_t)(gamma + 1));
+    if (!u || !u2 || !u3) { free(u); free(u2); free(u3); return -2; }
     int rc = 0;
     for (int b = 0; b < B && rc == 0; ++b) {
         const int Lb = L[b];
-        for (int k = 0; k <= Lb; ++k) orc_uniforms(seed, b, k, &u[k], &u2[k]);
+        for (int k = 0; k <= Lb; ++k) orc_uniforms(seed, b, k, &u[k], &u2[k], &u3[k]);
         const void *tgt = (const char *)target_logits + (size_t)row_off[b] * V * es;
         const void *dft = (const char *)draft_logits + (size_t)b * gamma * V * es;
         int32_t a, tok;
         rc = orc_verify_request(Lb, V, dtype, draft_tokens + (size_t)b * gamma, tgt, dft,
-                                Tm, u, u2, eps, &a, &tok, p_tok + draft_off[b],
-                                q_tok + draft_off[b], &tie[b]);
+                                Tm, u, u2, u3, eps, eps_blk, eps_tok, &a, &tok,
+                                p_tok + draft_off[b], q_tok + draft_off[b], &tie[b]);
         if (rc) break;
         accept_len[b] = a;
         num_emitted[b] = a + 1;
@@ -447,5 +495,6 @@ int orc_verify(int B, int gamma, int V, int dtype, const int32_t *draft_tokens,
     }
     free(u);
     free(u2);
+    free(u3);
     return rc;
 }

@@ -1,0 +1,138 @@
+"""Helpers for the GPU parity tests: run the CUDA step through the C ABI and
+compare it with the oracle, decision by decision.
+
+Tolerances (derived in DESIGN.md, section "Parity"): conf and survival agree
+within TOL_S absolute; p(d), q(d) within 1e-3 relative (floor 1e-30).  Every
+integer output is compared exactly, except a decision the oracle flags as a
+near tie (its fp64 margin below the tolerance the fp32 kernels are held to);
+there the GPU's choice is checked for validity and adopted, and the oracle
+continues from it.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from confidence_driven_speculative_gb300 import binding, workloads
+
+TOL_S = 1e-5           # |S_gpu - S_oracle|, |conf_gpu - conf_oracle|
+EPS_S = 2 * TOL_S      # oracle near-tie window for S_k vs c
+EPS_CAP = 4 * TOL_S    # oracle near-tie window between the T-th and (T+1)-th gains
+EPS_U = 1e-5           # |u - min(1, p/q)| window named by the method's tolerance
+RTOL_P = 1e-3
+
+
+def to_device(inp: dict, device="cuda") -> dict:
+    return {k: (v.to(device) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+
+
+def gpu_step(inp_dev: dict, seq_lens_commit: bool = True, bufs=None, stream=None):
+    """score_budget -> compact -> (target-forward stand-in) -> verify."""
+    B, g, V, d = inp_dev["B"], inp_dev["gamma"], inp_dev["V"], inp_dev["d"]
+    if bufs is None:
+        bufs = binding.StepBuffers(B, g, V, d, stream=stream)
+    commit = inp_dev["seq_lens"].clone() if seq_lens_commit else None
+    bufs.bind(inp_dev, seq_lens_commit=commit)
+    binding.dspark_score_budget(bufs.step, stream)
+    binding.dspark_compact(bufs.step, stream)
+    torch.cuda.synchronize()
+    n_rows = int(bufs.row_off[B].item()) if B > 0 else 0
+    tgt = workloads.ragged_target_rows(inp_dev["target_dense"], bufs.row_req, bufs.row_k,
+                                       n_rows).contiguous()
+    if tgt.numel() == 0:
+        tgt = torch.zeros((1, V), dtype=inp_dev["target_dense"].dtype, device="cuda")
+    bufs.bind_target(tgt)
+    binding.dspark_verify(bufs.step, stream)
+    torch.cuda.synchronize()
+    assert bufs.device_status() == 0
+    out = {k: getattr(bufs, k).cpu().numpy() for k in (
+        "conf", "survival", "L0", "L", "draft_off", "row_off", "packed_ids", "packed_pos",
+        "row_req", "row_k", "accept_len", "num_emitted", "out_tokens", "p_tok", "q_tok")}
+    out["seq_lens_commit"] = commit.cpu().numpy() if commit is not None else None
+    return out, bufs
+
+
+def check_L_valid(S, c, L0, L, T, tol=TOL_S):
+    """The GPU's L0 and L are a valid outcome of the budget rule and cap
+    given fp64 survival S (B x gamma, S_1..S_gamma) and an fp32 error <= tol."""
+    B, g = S.shape
+    Sx = np.concatenate([np.ones((B, 1)), S], axis=1)
+    for b in range(B):
+        l0 = L0[b]
+        assert 0 <= l0 <= g
+        if l0 > 0:
+            assert Sx[b, l0] >= c - tol, (b, l0)
+        if l0 < g:
+            assert not (Sx[b, l0 + 1] >= c + tol), (b, l0)
+        if c > 1 + tol:
+            assert l0 == 0
+    assert np.all((L >= 0) & (L <= L0))
+    if T < 0 or L0.sum() <= T:
+        assert np.array_equal(L, L0)
+        return
+    assert L.sum() == T
+    kept = [S[b, k] for b in range(B) for k in range(L[b])]
+    dropped = [S[b, k] for b in range(B) for k in range(L[b], L0[b])]
+    if kept and dropped:
+        assert min(kept) >= max(dropped) - 2 * tol
+
+
+def compare_with_oracle(inp_np: dict, gpu: dict, max_flag_frac: float = 0.05) -> dict:
+    """Check every GPU output of one step against the oracle.  Returns counts."""
+    B, g = inp_np["draft_tokens"].shape
+    stats = {"score_ties": 0, "cap_tie": 0, "verify_ties": 0}
+    fixed = inp_np.get("fixed_budget", -1)
+    if fixed is not None and fixed >= 0:
+        L = oracle.fixed_budget(B, g, fixed)
+        assert np.array_equal(gpu["L"], L)
+    else:
+        conf, surv, L0, tie = oracle.score(inp_np["hidden"], inp_np["head_w"],
+                                           inp_np["head_bias"], inp_np["sts_tau"],
+                                           inp_np["cost_c"], EPS_S)
+        np.testing.assert_allclose(gpu["conf"], conf, rtol=0, atol=TOL_S)
+        np.testing.assert_allclose(gpu["survival"], surv, rtol=0, atol=TOL_S)
+        assert np.all(np.diff(gpu["survival"], axis=1) <= 0)
+        c = float(np.float32(inp_np["cost_c"]))
+        untied = tie == 0
+        assert np.array_equal(gpu["L0"][untied], L0[untied]), "pre-cap lengths differ"
+        stats["score_ties"] = int((~untied).sum())
+        Lcap, cap_tie = oracle.cap(surv, gpu["L0"], inp_np["cap_T"], EPS_CAP)
+        stats["cap_tie"] = cap_tie
+        if cap_tie == 0:
+            assert np.array_equal(gpu["L"], Lcap), "capped lengths differ"
+        check_L_valid(surv, c, gpu["L0"], gpu["L"], inp_np["cap_T"])
+        L = gpu["L"]
+    cpt = oracle.compact(L, inp_np["draft_tokens"], inp_np["last_tokens"], inp_np["seq_lens"])
+    for k in ("draft_off", "row_off", "packed_ids", "packed_pos", "row_req", "row_k"):
+        assert np.array_equal(gpu[k], cpt[k]), k
+    tgt = oracle.ragged_target(inp_np["target_dense"], L, cpt["row_off"])
+    ver = oracle.verify(inp_np["draft_tokens"], inp_np["draft_logits"], tgt, L, cpt["row_off"],
+                        cpt["draft_off"], inp_np["temperature"], inp_np["seed"], EPS_U,
+                        inp_np["seq_lens"])
+    n = int(cpt["draft_off"][B])
+    flagged = ver["tie"] > 0
+    stats["verify_ties"] = int(flagged.sum())
+    assert stats["verify_ties"] <= max(2, int(max_flag_frac * B)), stats
+    ok = ~flagged
+    assert np.array_equal(gpu["accept_len"][ok], ver["accept_len"][ok]), "accept lengths differ"
+    assert np.array_equal(gpu["num_emitted"][ok], ver["num_emitted"][ok])
+    assert np.array_equal(gpu["out_tokens"][ok], ver["out_tokens"][ok]), "emitted tokens differ"
+    if inp_np["temperature"] > 0:
+        p_o, q_o = ver["p_tok"], ver["q_tok"]
+        p_g, q_g = gpu["p_tok"][:n].astype(np.float64), gpu["q_tok"][:n].astype(np.float64)
+        np.testing.assert_allclose(p_g, p_o, rtol=RTOL_P, atol=1e-30)
+        np.testing.assert_allclose(q_g, q_o, rtol=RTOL_P, atol=1e-30)
+    # flagged requests: still a valid outcome
+    V = inp_np["draft_logits"].shape[-1]
+    for b in np.nonzero(flagged)[0]:
+        a = gpu["accept_len"][b]
+        assert 0 <= a <= L[b]
+        assert np.array_equal(gpu["out_tokens"][b, :a], inp_np["draft_tokens"][b, :a])
+        assert 0 <= gpu["out_tokens"][b, a] < V
+        assert np.all(gpu["out_tokens"][b, a + 1:] == -1)
+    if gpu.get("seq_lens_commit") is not None:
+        assert np.array_equal(gpu["seq_lens_commit"], inp_np["seq_lens"] + gpu["accept_len"] + 1)
+    stats["mean_L"] = float(L.mean()) if B else 0.0
+    stats["mean_accept"] = float(gpu["accept_len"].mean()) if B else 0.0
+    return stats

@@ -1,0 +1,172 @@
+"""CPU checks of the C ABI: the library builds for sm_103a, exports every
+function include/dspark.h declares, the ctypes struct matches the C layout, and
+host-side validation returns the documented codes before touching the GPU."""
+import ctypes
+import os
+import re
+import subprocess
+import tempfile
+
+import pytest
+
+from confidence_driven_speculative_gb300 import _build, binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dspark.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return binding.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dspark_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_three_step_calls():
+    names = declared_functions()
+    for n in ("dspark_score_budget", "dspark_compact", "dspark_verify",
+              "dspark_workspace_size", "dspark_workspace_init", "dspark_last_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_function(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing
+    out = subprocess.run(["nm", "-D", "--defined-only", binding.lib_path()],
+                         capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (dspark_\w+)", out))
+    assert set(declared_functions()) <= exported
+
+
+def test_struct_layout_matches_c(lib):
+    fields = [f for f, _ in binding.DsparkStep._fields_]
+    src = ["#include <stdio.h>", "#include <stddef.h>", '#include "dspark.h"', "int main(void){",
+           'printf("%zu\\n", sizeof(dspark_step));']
+    src += [f'printf("%zu\\n", offsetof(dspark_step, {f}));' for f in fields]
+    src += ["return 0;}"]
+    with tempfile.TemporaryDirectory() as td:
+        c = os.path.join(td, "layout.c")
+        exe = os.path.join(td, "layout")
+        open(c, "w").write("\n".join(src))
+        subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), c, "-o", exe], check=True)
+        vals = [int(x) for x in subprocess.run([exe], capture_output=True, text=True,
+                                               check=True).stdout.split()]
+    assert vals[0] == ctypes.sizeof(binding.DsparkStep)
+    for f, off in zip(fields, vals[1:]):
+        assert getattr(binding.DsparkStep, f).offset == off, f
+
+
+def test_workspace_size(lib):
+    assert binding.dspark_workspace_size(256, 16, 129280, 7168) > 0
+    assert binding.dspark_workspace_size(0, 16, 129280, 7168) > 0
+    assert binding.dspark_workspace_size(-1, 16, 10, 10) == 0
+    assert binding.dspark_workspace_size(4, 0, 10, 10) == 0
+    assert binding.dspark_workspace_size(4, 65, 10, 10) == 0
+    assert binding.dspark_workspace_size(4, 8, 0, 10) == 0
+    a = binding.dspark_workspace_size(64, 16, 129280, 7168)
+    b = binding.dspark_workspace_size(128, 16, 129280, 7168)
+    assert b > a and a % 256 == 0 and b % 256 == 0
+
+
+FAKE = 1 << 20  # a 256-aligned non-null address; validation never dereferences it
+
+
+def valid_step(B=4, gamma=8, V=1024, d=256):
+    s = binding.DsparkStep()
+    s.B, s.gamma, s.V, s.d = B, gamma, V, d
+    s.logit_dtype = s.hidden_dtype = binding.DSPARK_BF16
+    for name, _ in binding.DsparkStep._fields_:
+        if isinstance(getattr(s, name), (int, type(None))) and name not in (
+                "B", "gamma", "V", "d", "logit_dtype", "hidden_dtype", "cap_T", "fixed_budget",
+                "seed", "workspace_bytes"):
+            setattr(s, name, FAKE)
+    s.cap_T = binding.DSPARK_NO_CAP
+    s.fixed_budget = binding.DSPARK_DYNAMIC
+    s.cost_c = 0.3
+    s.temperature = 1.0
+    s.workspace_bytes = binding.dspark_workspace_size(B, gamma, V, d)
+    return s
+
+
+CALLS = ["dspark_score_budget", "dspark_compact", "dspark_verify"]
+
+
+@pytest.mark.parametrize("call", CALLS)
+def test_null_step_and_bad_shapes(lib, call):
+    fn = getattr(lib, call)
+    assert fn(None, None) == binding.DSPARK_EINVAL
+    assert "NULL" in binding.last_error()
+    for field, val in [("B", -1), ("B", 65537), ("gamma", 0), ("gamma", 65), ("V", 0), ("d", 0)]:
+        s = valid_step()
+        setattr(s, field, val)
+        assert fn(ctypes.byref(s), None) == binding.DSPARK_EINVAL, (field, val)
+    s = valid_step()
+    s.logit_dtype = 7
+    assert fn(ctypes.byref(s), None) == binding.DSPARK_EDTYPE
+    s = valid_step()
+    s.hidden_dtype = -3
+    assert fn(ctypes.byref(s), None) == binding.DSPARK_EDTYPE
+
+
+@pytest.mark.parametrize("call", CALLS)
+def test_empty_batch_is_a_no_op(lib, call):
+    s = valid_step(B=0)
+    assert getattr(lib, call)(ctypes.byref(s), None) == binding.DSPARK_OK
+
+
+def test_score_budget_validation(lib):
+    f = lib.dspark_score_budget
+    s = valid_step(); s.L = None
+    assert f(ctypes.byref(s), None) == binding.DSPARK_EINVAL
+    s = valid_step(); s.hidden = None
+    assert f(ctypes.byref(s), None) == binding.DSPARK_EINVAL
+    s = valid_step(); s.fixed_budget = 5; s.cap_T = 10
+    assert f(ctypes.byref(s), None) == binding.DSPARK_EINVAL
+    assert "fixed budget" in binding.last_error()
+    s = valid_step(); s.cost_c = float("nan")
+    assert f(ctypes.byref(s), None) == binding.DSPARK_EINVAL
+    s = valid_step(); s.hidden = FAKE + 8
+    assert f(ctypes.byref(s), None) == binding.DSPARK_EALIGN
+    s = valid_step(d=4)  # 8 bytes per bf16 row
+    assert f(ctypes.byref(s), None) == binding.DSPARK_EALIGN
+    s = valid_step(); s.workspace = None
+    assert f(ctypes.byref(s), None) == binding.DSPARK_EWORKSPACE
+    s = valid_step(); s.workspace_bytes -= 256
+    assert f(ctypes.byref(s), None) == binding.DSPARK_EWORKSPACE
+    s = valid_step(); s.workspace = FAKE + 16
+    assert f(ctypes.byref(s), None) == binding.DSPARK_EWORKSPACE
+
+
+def test_compact_validation(lib):
+    for field in ("L", "row_off", "draft_tokens", "packed_ids", "packed_pos", "row_req", "row_k"):
+        s = valid_step()
+        setattr(s, field, None)
+        assert lib.dspark_compact(ctypes.byref(s), None) == binding.DSPARK_EINVAL, field
+
+
+def test_verify_validation(lib):
+    f = lib.dspark_verify
+    for field in ("draft_tokens", "target_logits", "draft_logits", "L", "draft_off", "row_off",
+                  "row_req", "row_k", "accept_len", "num_emitted", "out_tokens", "p_tok", "q_tok"):
+        s = valid_step()
+        setattr(s, field, None)
+        assert f(ctypes.byref(s), None) == binding.DSPARK_EINVAL, field
+    s = valid_step(); s.temperature = -1.0
+    assert f(ctypes.byref(s), None) == binding.DSPARK_EINVAL
+    s = valid_step(); s.temperature = float("inf")
+    assert f(ctypes.byref(s), None) == binding.DSPARK_EINVAL
+    s = valid_step(V=1001)  # bf16 row of 2002 bytes
+    assert f(ctypes.byref(s), None) == binding.DSPARK_EALIGN
+    s = valid_step(); s.target_logits = FAKE + 4
+    assert f(ctypes.byref(s), None) == binding.DSPARK_EALIGN
+    s = valid_step(); s.workspace_bytes = 16
+    assert f(ctypes.byref(s), None) == binding.DSPARK_EWORKSPACE
+
+
+def test_version(lib):
+    assert "sm_103a" in binding.version()

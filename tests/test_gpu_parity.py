@@ -1,0 +1,145 @@
+"""Parity of the CUDA step (through the C ABI) with the CPU oracle.
+
+Every integer output (L0, L, offsets, packed arrays, accept lengths, emitted
+tokens, committed lengths) must match exactly, apart from decisions the oracle
+flags as near ties; conf/survival within 1e-5 absolute; p(d), q(d) within
+1e-3 relative.  Workloads: the five synthetic configurations at full size,
+plus small shapes that span several vocab tiles with a ragged tail, and the
+method's degenerate cases.
+"""
+import numpy as np
+import pytest
+import torch
+
+from confidence_driven_speculative_gb300 import workloads as W
+from tests.gpu_harness import compare_with_oracle, gpu_step, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+def run_and_compare(inp_cpu, **kw):
+    gpu, bufs = gpu_step(to_device(inp_cpu))
+    stats = compare_with_oracle(W.to_numpy(inp_cpu), gpu, **kw)
+    return gpu, stats, bufs
+
+
+@pytest.mark.parametrize("Tm", [0.0, 1.0])
+def test_tiny_workload(cuda_lib, Tm):
+    for step in range(3):
+        run_and_compare(W.make_inputs(W.TINY, step, temperature=Tm))
+
+
+@pytest.mark.parametrize("T", [0, 1, 3, 7, 24, -1])
+@pytest.mark.parametrize("Tm", [0.0, 1.0])
+def test_tiny_cap_binding(cuda_lib, T, Tm):
+    inp = W.make_inputs(W.TINY, 5, temperature=Tm, cap_T=T, cost_c=0.05)
+    gpu, _, _ = run_and_compare(inp)
+    if T >= 0:
+        assert gpu["L"].sum() <= T
+
+
+@pytest.mark.parametrize("c", [-0.5, 0.0, 0.999, 1.0, 1.5])
+def test_cost_edges(cuda_lib, c):
+    inp = W.make_inputs(W.TINY, 1, cost_c=c, cap_T=-1)
+    gpu, _, _ = run_and_compare(inp)
+    if c <= 0:
+        assert np.all(gpu["L"] == 8)
+    if c >= 1.0:
+        assert np.all(gpu["L"] == 0)
+
+
+@pytest.mark.parametrize("F", [0, 3, 8, 20])
+def test_fixed_budget(cuda_lib, F):
+    inp = W.make_inputs(W.TINY, 2, cap_T=-1, fixed_budget=F)
+    gpu, _, _ = run_and_compare(inp)
+    assert np.all(gpu["L"] == min(F, 8))
+
+
+# Small shapes: several vocab tiles (16 KB each) with a ragged tail, odd B and
+# gamma, both dtypes, both modes.
+SHAPES = [
+    # (B, gamma, V, d, dtype)
+    (1, 1, 8, 8, "bf16"),
+    (3, 5, 8200, 40, "bf16"),      # 2 tiles, the second 16 bytes
+    (37, 7, 20000, 264, "bf16"),   # 3 tiles, ragged
+    (5, 16, 12292, 100, "f32"),    # 4 fp32 tiles, ragged
+    (300, 4, 520, 64, "bf16"),     # many requests, one tile each
+    (9, 64, 1000, 16, "bf16"),     # the largest gamma
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+@pytest.mark.parametrize("Tm", [0.0, 0.8])
+def test_small_shapes(cuda_lib, shape, Tm):
+    B, g, V, d, dt = shape
+    base = W.TINY if dt == "f32" else W.MIXED_B256
+    for step, (T, c) in enumerate([(-1, 0.3), (max(1, B * g // 3), 0.05)]):
+        inp = W.make_inputs(base, 10 + step, B=B, gamma=g, V=V, d=d, temperature=Tm,
+                            cap_T=T, cost_c=c)
+        run_and_compare(inp)
+
+
+def test_draft_equals_target_accepts_everything(cuda_lib):
+    inp = W.make_inputs(W.MIXED_B256, 3, B=16, V=20000, d=64, cap_T=-1, cost_c=0.0)
+    inp["draft_logits"] = inp["target_dense"][:, :-1].clone()
+    gpu, _, _ = run_and_compare(inp)
+    assert np.array_equal(gpu["accept_len"], gpu["L"])
+
+
+def test_out_of_range_drafts_are_rejected(cuda_lib):
+    for Tm in (0.0, 1.0):
+        inp = W.make_inputs(W.MIXED_B256, 4, B=8, V=4096, d=64, cap_T=-1, cost_c=0.0,
+                            temperature=Tm)
+        inp["draft_tokens"][:, 2] = torch.tensor([-1, 4096, 10**6, -7, 4096, 5000, -2, 9999],
+                                                 dtype=torch.int32)
+        gpu, _, _ = run_and_compare(inp)
+        assert np.all(gpu["accept_len"] <= 2)
+
+
+def test_repeated_calls_reuse_the_workspace(cuda_lib):
+    """Counters reset themselves: the same buffers give identical results on a
+    second and third run, and the device status stays clean."""
+    inp = to_device(W.make_inputs(W.MIXED_B256, 6, B=40, V=30000, d=128, cap_T=100))
+    first, bufs = gpu_step(inp)
+    for _ in range(2):
+        again, _ = gpu_step(inp, bufs=bufs)
+        for k in first:
+            if first[k] is not None:
+                assert np.array_equal(first[k], again[k]), k
+    assert bufs.device_status() == 0
+
+
+def test_empty_batch(cuda_lib):
+    from confidence_driven_speculative_gb300 import binding
+    step = binding.DsparkStep()
+    step.B, step.gamma, step.V, step.d = 0, 4, 16, 8
+    for fn in (binding.dspark_score_budget, binding.dspark_compact, binding.dspark_verify):
+        assert fn(step) == binding.DSPARK_OK
+
+
+def test_qwen3_8b_shape(cuda_lib):
+    for step in range(2):
+        run_and_compare(W.make_inputs(W.QWEN3_8B, step))
+
+
+def test_latency_b1(cuda_lib):
+    for step in range(3):
+        run_and_compare(W.make_inputs(W.LATENCY_B1, step))
+
+
+@pytest.mark.slow
+def test_mixed_b256_dynamic(cuda_lib):
+    for step in range(2):
+        _, stats, _ = run_and_compare(W.make_inputs(W.MIXED_B256, step))
+
+
+@pytest.mark.slow
+def test_mixed_b256_fixed_budget(cuda_lib):
+    gpu, _, _ = run_and_compare(W.make_inputs(W.MIXED_B256, 0, cap_T=-1, fixed_budget=5))
+    assert np.all(gpu["L"] == 5)
+
+
+@pytest.mark.slow
+def test_qwen3_14b_sweep(cuda_lib):
+    for step in range(2):
+        run_and_compare(W.make_inputs(W.QWEN3_14B_SWEEP, step))

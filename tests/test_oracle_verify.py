@@ -27,7 +27,7 @@ def test_greedy_worked_example():
     tgt = np.array(g["target"], np.float32)
     for case in g["cases"]:
         a, tok, _, _, tie = oracle.verify_request(3, case["drafts"], tgt, None, 0.0,
-                                                  np.zeros(4), np.zeros(4))
+                                                  np.zeros(4), np.zeros(4), np.zeros(4))
         assert (a, tok) == (case["a"], case["token"]), case
         assert tie == 0
 
@@ -39,10 +39,27 @@ def test_sampling_worked_examples():
         dft = np.array([np.log(case["q"])], np.float64) * Tm
         a, tok, p, q, _ = oracle.verify_request(1, [case["draft"]], tgt.astype(np.float32),
                                                 dft.astype(np.float32), Tm,
-                                                np.array(case["u"]), np.array(case["u2"]))
+                                                np.array(case["u"]), np.array(case["u_blk"]),
+                                                np.array(case["u_tok"]))
         assert (a, tok) == (case["a"], case["token"]), case["name"]
         np.testing.assert_allclose(p[0], case["p_tok"], atol=1e-6)
         np.testing.assert_allclose(q[0], case["q_tok"], atol=1e-6)
+
+
+def _runs(runs):
+    return np.concatenate([np.full(n, v, np.float64) for n, v in runs]).astype(np.float32)
+
+
+def test_two_level_draw_worked_examples():
+    for case in GOLDEN["verify_sampling"]["two_block_cases"]["cases"]:
+        p1 = _runs(case["p1_runs"])
+        row0 = np.zeros_like(p1)
+        tgt = np.stack([row0, p1])
+        a, tok, _, _, _ = oracle.verify_request(1, [5], tgt, row0[None], 1.0,
+                                                np.array([0.5, 0.0]),
+                                                np.array([0.0, case["u_blk"]]),
+                                                np.array([0.0, case["u_tok"]]))
+        assert (a, tok) == (1, case["token"]), case
 
 
 def _ragged(tgt_rows_per_req, L):
@@ -245,24 +262,27 @@ def test_inverse_cdf_uses_strict_crossing():
     V = 4
     zero = np.zeros(V, np.float32)                   # uniform: C = [.25, .5, .75, 1]
     tgt = np.stack([zero, zero])
-    for u2, want in [(0.0, 0), (0.25, 1), (0.5, 2), (0.75, 3), (0.99, 3)]:
+    for u3, want in [(0.0, 0), (0.25, 1), (0.5, 2), (0.75, 3), (0.99, 3)]:
         a, tok, _, _, _ = oracle.verify_request(1, [0], tgt, zero[None], 1.0,
-                                                np.array([0.0, 0.0]), np.array([0.0, u2]))
-        assert (a, tok) == (1, want), u2
+                                                np.array([0.0, 0.0]), np.array([0.0, 0.3]),
+                                                np.array([0.0, u3]))
+        assert (a, tok) == (1, want), u3
     # residual max(0, p - q) = [0, 0.4, 0, 0], u' = 0: the first positive weight
     p = np.array([0.1, 0.5, 0.2, 0.2])
     q = np.array([0.2, 0.1, 0.4, 0.3])
     tgt = np.stack([np.log(p), np.log(p)]).astype(np.float32)
     a, tok, _, _, _ = oracle.verify_request(1, [2], tgt, np.log(q)[None].astype(np.float32), 1.0,
-                                            np.array([0.9, 0.0]), np.array([0.0, 0.0]))
+                                            np.array([0.9, 0.0]), np.array([0.0, 0.0]),
+                                            np.array([0.0, 0.0]))
     assert (a, tok) == (0, 1)
 
 
 def test_uniforms_are_wired_to_philox_words():
     """Per slot b the accept test uses word 0 of Philox((b, k, 0, 0), (seed, 0))
-    and the resample uses word 1: r = 1/2 at every slot, so slot b accepts iff
-    u_b < 1/2; after a rejection the residual [0.3, 0, 0.1, 0] (Z = 0.4) gives
-    token 0 iff u'_b * 0.4 < 0.3."""
+    and the in-block draw uses word 2 (one block here, so word 1 plays no
+    part): r = 1/2 at every slot, so slot b accepts iff u_b < 1/2; after a
+    rejection the residual [0.3, 0, 0.1, 0] (mass 0.4) gives token 0 iff
+    u''_b * 0.4 < 0.3."""
     from tests.test_oracle_philox import numpy_block
     seed, n = 77, 300
     p = np.array([0.4, 0.1, 0.3, 0.2])
@@ -271,9 +291,9 @@ def test_uniforms_are_wired_to_philox_words():
     zq = np.log(q).astype(np.float32)
     out = _replicate(zp, zq, zp, np.ones(n, np.int32), n, seed)
     for b in range(n):
-        w0, w1 = numpy_block((b, 0, 0, 0), (seed, 0))[:2]
+        w0, _, w2 = numpy_block((b, 0, 0, 0), (seed, 0))[:3]
         u = int(w0 >> np.uint64(40)) / 2.0**24
-        u2 = int(w1 >> np.uint64(40)) / 2.0**24
+        u2 = int(w2 >> np.uint64(40)) / 2.0**24
         if abs(u - 0.5) < 1e-6:
             continue
         assert out["accept_len"][b] == (1 if u < 0.5 else 0), b
