@@ -163,7 +163,7 @@ dspark_status dspark_score_budget(const dspark_step *s, dspark_stream_t stream) 
     if ((st = device_info(&dev))) return st;
 
     const int nvec = int(size_t(s->d) * hs / 16);
-    int splits = (2 * dev->sms + s->B - 1) / s->B;
+    int splits = (4 * dev->sms + s->B - 1) / s->B;
     splits = std::min(splits, dspark::kMaxScoreSplits);
     splits = std::min(splits, std::max(1, nvec / 32));
     splits = std::max(splits, 1);
@@ -240,9 +240,13 @@ dspark_status dspark_verify(const dspark_step *s, dspark_stream_t stream) {
     const int bf = s->logit_dtype == DSPARK_BF16;
     dspark::VerifyArgs a{};
     a.B = s->B; a.gamma = s->gamma; a.V = s->V;
+    a.elem_bytes = int(ls);
     a.row_bytes = int(size_t(s->V) * ls);
     a.nc = (a.row_bytes + dspark::kChunkBytes - 1) / dspark::kChunkBytes;
     a.chunk_elems = int(dspark::kChunkBytes / ls);
+    a.nblk = lay.nblk;
+    a.nblk_stride = lay.nblk;
+    a.qcap = lay.qcap;
     a.greedy = greedy;
     a.scale = greedy ? 0.f : float(1.4426950408889634 / double(s->temperature));
     a.seed = s->seed;
@@ -253,13 +257,19 @@ dspark_status dspark_verify(const dspark_step *s, dspark_stream_t stream) {
     a.row_req = s->row_req; a.row_k = s->row_k;
     a.accept_len = s->accept_len; a.num_emitted = s->num_emitted; a.out_tokens = s->out_tokens;
     a.p_tok = s->p_tok; a.q_tok = s->q_tok; a.seq_lens_commit = s->seq_lens_commit;
-    a.part = ws_at<float4>(s, lay.part);
+    a.rec = ws_at<float4>(s, lay.rec);
     a.gath = ws_at<float2>(s, lay.gath);
+    a.zrec = ws_at<float>(s, lay.zrec);
+    a.dstate = ws_at<dspark::DecideState>(s, lay.dstate);
+    a.q_job = ws_at<int2>(s, lay.q_job);
+    a.q_ready = ws_at<int32_t>(s, lay.q_ready);
+    a.q_ctr = ws_at<int32_t>(s, lay.q_ctr);
     a.req_cnt = ws_at<int32_t>(s, lay.verify_cnt);
+    a.r1_cnt = ws_at<int32_t>(s, lay.r1_cnt);
     a.status = ws_at<int32_t>(s, lay.status);
-    const long long max_tasks = (long long)s->B * (s->gamma + 1) * a.nc;
-    const long long resident = (long long)dev->sms * dev->verify_blocks[bf];
-    const int grid = int(std::min(max_tasks, resident));
+    // One CTA per resident slot: the cooperative launch requires it, and the
+    // work is spread over the grid inside the kernel.
+    const int grid = dev->sms * dev->verify_blocks[bf];
     cudaError_t e = dspark::launch_verify(a, bf, grid, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "verify_kernel launch");
     return DSPARK_OK;

@@ -12,16 +12,27 @@ namespace dspark {
 // ---------------------------------------------------------------------------
 // Tuning constants.
 // ---------------------------------------------------------------------------
-constexpr int kThreads = 256;            // every kernel uses 256-thread CTAs
+constexpr int kThreads = 256;            // score / compact kernels: 256-thread CTAs
 constexpr int kWarps = kThreads / 32;
+constexpr int kConsumerWarps = 8;        // verify: consumer warps per CTA
+constexpr int kVerifyThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
 constexpr int kChunkBytes = 16384;       // one vocab tile of one row (verify)
 constexpr int kStages = 3;               // verify smem ring: kStages x (target + draft) tiles
 constexpr int kMaxScoreSplits = 32;      // d-splits per request in the score kernel
-constexpr int kSampleBlock = 8192;       // token ids per block of the two-level draw
-constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // bounded mbarrier wait: 2 s
+constexpr int kSampleBlock = 4096;       // token ids per block of the two-level draw
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // bounded waits: 2 s
 
 // Device status bits (workspace word 0).
-constexpr int32_t kStatusWaitTimeout = 1;
+constexpr int32_t kStatusWaitTimeout = 1;   // an mbarrier wait gave up
+constexpr int32_t kStatusQueueTimeout = 2;  // the verify job queue stalled
+
+// Per-request draw state written by the verify kernel's decide step.
+struct DecideState {
+    int a;                   // accepted drafts a_b
+    int mode;                // 0 bonus (p at row L_b), 1 residual, 2 p at row a_b
+    float Mp, Sp, Mq, Sq;    // normalisers of the drawn row (max, sum of 2^((z-max)s))
+    float u_blk, u_tok;      // the draw's two uniforms
+};
 
 // ---------------------------------------------------------------------------
 // Workspace layout (all offsets 256-byte aligned).
@@ -30,12 +41,19 @@ struct WorkspaceLayout {
     size_t status;        // int32
     size_t score_cnt;     // int32 [B]   per-request split counter
     size_t score_done;    // int32 [1]   requests finished
-    size_t verify_cnt;    // int32 [B]   per-request task counter
+    size_t verify_cnt;    // int32 [B]   per-request stream tiles done
+    size_t r1_cnt;        // int32 [B]   per-request residual tiles done
+    size_t q_ctr;         // int32 [8]   queue head, tail, finished, exited, epoch
     size_t dot_part;      // float [B * gamma * kMaxScoreSplits]
-    size_t part;          // float4 [B * (gamma+1) * NC]
-    size_t gath;          // float2 [B * (gamma+1)]
+    size_t rec;           // float4 [B * (gamma+1) * nblk]   per sampling-block records
+    size_t gath;          // float2 [B * (gamma+1)]          z_p[d], z_q[d]
+    size_t zrec;          // float [B * nblk]                residual block masses
+    size_t dstate;        // DecideState [B]
+    size_t q_job;         // int2 [qcap]
+    size_t q_ready;       // int32 [qcap]
     size_t total;
-    int nc_max;           // chunk slots per row reserved in `part`
+    int nblk;             // sampling blocks per row (record stride)
+    int qcap;             // queue capacity
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -43,18 +61,25 @@ __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_
 inline WorkspaceLayout workspace_layout(int B, int gamma, int V) {
     WorkspaceLayout w;
     const size_t rows = size_t(B) * size_t(gamma + 1);
-    // fp32 rows need the most chunks; size for that so one workspace serves both dtypes
+    // fp32 rows need the most tiles; size for that so one workspace serves both dtypes
     const int nc = int((size_t(V) * 4 + kChunkBytes - 1) / kChunkBytes);
+    w.nblk = (V + kSampleBlock - 1) / kSampleBlock;
+    w.qcap = B * (nc + 3);  // per request: decide, nc residual tiles, block choice, pick
     size_t off = 0;
     w.status = off;      off = align256(off + sizeof(int32_t));
     w.score_cnt = off;   off = align256(off + sizeof(int32_t) * size_t(B));
     w.score_done = off;  off = align256(off + sizeof(int32_t));
     w.verify_cnt = off;  off = align256(off + sizeof(int32_t) * size_t(B));
+    w.r1_cnt = off;      off = align256(off + sizeof(int32_t) * size_t(B));
+    w.q_ctr = off;       off = align256(off + sizeof(int32_t) * 8);
     w.dot_part = off;    off = align256(off + sizeof(float) * size_t(B) * gamma * kMaxScoreSplits);
-    w.part = off;        off = align256(off + 16 * rows * size_t(nc));
+    w.rec = off;         off = align256(off + 16 * rows * size_t(w.nblk));
     w.gath = off;        off = align256(off + 8 * rows);
+    w.zrec = off;        off = align256(off + sizeof(float) * size_t(B) * w.nblk);
+    w.dstate = off;      off = align256(off + sizeof(DecideState) * size_t(B));
+    w.q_job = off;       off = align256(off + 8 * size_t(w.qcap));
+    w.q_ready = off;     off = align256(off + 4 * size_t(w.qcap));
     w.total = off;
-    w.nc_max = nc;
     return w;
 }
 
@@ -260,9 +285,16 @@ struct CompactArgs {
 };
 
 struct VerifyArgs {
-    int B, gamma, V, nc, chunk_elems, row_bytes;
+    int B, gamma, V;
+    int nc;            // 16 KB tiles per row
+    int chunk_elems;   // tokens per tile
+    int elem_bytes;    // 2 (bf16) or 4 (fp32)
+    int row_bytes;     // V * elem_bytes
+    int nblk;          // sampling blocks per row
+    int nblk_stride;   // record stride per row (= nblk)
+    int qcap;          // job queue capacity
     int greedy;
-    float scale;  // log2(e) / Tm (sampling only)
+    float scale;       // log2(e) / Tm (sampling only)
     uint64_t seed;
     const int32_t *draft_tokens;
     const void *draft_logits, *target_logits;
@@ -270,9 +302,13 @@ struct VerifyArgs {
     int32_t *accept_len, *num_emitted, *out_tokens;
     float *p_tok, *q_tok;
     int32_t *seq_lens_commit;
-    float4 *part;
+    float4 *rec;
     float2 *gath;
-    int32_t *req_cnt, *status;
+    float *zrec;
+    DecideState *dstate;
+    int2 *q_job;
+    int32_t *q_ready, *q_ctr;
+    int32_t *req_cnt, *r1_cnt, *status;
 };
 
 cudaError_t launch_score_budget(const ScoreArgs &a, int grid, cudaStream_t s);

@@ -75,7 +75,10 @@ __device__ void write_offsets(int B, const int32_t *L, int32_t *draft_off, int32
 }
 
 // The cap, run by one CTA once every L0 and S of the batch is written.
+constexpr int kSmemKeys = 4096;  // candidate keys the cap stages in shared memory
+
 __device__ void budget_and_scan(const ScoreArgs &a) {
+    __shared__ unsigned keys[kSmemKeys];
     __shared__ int sh[kWarps + 1];
     __shared__ unsigned hist[256];
     __shared__ int sel[2];
@@ -92,6 +95,19 @@ __device__ void budget_and_scan(const ScoreArgs &a) {
         for (int b = tid; b < B; b += kThreads) a.L[b] = 0;
     } else {
         // Find the cap_T-th largest candidate key, 8 bits per pass from the top.
+        // Up to kSmemKeys candidate keys are staged in shared memory (one
+        // round of loads, non-candidates marked 0xffffffff); larger batches
+        // are re-read from L2 each pass.
+        const int nkeys = B * g;
+        const bool staged = nkeys <= kSmemKeys;
+        if (staged) {
+            for (int f = tid; f < nkeys; f += kThreads) {
+                const int b = f / g, k = f - b * g + 1;
+                const int l0 = __ldcg(&a.L0[b]);
+                const unsigned kv = __float_as_uint(__ldcg(&a.survival[f]));
+                keys[f] = k <= l0 ? kv : 0xffffffffu;
+            }
+        }
         unsigned prefix = 0, mask = 0;
         int need = a.cap_T;  // rank still to place within keys matching `prefix`
         for (int pass = 0; pass < 4; ++pass) {
@@ -102,11 +118,19 @@ __device__ void budget_and_scan(const ScoreArgs &a) {
                 sel[1] = need;
             }
             __syncthreads();
-            for (int f = tid; f < B * g; f += kThreads) {
-                const int b = f / g, k = f - b * g + 1;
-                if (k <= __ldcg(&a.L0[b])) {
-                    const unsigned key = __float_as_uint(__ldcg(&a.survival[f]));
-                    if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+            if (staged) {
+                for (int f = tid; f < nkeys; f += kThreads) {
+                    const unsigned kv = keys[f];
+                    if (kv != 0xffffffffu && (kv & mask) == prefix)
+                        atomicAdd(&hist[(kv >> shift) & 255u], 1u);
+                }
+            } else {
+                for (int f = tid; f < nkeys; f += kThreads) {
+                    const int b = f / g, k = f - b * g + 1;
+                    if (k <= __ldcg(&a.L0[b])) {
+                        const unsigned kv = __float_as_uint(__ldcg(&a.survival[f]));
+                        if ((kv & mask) == prefix) atomicAdd(&hist[(kv >> shift) & 255u], 1u);
+                    }
                 }
             }
             __syncthreads();
@@ -186,12 +210,13 @@ __global__ void __launch_bounds__(kThreads) score_budget_kernel(const ScoreArgs 
             static_cast<const char *>(a.hidden) + (size_t(b) * g + i) * size_t(a.d) * sizeof(T));
         float acc = 0.f;
         int v = v0 + lane;
-        for (; v + 96 < v1; v += 128) {
-            uint4 h[4];
+        // eight 16-byte loads in flight per lane
+        for (; v + 224 < v1; v += 256) {
+            uint4 h[8];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) h[u] = __ldcs(hv + v + 32 * u);
+            for (int u = 0; u < 8; ++u) h[u] = __ldcs(hv + v + 32 * u);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < 8; ++u) {
                 float x[VE];
                 Vec<T>::unpack(h[u], x);
 #pragma unroll

@@ -315,7 +315,7 @@ static void softmax_row(const void *row, int dtype, int V, double Tm, double *pr
 }
 
 /* Tokens per sampling block of the two-level draw (reading, see below). */
-#define ORC_SAMPLE_BLOCK 8192
+#define ORC_SAMPLE_BLOCK 4096
 
 /* Two-level inverse-CDF draw from nonnegative weights wt[0..V-1].
  * Reading taken (the pages do not fix how a token is drawn): ids are split
