@@ -245,8 +245,9 @@ dspark_status dspark_verify(const dspark_step *s, dspark_stream_t stream) {
     a.nc = (a.row_bytes + dspark::kChunkBytes - 1) / dspark::kChunkBytes;
     a.chunk_elems = int(dspark::kChunkBytes / ls);
     a.nblk = lay.nblk;
-    a.nblk_stride = lay.nblk;
+    a.grp_stride = lay.nc;
     a.qcap = lay.qcap;
+    a.qbcap = 2 * s->B;
     a.greedy = greedy;
     a.scale = greedy ? 0.f : float(1.4426950408889634 / double(s->temperature));
     a.seed = s->seed;
@@ -257,13 +258,16 @@ dspark_status dspark_verify(const dspark_step *s, dspark_stream_t stream) {
     a.row_req = s->row_req; a.row_k = s->row_k;
     a.accept_len = s->accept_len; a.num_emitted = s->num_emitted; a.out_tokens = s->out_tokens;
     a.p_tok = s->p_tok; a.q_tok = s->q_tok; a.seq_lens_commit = s->seq_lens_commit;
-    a.rec = ws_at<float4>(s, lay.rec);
+    a.rowrec = ws_at<float4>(s, lay.rowrec);
+    a.blkrec = ws_at<float2>(s, lay.blkrec);
+    a.zrec = ws_at<float2>(s, lay.zrec);
     a.gath = ws_at<float2>(s, lay.gath);
-    a.zrec = ws_at<float>(s, lay.zrec);
     a.dstate = ws_at<dspark::DecideState>(s, lay.dstate);
     a.q_job = ws_at<int2>(s, lay.q_job);
     a.q_ready = ws_at<int32_t>(s, lay.q_ready);
     a.q_ctr = ws_at<int32_t>(s, lay.q_ctr);
+    a.qb_job = ws_at<int32_t>(s, lay.qb_job);
+    a.qb_ready = ws_at<int32_t>(s, lay.qb_ready);
     a.req_cnt = ws_at<int32_t>(s, lay.verify_cnt);
     a.r1_cnt = ws_at<int32_t>(s, lay.r1_cnt);
     a.status = ws_at<int32_t>(s, lay.status);

@@ -15,7 +15,7 @@ namespace dspark {
 constexpr int kThreads = 256;            // score / compact kernels: 256-thread CTAs
 constexpr int kWarps = kThreads / 32;
 constexpr int kConsumerWarps = 8;        // verify: consumer warps per CTA
-constexpr int kVerifyThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
+constexpr int kVerifyThreads = (kConsumerWarps + 2) * 32;  // + producer and decider warps
 constexpr int kChunkBytes = 16384;       // one vocab tile of one row (verify)
 constexpr int kStages = 3;               // verify smem ring: kStages x (target + draft) tiles
 constexpr int kMaxScoreSplits = 32;      // d-splits per request in the score kernel
@@ -43,17 +43,21 @@ struct WorkspaceLayout {
     size_t score_done;    // int32 [1]   requests finished
     size_t verify_cnt;    // int32 [B]   per-request stream tiles done
     size_t r1_cnt;        // int32 [B]   per-request residual tiles done
-    size_t q_ctr;         // int32 [8]   queue head, tail, finished, exited, epoch
+    size_t q_ctr;         // int32 [8]   queue head, tail, finished, exited, epoch, chunk
     size_t dot_part;      // float [B * gamma * kMaxScoreSplits]
-    size_t rec;           // float4 [B * (gamma+1) * nblk]   per sampling-block records
-    size_t gath;          // float2 [B * (gamma+1)]          z_p[d], z_q[d]
-    size_t zrec;          // float [B * nblk]                residual block masses
+    size_t rowrec;        // float4 [B*(gamma+1) * nc * 8]  row partials per (row, chunk, warp)
+    size_t blkrec;        // float2 [B * nblk * 8]          bonus-row block partials per warp
+    size_t zrec;          // float2 [B * nblk * 8]          residual / p block masses per warp
+    size_t gath;          // float2 [B * (gamma+1)]         z_p[d], z_q[d]
     size_t dstate;        // DecideState [B]
-    size_t q_job;         // int2 [qcap]
+    size_t q_job;         // int2 [qcap]    residual-tile jobs (request, tile)
     size_t q_ready;       // int32 [qcap]
+    size_t qb_job;        // int32 [2B]     decider jobs (decide / finish residual)
+    size_t qb_ready;      // int32 [2B]
     size_t total;
-    int nblk;             // sampling blocks per row (record stride)
-    int qcap;             // queue capacity
+    int nblk;             // sampling blocks per row
+    int nc;               // 16 KB tiles per row (fp32, the larger count)
+    int qcap;             // residual-tile queue capacity
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -62,9 +66,10 @@ inline WorkspaceLayout workspace_layout(int B, int gamma, int V) {
     WorkspaceLayout w;
     const size_t rows = size_t(B) * size_t(gamma + 1);
     // fp32 rows need the most tiles; size for that so one workspace serves both dtypes
-    const int nc = int((size_t(V) * 4 + kChunkBytes - 1) / kChunkBytes);
+    w.nc = int((size_t(V) * 4 + kChunkBytes - 1) / kChunkBytes);
     w.nblk = (V + kSampleBlock - 1) / kSampleBlock;
-    w.qcap = B * (nc + 3);  // per request: decide, nc residual tiles, block choice, pick
+    w.qcap = B * w.nc;  // per request at most one residual pass of nc tiles
+    const size_t warps = kConsumerWarps;
     size_t off = 0;
     w.status = off;      off = align256(off + sizeof(int32_t));
     w.score_cnt = off;   off = align256(off + sizeof(int32_t) * size_t(B));
@@ -73,12 +78,15 @@ inline WorkspaceLayout workspace_layout(int B, int gamma, int V) {
     w.r1_cnt = off;      off = align256(off + sizeof(int32_t) * size_t(B));
     w.q_ctr = off;       off = align256(off + sizeof(int32_t) * 8);
     w.dot_part = off;    off = align256(off + sizeof(float) * size_t(B) * gamma * kMaxScoreSplits);
-    w.rec = off;         off = align256(off + 16 * rows * size_t(w.nblk));
+    w.rowrec = off;      off = align256(off + 16 * rows * size_t(w.nc) * warps);
+    w.blkrec = off;      off = align256(off + 8 * size_t(B) * w.nblk * warps);
+    w.zrec = off;        off = align256(off + 8 * size_t(B) * w.nblk * warps);
     w.gath = off;        off = align256(off + 8 * rows);
-    w.zrec = off;        off = align256(off + sizeof(float) * size_t(B) * w.nblk);
     w.dstate = off;      off = align256(off + sizeof(DecideState) * size_t(B));
     w.q_job = off;       off = align256(off + 8 * size_t(w.qcap));
     w.q_ready = off;     off = align256(off + 4 * size_t(w.qcap));
+    w.qb_job = off;      off = align256(off + 8 * size_t(B));
+    w.qb_ready = off;    off = align256(off + 8 * size_t(B));
     w.total = off;
     return w;
 }
@@ -241,6 +249,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking test of phase `parity` of `bar`.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(smem_addr(bar)), "r"(parity) : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -291,8 +310,9 @@ struct VerifyArgs {
     int elem_bytes;    // 2 (bf16) or 4 (fp32)
     int row_bytes;     // V * elem_bytes
     int nblk;          // sampling blocks per row
-    int nblk_stride;   // record stride per row (= nblk)
-    int qcap;          // job queue capacity
+    int grp_stride;    // chunk slots per row in rowrec
+    int qcap;          // residual-tile queue capacity
+    int qbcap;         // decider queue capacity
     int greedy;
     float scale;       // log2(e) / Tm (sampling only)
     uint64_t seed;
@@ -302,12 +322,12 @@ struct VerifyArgs {
     int32_t *accept_len, *num_emitted, *out_tokens;
     float *p_tok, *q_tok;
     int32_t *seq_lens_commit;
-    float4 *rec;
-    float2 *gath;
-    float *zrec;
+    float4 *rowrec;
+    float2 *blkrec, *zrec, *gath;
     DecideState *dstate;
     int2 *q_job;
     int32_t *q_ready, *q_ctr;
+    int32_t *qb_job, *qb_ready;
     int32_t *req_cnt, *r1_cnt, *status;
 };
 

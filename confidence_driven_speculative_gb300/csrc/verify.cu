@@ -14,32 +14,35 @@
 // Design (GB300).  The pass is HBM-bound: every packed target row (sum L + B)
 // and every kept draft row (sum L) is read once, V logits each.
 //
-//  * One persistent cooperative grid, 2 CTAs per SM.  Each CTA is one
-//    producer warp and 8 consumer warps.  The producer's lane 0 fills a
-//    3-stage shared-memory ring with 1-D bulk TMA copies (cp.async.bulk),
-//    each stage completing on a "full" mbarrier with a byte count; consumers
-//    release a stage on an "empty" mbarrier (one arrival per warp).  There is
-//    no block-wide barrier in the loop: warps only meet through mbarriers and
-//    a per-stage shared counter that elects the last warp of each stage.
-//  * Stream tasks: (packed row r, 16 KB vocab tile j).  Row r of request b
-//    at index k < L_b is a pair (target row r, draft row (b, k)); k = L_b is
-//    the bonus row.  Each CTA takes a contiguous range of stream tasks.  Each
-//    consumer warp folds its eighth of the tile into an online (max, sum) of
-//    2^(z * log2(e)/Tm) for p and q (greedy: max and lowest argmax); the
-//    stage's last warp merges the eight partials into one record per
-//    4096-token sampling block and counts the tile for its request.
-//  * The warp that counts a request's last tile decides it: accept tests
-//    (Philox uniforms), p(d)/q(d) outputs, and the draw of the emitted token
-//    in two levels, a 4096-id block by mass (u') then an id inside it (u'').
-//    A bonus draw takes block masses from the records and pushes one "pick"
-//    job; a residual draw pushes one "residual mass" job per tile of the
-//    rejecting row pair (read again while it is still in L2), and the last
-//    of those pushes the pick.  Jobs go to a device-wide queue that every
-//    producer serves before its own stream tasks, so this work is spread over
-//    the whole GPU and flows through the same TMA ring.
-//  * Every wait is bounded (mbarrier waits and queue polls give up after 2 s
-//    and set a status bit); counters reset themselves at the end of the
-//    launch, so the kernel can be replayed.
+//  * One persistent cooperative grid, 2 CTAs per SM; each CTA is one producer
+//    warp and 8 consumer warps.  The producer's lane 0 fills a 3-stage
+//    shared-memory ring with 1-D bulk TMA copies (cp.async.bulk) completing
+//    on "full" mbarriers with byte counts; each consumer warp releases a
+//    stage on its "empty" mbarrier.  No block-wide barrier in the loop.
+//  * Stream work is a queue of chunks -- whole packed rows (or single 16 KB
+//    tiles for small batches) -- handed out in row order by an atomic
+//    counter, so requests finish progressively while the grid streams.  Row
+//    r of request b at index k < L_b is a pair (target row, draft row
+//    (b, k)); k = L_b is the bonus row.
+//  * A consumer warp owns one eighth of every tile.  For a pair row its
+//    lanes keep online (max, sum of 2^(z log2(e)/Tm - max)) accumulators for
+//    p and q across all tiles of the chunk and reduce once, at the chunk's
+//    end, into the warp's own record slot (plain stores: deterministic).  A
+//    bonus row stores one slot per tile and warp, which gives the per-block
+//    masses of the draw.  Greedy rows keep (max, lowest argmax).
+//  * The producer books the stages it gets back: tiles are counted per
+//    request locally and published with one fenced atomic per request
+//    change; a completed request becomes a "decide" job on a device-wide
+//    queue that every producer serves before its own chunks.  Jobs: decide
+//    (accept tests with Philox uniforms, p(d)/q(d), the bonus block choice),
+//    residual mass (one tile of the rejecting row pair, read again while it
+//    is still in L2), block choice, and pick (one 4096-id block).  All flow
+//    through the same TMA ring, spread over the whole GPU.
+//  * Draws are two-level: a 4096-id block by mass (u'), then an id inside it
+//    (u''); in-block running sums are fp32 over short lane runs combined in
+//    fp64.
+//  * Every wait is bounded (2 s) and sets a status bit when it gives up;
+//    counters reset themselves at the end of the launch.
 #include <climits>
 
 #include "dspark_internal.cuh"
@@ -51,9 +54,12 @@ constexpr int kCW = kConsumerWarps;
 constexpr int kStageBytes = 2 * kChunkBytes;  // target tile + draft tile
 constexpr size_t kSmemBytes = size_t(kStages) * kStageBytes;
 
-enum : int { T_EXIT = 0, T_STREAM = 1, T_RESID = 2, T_PICK = 3, T_DECIDE = 4, T_RBLOCK = 5 };
+enum : int { T_EXIT = 0, T_STREAM = 1, T_RESID = 2 };
 enum : int { D_BONUS = 0, D_RESID = 1, D_FALLBACK = 2 };
-enum : int { Q_HEAD = 0, Q_TAIL = 1, Q_FINISHED = 2, Q_EXITED = 3, Q_EPOCH = 4 };
+// q_ctr words: residual-tile queue head / tail, finished requests, exited CTAs,
+// launch epoch, stream-chunk counter, decide queue head / tail.
+enum : int { QA_HEAD = 0, QA_TAIL = 1, Q_FINISHED = 2, Q_EXITED = 3, Q_EPOCH = 4, Q_CHUNK = 5,
+             QB_HEAD = 6, QB_TAIL = 7 };
 
 struct TaskInfo {
     int type;   // T_*
@@ -61,25 +67,33 @@ struct TaskInfo {
     int r;      // packed target row read by the stage
     int k;      // draft index of the draft row (pair) / of the drawn row
     int Lb;     // verify length of request b
-    int j;      // stream / residual: tile index; pick: sampling block index
+    int j;      // tile index
+    int g;      // stream: chunk slot of the row
     int y0;     // first token id of the stage
     int bytes;  // bytes per row in the stage
     int pair;   // a draft row sits in the second half of the stage
-    int d;      // drafted id of a stream pair (its gather target)
+    int d;      // stream pair: drafted id (its gather target)
+    int flush;  // stream: last tile of the chunk
 };
 
 struct VSmem {
     uint64_t full[kStages], empty[kStages];
     TaskInfo task[kStages];
-    float4 wpart[kStages][kCW];
-    double wd[kStages][kCW];
-    float2 gath[kStages];
-    int gflag[kStages];
-    int done[kStages];
+};
+
+// Grid-wide shape of the stream work, the same in every thread.  Rows
+// below nA are one chunk each; the remaining rows are cut into chunks of Cb
+// tiles (gprb per row) so the last wave of work balances finely.
+struct StreamShape {
+    int n_rows;    // packed rows
+    int nA;        // rows handed out whole
+    int Cb;        // tiles per chunk in the remaining rows
+    int gprb;      // chunks per remaining row
+    int n_chunks;
 };
 
 // ---------------------------------------------------------------------------
-// small memory-model helpers
+// small helpers
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ int ld_acquire(const int *p) {
     int v;
@@ -120,7 +134,27 @@ __device__ __forceinline__ int verify_len(const VerifyArgs &a, int b) {
     return min(max(a.L[b], 0), a.gamma);
 }
 
+__device__ __forceinline__ StreamShape stream_shape(const VerifyArgs &a) {
+    StreamShape sh;
+    // packed rows as written by the compaction, never more than its capacity
+    sh.n_rows = min(max(a.row_off[a.B], 0), a.B * (a.gamma + 1));
+    const long long n_tiles = (long long)sh.n_rows * a.nc;
+    if (n_tiles >= 32LL * gridDim.x) {
+        // many rows: whole rows, except the last gridDim.x rows in quarters
+        sh.nA = max(0, sh.n_rows - int(gridDim.x));
+        sh.Cb = max(1, a.nc / 4);
+    } else {
+        // few rows: single tiles
+        sh.nA = 0;
+        sh.Cb = 1;
+    }
+    sh.gprb = (a.nc + sh.Cb - 1) / sh.Cb;
+    sh.n_chunks = sh.nA + (sh.n_rows - sh.nA) * sh.gprb;
+    return sh;
+}
+
 // Fold one vector of logits into a running (max, sum of 2^((z - max) * s)).
+// The vector's terms are summed pairwise before joining the running sum.
 template <int VE>
 __device__ __forceinline__ void online_update(float &m, float &s, const float (&x)[VE],
                                               float scale) {
@@ -132,8 +166,14 @@ __device__ __forceinline__ void online_update(float &m, float &s, const float (&
         m = vm;
     }
     const float ms = m * scale;
+    float t[VE];
 #pragma unroll
-    for (int e = 0; e < VE; ++e) s += exp2_approx(fmaf(x[e], scale, -ms));
+    for (int e = 0; e < VE; ++e) t[e] = exp2_approx(fmaf(x[e], scale, -ms));
+#pragma unroll
+    for (int w = 1; w < VE; w <<= 1)
+#pragma unroll
+        for (int e = 0; e + w < VE; e += 2 * w) t[e] += t[e + w];
+    s += t[0];
 }
 
 // Inclusive warp scan in double (lane order).
@@ -146,90 +186,103 @@ __device__ __forceinline__ double warp_scan_incl(double v, int lane) {
     return v;
 }
 
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
 // ---------------------------------------------------------------------------
-// job queue
+// queues
 // ---------------------------------------------------------------------------
-__device__ void push_jobs(const VerifyArgs &a, int type, int b, int first, int count,
-                          int epoch) {
-    const int pos = atomicAdd(&a.q_ctr[Q_TAIL], count);
-    for (int i = 0; i < count; ++i)
-        if (pos + i < a.qcap) a.q_job[pos + i] = make_int2((type << 24) | b, first + i);
+// Residual-tile jobs (request b, tile c), served by every producer through
+// its TMA ring.
+__device__ void push_resid_jobs(const VerifyArgs &a, int b, int epoch) {
+    const int pos = atomicAdd(&a.q_ctr[QA_TAIL], a.nc);
+    for (int i = 0; i < a.nc; ++i)
+        if (pos + i < a.qcap) a.q_job[pos + i] = make_int2(b, i);
     __threadfence();
-    for (int i = 0; i < count; ++i)
+    for (int i = 0; i < a.nc; ++i)
         if (pos + i < a.qcap) st_release(&a.q_ready[pos + i], epoch);
 }
 
-// Turn a queued job into the stage it reads (decide jobs read nothing).
-__device__ TaskInfo decode_job(const VerifyArgs &a, int2 jb) {
+// Decider jobs, served by the decider warps: decide request b, or (with
+// kFinishResidual set) finish its residual draw.
+constexpr int kFinishResidual = 1 << 30;
+
+__device__ void push_decide(const VerifyArgs &a, int job, int epoch) {
+    const int pos = atomicAdd(&a.q_ctr[QB_TAIL], 1);
+    if (pos < a.qbcap) {
+        a.qb_job[pos] = job;
+        __threadfence();
+        st_release(&a.qb_ready[pos], epoch);
+    }
+}
+
+__device__ TaskInfo resid_task(const VerifyArgs &a, int2 jb) {
     TaskInfo t;
-    t.type = jb.x >> 24;
-    t.b = jb.x & 0xffffff;
+    t.type = T_RESID;
+    t.b = jb.x;
     t.j = jb.y;
     t.d = -1;
+    t.g = t.flush = 0;
     t.Lb = verify_len(a, t.b);
-    t.r = t.k = t.y0 = t.bytes = t.pair = 0;
-    if (t.type == T_DECIDE || t.type == T_RBLOCK) return t;
     const DecideState st = load_state(a, t.b);
-    const int r0 = a.row_off[t.b];
-    if (t.type == T_RESID) {
-        t.k = st.a;
-        t.r = r0 + st.a;
-        t.pair = 1;
-        t.y0 = t.j * a.chunk_elems;
-        t.bytes = min(kChunkBytes, a.row_bytes - t.j * kChunkBytes);
-    } else {
-        t.k = st.mode == D_BONUS ? t.Lb : st.a;
-        t.r = r0 + t.k;
-        t.pair = st.mode == D_RESID;
-        t.y0 = t.j * kSampleBlock;
-        t.bytes = min(kSampleBlock * a.elem_bytes, a.row_bytes - t.y0 * a.elem_bytes);
-    }
+    t.k = st.a;
+    t.r = a.row_off[t.b] + st.a;
+    t.pair = 1;
+    t.y0 = t.j * a.chunk_elems;
+    t.bytes = min(kChunkBytes, a.row_bytes - t.j * kChunkBytes);
     return t;
 }
 
-// Per-row metadata of the packed rows, fetched ahead of use.
-struct RowMeta {
-    int b, k, Lb, d;
+// ---------------------------------------------------------------------------
+// producer: lane 0 of warp kCW
+// ---------------------------------------------------------------------------
+// The next chunk, fetched over several fills so that its global loads
+// (counter, row ids, request metadata) never stall the issue of a tile.
+struct ChunkFetch {
+    int stage;  // 0: claim an index, 1: row ids, 2: request data, 3: ready, 4: none left
+    int c, r, g, b, k, Lb, d;
 };
 
-__device__ __forceinline__ void row_ids(const VerifyArgs &a, int r, int n_rows, int &b, int &k) {
-    b = r < n_rows ? a.row_req[r] : 0;
-    k = r < n_rows ? a.row_k[r] : 0;
+__device__ __forceinline__ void fetch_step(const VerifyArgs &a, const StreamShape &sh,
+                                           ChunkFetch &f) {
+    if (f.stage == 0) {
+        f.c = int(gridDim.x) + atomicAdd(&a.q_ctr[Q_CHUNK], 1);
+        f.stage = 1;
+    } else if (f.stage == 1) {
+        if (f.c >= sh.n_chunks) {
+            f.stage = 4;
+            return;
+        }
+        if (f.c < sh.nA) {
+            f.r = f.c;
+            f.g = 0;
+        } else {
+            const int cc = f.c - sh.nA;
+            f.r = sh.nA + cc / sh.gprb;
+            f.g = cc - (f.r - sh.nA) * sh.gprb;
+        }
+        f.b = a.row_req[f.r];
+        f.k = a.row_k[f.r];
+        f.stage = 2;
+    } else if (f.stage == 2) {
+        f.Lb = verify_len(a, f.b);
+        f.d = f.k < a.gamma ? a.draft_tokens[size_t(f.b) * a.gamma + f.k] : -1;
+        f.stage = 3;
+    }
 }
 
-__device__ __forceinline__ RowMeta row_meta(const VerifyArgs &a, int b, int k) {
-    RowMeta m;
-    m.b = b;
-    m.k = k;
-    m.Lb = verify_len(a, b);
-    m.d = k < a.gamma ? a.draft_tokens[size_t(b) * a.gamma + k] : -1;
-    return m;
-}
-
-__device__ __forceinline__ TaskInfo stream_task(const VerifyArgs &a, const RowMeta &m, int r,
-                                                int j) {
-    TaskInfo t;
-    t.type = T_STREAM;
-    t.r = r;
-    t.j = j;
-    t.b = m.b;
-    t.k = m.k;
-    t.Lb = m.Lb;
-    t.d = m.d;
-    t.pair = !a.greedy && m.k < m.Lb;
-    t.y0 = j * a.chunk_elems;
-    t.bytes = min(kChunkBytes, a.row_bytes - j * kChunkBytes);
-    return t;
-}
-
-// ---------------------------------------------------------------------------
-// producer: lane 0 of the last warp.  Besides feeding the ring it keeps the
-// books of the stages it gets back: stream tiles are counted per request
-// locally and added to the request's counter once per request change (one
-// fence and one atomic instead of one per tile); a request whose count
-// completes is pushed as a decide job, so no consumer ever stalls on a
-// device-wide fence or atomic while it holds a stage.
-// ---------------------------------------------------------------------------
+// Books of the stages the producer gets back: stream tiles are counted per
+// request locally and published with one fenced atomic per request change;
+// a request whose count completes goes to the decide queue.
 struct Books {
     int acc_b, acc_n, acc_total;
 };
@@ -238,22 +291,19 @@ __device__ void flush_books(const VerifyArgs &a, Books &bk, int epoch) {
     if (bk.acc_n == 0) return;
     __threadfence();
     const int old = atomicAdd(&a.req_cnt[bk.acc_b], bk.acc_n);
-    if (old + bk.acc_n == bk.acc_total) push_jobs(a, T_DECIDE, bk.acc_b, 0, 1, epoch);
+    if (old + bk.acc_n == bk.acc_total) push_decide(a, bk.acc_b, epoch);
     bk.acc_n = 0;
 }
 
-__device__ void account(const VerifyArgs &a, Books &bk, const TaskInfo &t, int epoch) {
-    if (t.type == T_STREAM) {
-        if (t.b != bk.acc_b) {
-            flush_books(a, bk, epoch);
-            bk.acc_b = t.b;
-            bk.acc_total = (t.Lb + 1) * a.nc;
-        }
-        ++bk.acc_n;
-    } else if (t.type == T_RESID) {
-        __threadfence();
-        if (atomicAdd(&a.r1_cnt[t.b], 1) == a.nc - 1) push_jobs(a, T_RBLOCK, t.b, 0, 1, epoch);
+__device__ __forceinline__ void account(const VerifyArgs &a, Books &bk, const TaskInfo &t,
+                                        int epoch) {
+    if (t.type != T_STREAM) return;
+    if (t.b != bk.acc_b) {
+        flush_books(a, bk, epoch);
+        bk.acc_b = t.b;
+        bk.acc_total = (t.Lb + 1) * a.nc;
     }
+    ++bk.acc_n;
 }
 
 // Wait for every fill below `upto` to come back from the consumers and book it.
@@ -270,65 +320,79 @@ __device__ bool reclaim(const VerifyArgs &a, VSmem &sm, Books &bk, int &booked, 
     return true;
 }
 
-__device__ void producer(const VerifyArgs &a, VSmem &sm, uint8_t *ring, long long s_lo,
-                         long long s_hi, int n_rows, int epoch) {
-    constexpr int kQueuePoll = 4;  // look at the queue every few stream tiles
-    long long s_next = s_lo;
-    // Row metadata pipeline: `cur` in use, `nxt` loaded, ids of the row after
-    // that in flight, so no global load latency sits between two tiles.
-    int r_cur = int(s_lo / a.nc), j_cur = int(s_lo - (long long)r_cur * a.nc);
-    RowMeta cur{}, nxt{};
-    int nb = 0, nk = 0;
-    if (s_lo < s_hi) {
-        int b, k;
-        row_ids(a, r_cur, n_rows, b, k);
-        cur = row_meta(a, b, k);
-        row_ids(a, r_cur + 1, n_rows, b, k);
-        nxt = row_meta(a, b, k);
-        row_ids(a, r_cur + 2, n_rows, nb, nk);
-    }
+__device__ void producer(const VerifyArgs &a, VSmem &sm, uint8_t *ring, const StreamShape &sh,
+                         int epoch) {
+    ChunkFetch nextc;
+    nextc.stage = 1;       // the first chunk is the CTA's own index; the counter
+    nextc.c = blockIdx.x;  // hands out the rest from gridDim.x on
+    int cr = 0, cg = 0, cb = 0, ck = 0, cLb = 0, cd = -1, cj = 0, cj_end = 0;
+    bool in_chunk = false;
     Books bk{-1, 0, 0};
     int booked = 0;
-    int pending = -1;  // a queue index this CTA has claimed but not yet seen filled
-    int since_poll = kQueuePoll;
+    // Residual-tile queue, polled one fill ahead: the values read at the end
+    // of a fill are used at the start of the next.
+    int pending = -1;      // a claimed queue index
+    int pend_rdy = 0;      // its ready word, read during the previous fill
+    int2 pend_job = make_int2(0, 0);
+    int obs_head = 0, obs_tail = 0;
     for (int fill = 0;; ++fill) {
         TaskInfo t;
         t.type = T_EXIT;
         bool have = false, ok = true;
-        if (since_poll >= kQueuePoll || s_next >= s_hi) {
-            since_poll = 0;
-            if (pending < 0 && ld_relaxed(&a.q_ctr[Q_HEAD]) < ld_relaxed(&a.q_ctr[Q_TAIL]))
-                pending = atomicAdd(&a.q_ctr[Q_HEAD], 1);
-            if (pending >= 0 && pending < a.qcap && ld_acquire(&a.q_ready[pending]) == epoch) {
-                t = decode_job(a, __ldcg(a.q_job + pending));
-                pending = -1;
-                have = true;
-            }
-        }
-        if (!have && s_next < s_hi) {
-            t = stream_task(a, cur, r_cur, j_cur);
+        // 1. residual tiles first
+        if (pending >= 0 && pend_rdy == epoch) {
+            t = resid_task(a, pend_job);
+            pending = -1;
             have = true;
-            ++s_next;
-            ++since_poll;
-            if (++j_cur == a.nc) {
-                j_cur = 0;
-                ++r_cur;
-                cur = nxt;
-                nxt = row_meta(a, nb, nk);
-                row_ids(a, r_cur + 2, n_rows, nb, nk);
+        } else if (pending < 0 && obs_head < obs_tail) {
+            pending = atomicAdd(&a.q_ctr[QA_HEAD], 1);
+            pend_rdy = 0;
+        }
+        // 2. then the stream chunks
+        if (!have && !in_chunk) {
+            while (nextc.stage < 3) fetch_step(a, sh, nextc);
+            if (nextc.stage == 3) {
+                cr = nextc.r;
+                cg = nextc.g;
+                cb = nextc.b;
+                ck = nextc.k;
+                cLb = nextc.Lb;
+                cd = nextc.d;
+                const int C = cr < sh.nA ? a.nc : sh.Cb;
+                cj = cg * C;
+                cj_end = min(a.nc, cj + C);
+                in_chunk = true;
+                nextc.stage = 0;
             }
         }
+        if (!have && in_chunk) {
+            t.type = T_STREAM;
+            t.r = cr;
+            t.g = cg;
+            t.b = cb;
+            t.k = ck;
+            t.Lb = cLb;
+            t.d = cd;
+            t.j = cj;
+            t.pair = !a.greedy && ck < cLb;
+            t.y0 = cj * a.chunk_elems;
+            t.bytes = min(kChunkBytes, a.row_bytes - cj * kChunkBytes);
+            t.flush = cj + 1 == cj_end;
+            if (++cj == cj_end) in_chunk = false;
+            have = true;
+        }
+        if (nextc.stage < 3) fetch_step(a, sh, nextc);  // keep the next chunk coming
+        // 3. nothing of our own left: book everything, then serve the
+        //    residual queue until every request has finished
         if (!have) {
-            // Own tiles are done: book everything in flight, then serve the
-            // queue until every request has finished.
             ok = reclaim(a, sm, bk, booked, fill, epoch);
             flush_books(a, bk, epoch);
-            if (pending < 0) pending = atomicAdd(&a.q_ctr[Q_HEAD], 1);
+            if (pending < 0) pending = atomicAdd(&a.q_ctr[QA_HEAD], 1);
             const uint64_t t0 = global_timer_ns();
-            unsigned ns = 64;
+            unsigned ns = 32;
             while (ok) {
                 if (pending < a.qcap && ld_acquire(&a.q_ready[pending]) == epoch) {
-                    t = decode_job(a, __ldcg(a.q_job + pending));
+                    t = resid_task(a, __ldcg(a.q_job + pending));
                     pending = -1;
                     have = true;
                     break;
@@ -339,17 +403,17 @@ __device__ void producer(const VerifyArgs &a, VSmem &sm, uint8_t *ring, long lon
                     break;
                 }
                 __nanosleep(ns);
-                ns = min(ns * 2, 2048u);
+                ns = min(ns * 2, 256u);
             }
         }
+        // 4. take the stage back (booking what it held) and fill it
         const int s = fill % kStages;
         if (ok) ok = reclaim(a, sm, bk, booked, fill - kStages + 1, epoch);
         if (!have || !ok) t.type = T_EXIT;
         sm.task[s] = t;
-        if (t.type == T_EXIT || t.bytes == 0) {
-            mbar_arrive(&sm.full[s]);  // a stage without data
-            if (t.type == T_EXIT) return;
-            continue;
+        if (t.type == T_EXIT) {
+            mbar_arrive(&sm.full[s]);
+            return;
         }
         uint8_t *dst = ring + s * kStageBytes;
         uint64_t *bar = &sm.full[s];
@@ -363,11 +427,23 @@ __device__ void producer(const VerifyArgs &a, VSmem &sm, uint8_t *ring, long lon
                                size_t(t.y0) * a.elem_bytes;
             bulk_g2s(dst + kChunkBytes, dsrc, uint32_t(t.bytes), bar);
         }
+        // 5. book whatever has already come back, without waiting
+        while (booked < fill && mbar_test_wait(&sm.empty[booked % kStages], (booked / kStages) & 1)) {
+            account(a, bk, sm.task[booked % kStages], epoch);
+            ++booked;
+        }
+        // 6. look at the residual queue for the next fill
+        obs_head = ld_relaxed(&a.q_ctr[QA_HEAD]);
+        obs_tail = ld_relaxed(&a.q_ctr[QA_TAIL]);
+        if (pending >= 0 && pending < a.qcap) {
+            pend_rdy = ld_acquire(&a.q_ready[pending]);
+            pend_job = __ldcg(a.q_job + pending);
+        }
     }
 }
 
 // ---------------------------------------------------------------------------
-// request completion (warp-level)
+// decisions (warp-level)
 // ---------------------------------------------------------------------------
 __device__ void finish_request(const VerifyArgs &a, int b, int acc, int token, int lane) {
     const int g1 = a.gamma + 1;
@@ -391,14 +467,13 @@ __device__ void finish_request(const VerifyArgs &a, int b, int acc, int token, i
 
 // Choose a sampling block: the smallest i whose running mass exceeds
 // u * total; the last block with positive mass if rounding leaves no
-// crossing.  Warp-level; mass(i) is evaluated by the lane that owns i.
+// crossing.  mass(i) is evaluated by the lane that owns i.
 template <typename F>
 __device__ int choose_block(int nblk, float u, F mass, int lane) {
     double total = 0.0;
     for (int t0 = 0; t0 < nblk; t0 += 32) {
         const int i = t0 + lane;
-        const double incl = warp_scan_incl(i < nblk ? double(mass(i)) : 0.0, lane);
-        total += __shfl_sync(0xffffffffu, incl, 31);
+        total += warp_sum_d(i < nblk ? double(mass(i)) : 0.0);
     }
     const double target = double(u) * total;
     double run = 0.0;
@@ -416,70 +491,216 @@ __device__ int choose_block(int nblk, float u, F mass, int lane) {
     return last_pos;
 }
 
-// Decide request b once all its stream tiles are in (warp-level).
-__device__ void decide_request(const VerifyArgs &a, int b, int epoch, int lane) {
+// Draw weights of the VE elements of 16-byte vector v: 2^((z - Mp) s) for a
+// draw from p (bonus, fallback); max(0, p - q) for the residual.
+template <typename T>
+__device__ __forceinline__ void draw_weights(const uint4 *tv, const uint4 *dv, int v, int mode,
+                                             float Mp, float iSp, float Mq, float iSq,
+                                             float scale, float (&w)[Vec<T>::kElems]) {
+    constexpr int VE = Vec<T>::kElems;
+    float x[VE];
+    Vec<T>::unpack(__ldcg(tv + v), x);
+    if (mode == D_RESID) {
+        float y[VE];
+        Vec<T>::unpack(__ldcg(dv + v), y);
+#pragma unroll
+        for (int e = 0; e < VE; ++e)
+            w[e] = fmaxf(0.f, exp2_approx((x[e] - Mp) * scale) * iSp -
+                                  exp2_approx((y[e] - Mq) * scale) * iSq);
+    } else {
+#pragma unroll
+        for (int e = 0; e < VE; ++e) w[e] = exp2_approx((x[e] - Mp) * scale);
+    }
+}
+
+template <int VE>
+__device__ __forceinline__ float pair_sum(const float (&w)[VE]) {
+    float t[VE];
+#pragma unroll
+    for (int e = 0; e < VE; ++e) t[e] = w[e];
+#pragma unroll
+    for (int s = 1; s < VE; s <<= 1)
+#pragma unroll
+        for (int e = 0; e + s < VE; e += 2 * s) t[e] += t[e + s];
+    return t[0];
+}
+
+// The token inside sampling block `blk` of the drawn row(s): the smallest id
+// whose running in-block weight exceeds u_tok times the block's weight.
+// Each lane owns a contiguous run of 128 ids (kRunVec 16-byte vectors),
+// loaded four vectors at a time; per-vector weights are summed pairwise and
+// kept in registers, runs are combined in fp64, and the lane holding the
+// crossing finds its vector from the kept sums (same fp32 association) and
+// reloads only that vector.  The rows were streamed moments earlier, so the
+// loads hit L2.
+template <typename T>
+__device__ int inline_pick(const VerifyArgs &a, const DecideState &st, int b, int blk, int lane) {
+    constexpr int VE = Vec<T>::kElems;
+    constexpr int kRunVec = kSampleBlock / 32 / VE;  // vectors per lane run
+    const int r = a.row_off[b] + (st.mode == D_BONUS ? verify_len(a, b) : st.a);
+    const uint4 *tv = reinterpret_cast<const uint4 *>(static_cast<const char *>(a.target_logits) +
+                                                      size_t(r) * a.row_bytes);
+    const uint4 *dv = reinterpret_cast<const uint4 *>(
+        static_cast<const char *>(a.draft_logits) + (size_t(b) * a.gamma + st.a) * a.row_bytes);
+    const int nvec_row = a.row_bytes / 16;
+    const float scale = a.scale, iSp = 1.f / st.Sp, iSq = 1.f / st.Sq;
+    const bool resid = st.mode == D_RESID;
+    const int v0 = blk * (kSampleBlock / VE) + lane * kRunVec;
+    auto weights = [&](const uint4 &xv, const uint4 &yv, float (&w)[VE]) {
+        float x[VE];
+        Vec<T>::unpack(xv, x);
+        if (resid) {
+            float y[VE];
+            Vec<T>::unpack(yv, y);
+#pragma unroll
+            for (int e = 0; e < VE; ++e)
+                w[e] = fmaxf(0.f, exp2_approx((x[e] - st.Mp) * scale) * iSp -
+                                      exp2_approx((y[e] - st.Mq) * scale) * iSq);
+        } else {
+#pragma unroll
+            for (int e = 0; e < VE; ++e) w[e] = exp2_approx((x[e] - st.Mp) * scale);
+        }
+    };
+    constexpr int kBatch = 4;
+    float vs[kRunVec];
+#pragma unroll
+    for (int q0 = 0; q0 < kRunVec; q0 += kBatch) {
+        uint4 xv[kBatch], yv[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int v = v0 + q0 + u;
+            const bool in = v < nvec_row;
+            xv[u] = in ? __ldcg(tv + v) : make_uint4(0, 0, 0, 0);
+            yv[u] = in && resid ? __ldcg(dv + v) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            float w[VE];
+            weights(xv[u], yv[u], w);
+            vs[q0 + u] = v0 + q0 + u < nvec_row ? pair_sum<VE>(w) : 0.f;
+        }
+    }
+    float ls = 0.f;
+#pragma unroll
+    for (int q = 0; q < kRunVec; ++q) ls += vs[q];
+    const double incl = warp_scan_incl(double(ls), lane);
+    const double total = __shfl_sync(0xffffffffu, incl, 31);
+    const double target = double(st.u_tok) * total;
+    const double prev = __shfl_up_sync(0xffffffffu, incl, 1);
+    const double excl = lane > 0 ? prev : 0.0;
+    const unsigned hit = __ballot_sync(0xffffffffu, ls > 0.f && incl > target);
+    const unsigned pos = __ballot_sync(0xffffffffu, ls > 0.f);
+    const int lsel = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : -1);
+    if (lsel < 0) return blk * kSampleBlock;  // a block without weight (not drawn in practice)
+    int pick = -1;
+    if (lane == lsel) {
+        // the vector that crosses, from the kept sums (the last positive one
+        // if rounding leaves no crossing)
+        float run = 0.f, run_at = 0.f;
+        int qsel = -1, qlast = -1;
+#pragma unroll
+        for (int q = 0; q < kRunVec; ++q) {
+            if (qsel < 0 && vs[q] > 0.f) {
+                qlast = q;
+                run_at = run;
+                if (excl + double(run + vs[q]) > target) qsel = q;
+            }
+            run += vs[q];
+        }
+        if (qsel < 0) qsel = qlast;
+        if (qsel >= 0) {
+            const int v = v0 + qsel;
+            float w[VE];
+            weights(__ldcg(tv + v), resid ? __ldcg(dv + v) : make_uint4(0, 0, 0, 0), w);
+            float re = run_at;
+            int lastpos = -1;
+#pragma unroll
+            for (int e = 0; e < VE; ++e) {
+                re += w[e];
+                if (pick < 0 && w[e] > 0.f) {
+                    lastpos = v * VE + e;
+                    if (excl + double(re) > target) pick = v * VE + e;
+                }
+            }
+            if (pick < 0) pick = lastpos;
+        }
+        if (pick < 0) pick = v0 * VE;
+    }
+    return __shfl_sync(0xffffffffu, pick, lsel);
+}
+
+// Fold the record slots of packed row r (chunk slots x warps, fixed order).
+__device__ __forceinline__ float4 fold_row(const VerifyArgs &a, const StreamShape &sh, int r,
+                                           float scale) {
+    const float4 *rec = a.rowrec + size_t(r) * a.grp_stride * kCW;
+    const int n = (r < sh.nA ? 1 : sh.gprb) * kCW;
+    float4 acc = a.greedy ? make_float4(-INFINITY, __int_as_float(INT_MAX), 0.f, 0.f)
+                          : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
+    for (int i0 = 0; i0 < n; i0 += 8) {
+        float4 x[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) x[u] = i0 + u < n ? __ldcg(rec + i0 + u) : acc;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            if (i0 + u >= n) continue;
+            if (a.greedy) {
+                int bi = __float_as_int(acc.y);
+                am_combine(acc.x, bi, x[u].x, __float_as_int(x[u].y));
+                acc.y = __int_as_float(bi);
+            } else {
+                ms_combine(acc.x, acc.y, x[u].x, x[u].y, scale);
+                ms_combine(acc.z, acc.w, x[u].z, x[u].w, scale);
+            }
+        }
+    }
+    return acc;
+}
+
+// (max, sum) of p over sampling block i of request b's bonus row, from the
+// per-warp slots.
+__device__ __forceinline__ float2 bonus_block(const VerifyArgs &a, int b, int i, int wpb,
+                                              float scale) {
+    const float2 *sl = a.blkrec + (size_t(b) * a.nblk + i) * kCW;
+    float2 x[kCW];
+#pragma unroll
+    for (int w = 0; w < kCW; ++w) x[w] = w < wpb ? __ldcg(sl + w) : make_float2(-INFINITY, 0.f);
+    float m = -INFINITY, s = 0.f;
+#pragma unroll
+    for (int w = 0; w < kCW; ++w) ms_combine(m, s, x[w].x, x[w].y, scale);
+    return make_float2(m, s);
+}
+
+// Request b's stream tiles are all in: accept tests, outputs of the draft
+// rows, and either the whole bonus draw or the residual jobs.
+template <typename T>
+__device__ void decide_request(const VerifyArgs &a, const StreamShape &sh, int b, int wpb,
+                               int epoch, int lane) {
     const int Lb = verify_len(a, b), r0 = a.row_off[b], d0 = a.draft_off[b];
-    const int nb = a.nblk;
     const float scale = a.scale;
     int ab = Lb;                                   // first rejected draft (L_b: none)
     float Mp = 0.f, Sp = 0.f, Mq = 0.f, Sq = 0.f;  // normalisers of row a_b (sampling)
-    float Mbonus = 0.f;
     int g_tok = 0;
-    // One lane per row k (two rounds when gamma >= 32); each lane folds the
-    // row's block records, loads issued eight at a time.
+    // One lane per row k (two rounds when gamma >= 32).  In sampling mode
+    // the bonus row has no row record; it is drawn from its block slots.
     for (int base = 0; base <= Lb; base += 32) {
         const int k = base + lane;
-        const bool live = k <= Lb;
-        const float4 *rec = a.rec + size_t(r0 + (live ? k : 0)) * a.nblk_stride;
+        const bool live = a.greedy ? k <= Lb : k < Lb;
+        float4 rr = make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
         bool accept = false;
-        if (a.greedy) {
-            float bv = -INFINITY;
-            int bi = INT_MAX;
-            if (live) {
-                for (int i0 = 0; i0 < nb; i0 += 8) {
-                    float4 x[8];
-#pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        x[u] = i0 + u < nb ? __ldcg(rec + i0 + u)
-                                           : make_float4(-INFINITY, __int_as_float(INT_MAX), 0.f, 0.f);
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) am_combine(bv, bi, x[u].x, __float_as_int(x[u].y));
-                }
-                if (k < Lb) {
-                    accept = a.draft_tokens[size_t(b) * a.gamma + k] == bi;
+        if (live) {
+            rr = fold_row(a, sh, r0 + k, scale);
+            if (k < Lb) {
+                const int dt = a.draft_tokens[size_t(b) * a.gamma + k];
+                if (a.greedy) {
+                    accept = dt == __float_as_int(rr.y);
                     a.p_tok[d0 + k] = 0.f;
                     a.q_tok[d0 + k] = 0.f;
-                }
-            }
-            const unsigned acc = __ballot_sync(0xffffffffu, live && k < Lb && accept);
-            const unsigned rows = __ballot_sync(0xffffffffu, live && k < Lb);
-            const unsigned rej = rows & ~acc;
-            if (ab == Lb && rej) ab = base + __ffs(rej) - 1;
-            const int src = ab - base;
-            const int g = __shfl_sync(0xffffffffu, bi, src >= 0 && src < 32 ? src : 0);
-            if (src >= 0 && src < 32) g_tok = g;
-        } else {
-            float mp = -INFINITY, sp = 0.f, mq = -INFINITY, sq = 0.f;
-            if (live) {
-                for (int i0 = 0; i0 < nb; i0 += 8) {
-                    float4 x[8];
-#pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        x[u] = i0 + u < nb ? __ldcg(rec + i0 + u)
-                                           : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        ms_combine(mp, sp, x[u].x, x[u].y, scale);
-                        ms_combine(mq, sq, x[u].z, x[u].w, scale);
-                    }
-                }
-                if (k < Lb) {
-                    const int dt = a.draft_tokens[size_t(b) * a.gamma + k];
+                } else {
                     float p = 0.f, q = 0.f, ratio = 0.f;
                     if (dt >= 0 && dt < a.V) {
                         const float2 z = __ldcg(a.gath + r0 + k);
-                        p = exp2_approx((z.x - mp) * scale) / sp;
-                        q = exp2_approx((z.y - mq) * scale) / sq;
+                        p = exp2_approx((z.x - rr.x) * scale) / rr.y;
+                        q = exp2_approx((z.y - rr.z) * scale) / rr.w;
                         ratio = q > 0.f ? fminf(1.f, p / q) : 1.f;
                     }
                     float u, ub, ut;
@@ -489,23 +710,21 @@ __device__ void decide_request(const VerifyArgs &a, int b, int epoch, int lane) 
                     a.q_tok[d0 + k] = q;
                 }
             }
-            const unsigned acc = __ballot_sync(0xffffffffu, live && k < Lb && accept);
-            const unsigned rows = __ballot_sync(0xffffffffu, live && k < Lb);
-            const unsigned rej = rows & ~acc;
-            if (ab == Lb && rej) ab = base + __ffs(rej) - 1;
-            const int src = ab - base;
-            const int sl = src >= 0 && src < 32 ? src : 0;
-            const float m1 = __shfl_sync(0xffffffffu, mp, sl), s1 = __shfl_sync(0xffffffffu, sp, sl);
-            const float m2 = __shfl_sync(0xffffffffu, mq, sl), s2 = __shfl_sync(0xffffffffu, sq, sl);
-            if (src >= 0 && src < 32) {
-                Mp = m1;
-                Sp = s1;
-                Mq = m2;
-                Sq = s2;
-            }
-            const int bsrc = Lb - base;
-            const float mb = __shfl_sync(0xffffffffu, mp, bsrc >= 0 && bsrc < 32 ? bsrc : 0);
-            if (bsrc >= 0 && bsrc < 32) Mbonus = mb;
+        }
+        const unsigned acc = __ballot_sync(0xffffffffu, live && k < Lb && accept);
+        const unsigned rows = __ballot_sync(0xffffffffu, live && k < Lb);
+        const unsigned rej = rows & ~acc;
+        if (ab == Lb && rej) ab = base + __ffs(rej) - 1;
+        const int src = ab - base;
+        const int sl = src >= 0 && src < 32 ? src : 0;
+        const float m1 = __shfl_sync(0xffffffffu, rr.x, sl), s1 = __shfl_sync(0xffffffffu, rr.y, sl);
+        const float m2 = __shfl_sync(0xffffffffu, rr.z, sl), s2 = __shfl_sync(0xffffffffu, rr.w, sl);
+        if (src >= 0 && src < 32) {
+            Mp = m1;
+            Sp = s1;
+            Mq = m2;
+            Sq = s2;
+            g_tok = __float_as_int(s1);  // greedy: the row's argmax
         }
     }
     if (a.greedy) {
@@ -519,22 +738,43 @@ __device__ void decide_request(const VerifyArgs &a, int b, int epoch, int lane) 
     st.u_blk = ub;
     st.u_tok = ut;
     if (ab == Lb) {
-        // Bonus draw from p of row L_b: block masses from the tile records.
-        const float4 *rec = a.rec + size_t(r0 + Lb) * a.nblk_stride;
+        // Bonus draw from p of row L_b, done here: block masses from its
+        // slots, then the token inside the chosen block.
+        constexpr int kCache = 4;  // blocks per lane kept in registers
+        float2 bm[kCache];
+        float mb = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < kCache; ++q) {
+            const int i = q * 32 + lane;
+            bm[q] = i < a.nblk ? bonus_block(a, b, i, wpb, scale) : make_float2(-INFINITY, 0.f);
+            if (bm[q].y > 0.f) mb = fmaxf(mb, bm[q].x);
+        }
+        for (int i = kCache * 32 + lane; i < a.nblk; i += 32) {
+            const float2 x = bonus_block(a, b, i, wpb, scale);
+            if (x.y > 0.f) mb = fmaxf(mb, x.x);
+        }
+        const float M = warp_max(mb);
         auto mass = [&](int i) {
-            const float4 x = __ldcg(rec + i);
-            return x.y > 0.f ? x.y * exp2_approx((x.x - Mbonus) * scale) : 0.f;
+            const int q = i >> 5;
+            float2 x;
+            if (q < kCache) {
+                x = bm[0];
+#pragma unroll
+                for (int c = 1; c < kCache; ++c)
+                    if (q == c) x = bm[c];
+            } else {
+                x = bonus_block(a, b, i, wpb, scale);
+            }
+            return x.y > 0.f ? x.y * exp2_approx((x.x - M) * scale) : 0.f;
         };
-        const int blk = choose_block(nb, ub, mass, lane);
+        const int blk = choose_block(a.nblk, ub, mass, lane);
         st.mode = D_BONUS;
-        st.Mp = Mbonus;
+        st.Mp = M;
         st.Sp = 1.f;
         st.Mq = 0.f;
         st.Sq = 1.f;
-        if (lane == 0) {
-            a.dstate[b] = st;
-            push_jobs(a, T_PICK, b, blk, 1, epoch);
-        }
+        const int token = inline_pick<T>(a, st, b, blk, lane);
+        finish_request(a, b, ab, token, lane);
     } else {
         st.mode = D_RESID;
         st.Mp = Mp;
@@ -543,147 +783,59 @@ __device__ void decide_request(const VerifyArgs &a, int b, int epoch, int lane) 
         st.Sq = Sq;
         if (lane == 0) {
             a.dstate[b] = st;
-            push_jobs(a, T_RESID, b, 0, a.nc, epoch);
+            push_resid_jobs(a, b, epoch);
         }
     }
 }
 
-// All residual-mass tiles of request b are in: choose the block (warp-level).
-__device__ void decide_residual_block(const VerifyArgs &a, int b, int epoch, int lane) {
+// Every residual slot of request b is in: choose the block from the masses
+// and draw the token inside it.
+template <typename T>
+__device__ void finish_residual(const VerifyArgs &a, int b, int wpb, int lane) {
     DecideState st = load_state(a, b);
-    const float *z = a.zrec + size_t(b) * a.nblk_stride;
+    const float2 *z = a.zrec + size_t(b) * a.nblk * kCW;
+    auto mass = [&](int i, bool residual) {
+        double m = 0.0;
+        for (int w = 0; w < wpb; ++w) {
+            const float2 x = __ldcg(z + size_t(i) * kCW + w);
+            m += double(residual ? x.x : x.y);
+        }
+        return m;
+    };
     double total = 0.0;
     for (int t0 = 0; t0 < a.nblk; t0 += 32) {
         const int i = t0 + lane;
-        double v = i < a.nblk ? double(__ldcg(z + i)) : 0.0;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        total += v;
+        total += warp_sum_d(i < a.nblk ? mass(i, true) : 0.0);
     }
     int blk;
     if (total > 0.0) {
-        blk = choose_block(a.nblk, st.u_blk, [&](int i) { return __ldcg(z + i); }, lane);
+        blk = choose_block(a.nblk, st.u_blk, [&](int i) { return mass(i, true); }, lane);
     } else {
         // No residual mass: draw from p of the same row instead.
-        const float4 *rec = a.rec + size_t(a.row_off[b] + st.a) * a.nblk_stride;
-        const float M = st.Mp, scale = a.scale;
-        blk = choose_block(a.nblk, st.u_blk, [&](int i) {
-            const float4 x = __ldcg(rec + i);
-            return x.y > 0.f ? x.y * exp2_approx((x.x - M) * scale) : 0.f;
-        }, lane);
+        blk = choose_block(a.nblk, st.u_blk, [&](int i) { return mass(i, false); }, lane);
         st.mode = D_FALLBACK;
         st.Sp = 1.f;
     }
-    if (lane == 0) {
-        a.dstate[b] = st;
-        push_jobs(a, T_PICK, b, blk, 1, epoch);
-    }
+    const int token = inline_pick<T>(a, st, b, blk, lane);
+    finish_request(a, b, st.a, token, lane);
 }
 
 // ---------------------------------------------------------------------------
 // consumers
 // ---------------------------------------------------------------------------
-// Draw weights of the VE elements of 16-byte vector v: 2^((z - Mp) s) for a
-// draw from p (bonus, fallback); max(0, p - q) for the residual.
 template <typename T>
-__device__ __forceinline__ void draw_weights(const uint4 *tv, const uint4 *dv, int v, int mode,
-                                             float Mp, float iSp, float Mq, float iSq,
-                                             float scale, float (&w)[Vec<T>::kElems]) {
-    constexpr int VE = Vec<T>::kElems;
-    float x[VE];
-    Vec<T>::unpack(tv[v], x);
-    if (mode == D_RESID) {
-        float y[VE];
-        Vec<T>::unpack(dv[v], y);
-#pragma unroll
-        for (int e = 0; e < VE; ++e)
-            w[e] = fmaxf(0.f, exp2_approx((x[e] - Mp) * scale) * iSp -
-                                  exp2_approx((y[e] - Mq) * scale) * iSq);
-    } else {
-#pragma unroll
-        for (int e = 0; e < VE; ++e) w[e] = exp2_approx((x[e] - Mp) * scale);
-    }
-}
-
-// Sum of the draw weights of a lane's contiguous run [v0, v0 + per).
-template <typename T>
-__device__ __forceinline__ float run_weight(const uint4 *tv, const uint4 *dv, int v0, int per,
-                                            int nvec, const DecideState &st, float iSp,
-                                            float iSq, float scale) {
-    constexpr int VE = Vec<T>::kElems;
-    float ls = 0.f;
-    for (int q = 0; q < per; ++q) {
-        const int v = v0 + q;
-        if (v < nvec) {
-            float w[VE];
-            draw_weights<T>(tv, dv, v, st.mode, st.Mp, iSp, st.Mq, iSq, scale, w);
-#pragma unroll
-            for (int e = 0; e < VE; ++e) ls += w[e];
-        }
-    }
-    return ls;
-}
-
-// The pick of a stage holding one sampling block (warp-level, by the
-// stage's last warp): the warp share, then the lane run, then the token.
-template <typename T>
-__device__ int pick_token(const VSmem &sm, int s, const TaskInfo &t, const DecideState &st,
-                          const uint4 *tv, const uint4 *dv, float scale, int lane) {
-    constexpr int VE = Vec<T>::kElems;
-    const int nvec = t.bytes / 16;
-    const double wv = lane < kCW ? sm.wd[s][lane] : 0.0;
-    const double wincl = warp_scan_incl(wv, lane);
-    const double total = __shfl_sync(0xffffffffu, wincl, kCW - 1);
-    const double target = double(st.u_tok) * total;
-    unsigned hit = __ballot_sync(0xffffffffu, lane < kCW && wincl > target);
-    const unsigned posw = __ballot_sync(0xffffffffu, lane < kCW && wv > 0.0);
-    const int ws = hit ? __ffs(hit) - 1 : (posw ? 31 - __clz(posw) : 0);
-    const double wprev = __shfl_sync(0xffffffffu, wincl, ws > 0 ? ws - 1 : 0);
-    const double wbase = ws > 0 ? wprev : 0.0;
-    const float iSp = 1.f / st.Sp, iSq = 1.f / st.Sq;
-    const int pv = kSampleBlock / VE / kCW;  // vectors per warp share
-    const int per = pv / 32;                 // vectors per lane run
-    const int v0 = ws * pv + lane * per;
-    const float ls = run_weight<T>(tv, dv, v0, per, nvec, st, iSp, iSq, scale);
-    const double lincl = warp_scan_incl(double(ls), lane);
-    const double lprev = __shfl_up_sync(0xffffffffu, lincl, 1);
-    const double lexcl = lane > 0 ? lprev : 0.0;
-    hit = __ballot_sync(0xffffffffu, ls > 0.f && wbase + lincl > target);
-    const unsigned posl = __ballot_sync(0xffffffffu, ls > 0.f);
-    const int lsel = hit ? __ffs(hit) - 1 : (posl ? 31 - __clz(posl) : -1);
-    if (lsel < 0) return t.y0 + ws * pv * VE;  // the whole share carries no weight
-    int pick = -1;
-    if (lane == lsel) {
-        int lastpos = -1;
-        float run = 0.f;
-        for (int q = 0; q < per && pick < 0; ++q) {
-            const int v = v0 + q;
-            if (v >= nvec) break;
-            float w[VE];
-            draw_weights<T>(tv, dv, v, st.mode, st.Mp, iSp, st.Mq, iSq, scale, w);
-#pragma unroll
-            for (int e = 0; e < VE; ++e) {
-                run += w[e];
-                if (pick < 0 && w[e] > 0.f) {
-                    lastpos = v * VE + e;
-                    if (wbase + lexcl + double(run) > target) pick = v * VE + e;
-                }
-            }
-        }
-        if (pick < 0) pick = lastpos;
-    }
-    return t.y0 + __shfl_sync(0xffffffffu, pick, lsel);
-}
-
-template <typename T>
-__device__ void consumer(const VerifyArgs &a, VSmem &sm, const uint8_t *ring, int warp, int lane,
-                         int epoch) {
+__device__ void consumer(const VerifyArgs &a, VSmem &sm, const uint8_t *ring,
+                         const StreamShape &sh, int warp, int lane, int epoch) {
     constexpr int VE = Vec<T>::kElems;
     const float scale = a.scale;
     const int tpw = a.chunk_elems / kCW;  // tokens per warp in a tile
     const int vpw = tpw / VE;             // vectors per warp in a tile
     const int wpb = kSampleBlock / tpw;   // warps per sampling block
-    const int bpc = kCW / wpb;            // sampling blocks per tile
+    // Row accumulators of pair rows (sampling) / of every row (greedy),
+    // carried across the tiles of a chunk.
+    float mp = -INFINITY, sp = 0.f, mq = -INFINITY, sq = 0.f;
+    float bv = -INFINITY;
+    int bi = INT_MAX;
     for (int fill = 0;; ++fill) {
         const int s = fill % kStages, n = fill / kStages;
         if (!mbar_wait_bounded(&sm.full[s], n & 1)) {
@@ -695,12 +847,10 @@ __device__ void consumer(const VerifyArgs &a, VSmem &sm, const uint8_t *ring, in
         const uint4 *tv = reinterpret_cast<const uint4 *>(ring + s * kStageBytes);
         const uint4 *dv = tv + kChunkBytes / 16;
         const int nvec = t.bytes / 16;
+        const int v0 = min(nvec, warp * vpw), v1 = min(nvec, v0 + vpw);
 
         if (t.type == T_STREAM) {
-            const int v0 = min(nvec, warp * vpw), v1 = min(nvec, v0 + vpw);
             if (a.greedy) {
-                float bv = -INFINITY;
-                int bi = INT_MAX;
                 for (int v = v0 + lane; v < v1; v += 32) {
                     float z[VE];
                     Vec<T>::unpack(tv[v], z);
@@ -711,123 +861,119 @@ __device__ void consumer(const VerifyArgs &a, VSmem &sm, const uint8_t *ring, in
                             bi = t.y0 + v * VE + e;
                         }
                 }
-                warp_am_reduce(bv, bi);
-                if (lane == 0) sm.wpart[s][warp] = make_float4(bv, __int_as_float(bi), 0.f, 0.f);
-            } else {
-                float mp = -INFINITY, sp = 0.f, mq = -INFINITY, sq = 0.f;
-                if (t.pair) {
-                    for (int v = v0 + lane; v < v1; v += 32) {
-                        float z[VE];
-                        Vec<T>::unpack(tv[v], z);
-                        online_update<VE>(mp, sp, z, scale);
-                        Vec<T>::unpack(dv[v], z);
-                        online_update<VE>(mq, sq, z, scale);
-                    }
-                    warp_ms_reduce(mq, sq, scale);
-                } else {
-                    for (int v = v0 + lane; v < v1; v += 32) {
-                        float z[VE];
-                        Vec<T>::unpack(tv[v], z);
-                        online_update<VE>(mp, sp, z, scale);
-                    }
+            } else if (t.pair) {
+                for (int v = v0 + lane; v < v1; v += 32) {
+                    float z[VE];
+                    Vec<T>::unpack(tv[v], z);
+                    online_update<VE>(mp, sp, z, scale);
+                    Vec<T>::unpack(dv[v], z);
+                    online_update<VE>(mq, sq, z, scale);
                 }
-                warp_ms_reduce(mp, sp, scale);
                 if (lane == 0) {
-                    sm.wpart[s][warp] = make_float4(mp, sp, mq, sq);
-                    if (t.pair) {
-                        const int dt = t.d;
-                        const int lo = t.y0 + v0 * VE, hi = t.y0 + v1 * VE;
-                        if (dt >= lo && dt < hi) {
-                            sm.gath[s] = make_float2(Vec<T>::load1(tv, dt - t.y0),
-                                                     Vec<T>::load1(dv, dt - t.y0));
-                            sm.gflag[s] = 1;
-                        }
-                    }
+                    const int lo = t.y0 + v0 * VE, hi = t.y0 + v1 * VE;
+                    if (t.d >= lo && t.d < hi)
+                        a.gath[t.r] = make_float2(Vec<T>::load1(tv, t.d - t.y0),
+                                                  Vec<T>::load1(dv, t.d - t.y0));
                 }
-            }
-        } else if (t.type == T_RESID) {
-            const DecideState st = load_state(a, t.b);
-            const float iSp = 1.f / st.Sp, iSq = 1.f / st.Sq;
-            const int v0 = min(nvec, warp * vpw), v1 = min(nvec, v0 + vpw);
-            float zs = 0.f;
-            for (int v = v0 + lane; v < v1; v += 32) {
-                float w[VE];
-                draw_weights<T>(tv, dv, v, D_RESID, st.Mp, iSp, st.Mq, iSq, scale, w);
-#pragma unroll
-                for (int e = 0; e < VE; ++e) zs += w[e];
-            }
-            double zd = zs;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) zd += __shfl_xor_sync(0xffffffffu, zd, o);
-            if (lane == 0) sm.wd[s][warp] = zd;
-        } else if (t.type == T_PICK) {  // each lane sums one contiguous run of its warp's share
-            const DecideState st = load_state(a, t.b);
-            const float iSp = 1.f / st.Sp, iSq = 1.f / st.Sq;
-            const int pv = kSampleBlock / VE / kCW;
-            const int per = pv / 32;
-            const float ls = run_weight<T>(tv, dv, warp * pv + lane * per, per, nvec, st, iSp,
-                                           iSq, scale);
-            const double incl = warp_scan_incl(double(ls), lane);
-            if (lane == 31) sm.wd[s][warp] = incl;
-        }
-
-        // Elect the stage's last warp; it finishes the stage.
-        __syncwarp();
-        int last = 0;
-        if (lane == 0) {
-            __threadfence_block();
-            last = atomicAdd(&sm.done[s], 1) == kCW - 1;
-        }
-        last = __shfl_sync(0xffffffffu, last, 0);
-        if (last) {
-            __threadfence_block();
-            if (lane == 0) sm.done[s] = 0;
-            if (t.type == T_STREAM) {
-                const int blk0 = t.j * bpc;
-                if (lane < bpc && blk0 + lane < a.nblk) {
-                    float4 r;
-                    if (a.greedy) {
-                        float bv = -INFINITY;
-                        int bi = INT_MAX;
-                        for (int w = lane * wpb; w < (lane + 1) * wpb; ++w)
-                            am_combine(bv, bi, sm.wpart[s][w].x, __float_as_int(sm.wpart[s][w].y));
-                        r = make_float4(bv, __int_as_float(bi), 0.f, 0.f);
-                    } else {
-                        float mp = -INFINITY, sp = 0.f, mq = -INFINITY, sq = 0.f;
-                        for (int w = lane * wpb; w < (lane + 1) * wpb; ++w) {
-                            const float4 x = sm.wpart[s][w];
-                            ms_combine(mp, sp, x.x, x.y, scale);
-                            ms_combine(mq, sq, x.z, x.w, scale);
-                        }
-                        r = make_float4(mp, sp, mq, sq);
-                    }
-                    a.rec[size_t(t.r) * a.nblk_stride + blk0 + lane] = r;
-                }
-                if (lane == 0 && sm.gflag[s]) {
-                    a.gath[t.r] = sm.gath[s];
-                    sm.gflag[s] = 0;
-                }
-            } else if (t.type == T_RESID) {
-                const int blk0 = t.j * bpc;
-                if (lane < bpc && blk0 + lane < a.nblk) {
-                    double z = 0.0;
-                    for (int w = lane * wpb; w < (lane + 1) * wpb; ++w) z += sm.wd[s][w];
-                    a.zrec[size_t(t.b) * a.nblk_stride + blk0 + lane] = float(z);
-                }
-            } else if (t.type == T_PICK) {
-                const DecideState st = load_state(a, t.b);
-                const int token = pick_token<T>(sm, s, t, st, tv, dv, scale, lane);
-                finish_request(a, t.b, st.a, token, lane);
-            } else if (t.type == T_DECIDE) {
-                __threadfence();
-                decide_request(a, t.b, epoch, lane);
             } else {
+                // Bonus row: one (max, sum) slot per tile and warp.
+                float bm = -INFINITY, bs = 0.f;
+                for (int v = v0 + lane; v < v1; v += 32) {
+                    float z[VE];
+                    Vec<T>::unpack(tv[v], z);
+                    online_update<VE>(bm, bs, z, scale);
+                }
+                warp_ms_reduce(bm, bs, scale);
+                const int y = t.y0 + warp * tpw;
+                const int blk = y / kSampleBlock;
+                if (lane == 0 && blk < a.nblk)
+                    a.blkrec[(size_t(t.b) * a.nblk + blk) * kCW + (y % kSampleBlock) / tpw] =
+                        make_float2(bm, bs);
+            }
+            if (t.flush && (a.greedy || t.pair)) {
+                float4 rec;
+                if (a.greedy) {
+                    warp_am_reduce(bv, bi);
+                    rec = make_float4(bv, __int_as_float(bi), 0.f, 0.f);
+                } else {
+                    warp_ms_reduce(mp, sp, scale);
+                    warp_ms_reduce(mq, sq, scale);
+                    rec = make_float4(mp, sp, mq, sq);
+                }
+                if (lane == 0) a.rowrec[(size_t(t.r) * a.grp_stride + t.g) * kCW + warp] = rec;
+                mp = mq = bv = -INFINITY;
+                sp = sq = 0.f;
+                bi = INT_MAX;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.empty[s]);
+        } else {
+            // Residual tile: this warp's share of the residual and p masses.
+            const DecideState st = load_state(a, t.b);
+            const float iSp = 1.f / st.Sp, iSq = 1.f / st.Sq;
+            float zr = 0.f, zp = 0.f;
+            for (int v = v0 + lane; v < v1; v += 32) {
+                float x[VE], y[VE];
+                Vec<T>::unpack(tv[v], x);
+                Vec<T>::unpack(dv[v], y);
+#pragma unroll
+                for (int e = 0; e < VE; ++e) {
+                    const float pw = exp2_approx((x[e] - st.Mp) * scale);
+                    zp += pw;
+                    zr += fmaxf(0.f, pw * iSp - exp2_approx((y[e] - st.Mq) * scale) * iSq);
+                }
+            }
+            const double dr = warp_sum_d(zr), dp = warp_sum_d(zp);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.empty[s]);  // the stage is no longer read
+            const int y = t.y0 + warp * tpw;
+            const int blk = y / kSampleBlock;
+            int last = 0;
+            if (lane == 0) {
+                if (blk < a.nblk)
+                    a.zrec[(size_t(t.b) * a.nblk + blk) * kCW + (y % kSampleBlock) / tpw] =
+                        make_float2(float(dr), float(dp));
                 __threadfence();
-                decide_residual_block(a, t.b, epoch, lane);
+                last = atomicAdd(&a.r1_cnt[t.b], 1) == a.nc * kCW - 1;
+            }
+            if (lane == 0 && last) push_decide(a, t.b | kFinishResidual, epoch);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// decider: warp kCW + 1 serves the decide queue
+// ---------------------------------------------------------------------------
+template <typename T>
+__device__ void decider(const VerifyArgs &a, const StreamShape &sh, int epoch, int lane) {
+    const int wpb = kSampleBlock / (a.chunk_elems / kCW);
+    int pending = -1;
+    for (;;) {
+        int b = -1;
+        if (lane == 0) {
+            if (pending < 0) pending = atomicAdd(&a.q_ctr[QB_HEAD], 1);
+            const uint64_t t0 = global_timer_ns();
+            unsigned ns = 32;
+            for (;;) {
+                if (pending < a.qbcap && ld_acquire(&a.qb_ready[pending]) == epoch) {
+                    b = __ldcg(a.qb_job + pending);
+                    pending = -1;
+                    break;
+                }
+                if (ld_acquire(&a.q_ctr[Q_FINISHED]) >= a.B) break;
+                if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+                    atomicOr(a.status, kStatusQueueTimeout);
+                    break;
+                }
+                __nanosleep(ns);
+                ns = min(ns * 2, 256u);
             }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.empty[s]);
+        b = __shfl_sync(0xffffffffu, b, 0);
+        if (b < 0) return;
+        __threadfence();
+        if (b & kFinishResidual) finish_residual<T>(a, b & ~kFinishResidual, wpb, lane);
+        else decide_request<T>(a, sh, b, wpb, epoch, lane);
     }
 }
 
@@ -840,31 +986,28 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(const VerifyA
     if (tid < kStages) {
         mbar_init(&sm.full[tid], 1);
         mbar_init(&sm.empty[tid], kCW);
-        sm.done[tid] = 0;
-        sm.gflag[tid] = 0;
     }
     if (tid == 0) fence_barrier_init();
     __syncthreads();
-
-    // Packed rows as written by the compaction, never more than its capacity.
-    const int n_rows = min(max(a.row_off[a.B], 0), a.B * (a.gamma + 1));
-    const long long n_tasks = (long long)n_rows * a.nc;
-    const long long G = gridDim.x;
-    const long long s_lo = n_tasks * blockIdx.x / G, s_hi = n_tasks * (blockIdx.x + 1) / G;
-
+    const StreamShape sh = stream_shape(a);
     if (warp == kCW) {
-        if (lane == 0) producer(a, sm, ring, s_lo, s_hi, n_rows, epoch);
+        if (lane == 0) producer(a, sm, ring, sh, epoch);
+    } else if (warp == kCW + 1) {
+        decider<T>(a, sh, epoch, lane);
     } else {
-        consumer<T>(a, sm, ring, warp, lane, epoch);
+        consumer<T>(a, sm, ring, sh, warp, lane, epoch);
     }
     __syncthreads();
     if (tid == 0) {
         __threadfence();
-        if (atomicAdd(&a.q_ctr[Q_EXITED], 1) == int(G) - 1) {
-            // Every CTA is done: reset the queue for the next launch.
-            a.q_ctr[Q_HEAD] = 0;
-            a.q_ctr[Q_TAIL] = 0;
+        if (atomicAdd(&a.q_ctr[Q_EXITED], 1) == int(gridDim.x) - 1) {
+            // Every CTA is done: reset the queues for the next launch.
+            a.q_ctr[QA_HEAD] = 0;
+            a.q_ctr[QA_TAIL] = 0;
+            a.q_ctr[QB_HEAD] = 0;
+            a.q_ctr[QB_TAIL] = 0;
             a.q_ctr[Q_FINISHED] = 0;
+            a.q_ctr[Q_CHUNK] = 0;
             a.q_ctr[Q_EXITED] = 0;
             a.q_ctr[Q_EPOCH] = epoch;
             __threadfence();
@@ -892,8 +1035,8 @@ int verify_blocks_per_sm(int logit_bf16) {
 }
 
 cudaError_t launch_verify(const VerifyArgs &a, int logit_bf16, int grid, cudaStream_t s) {
-    // Cooperative launch: the producers poll a device-wide queue, so every
-    // CTA of the grid must be resident at once.
+    // Cooperative launch: producers and deciders poll device-wide queues, so
+    // every CTA of the grid must be resident at once.
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kVerifyThreads);
