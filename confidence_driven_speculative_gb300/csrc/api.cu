@@ -162,11 +162,15 @@ dspark_status dspark_score_budget(const dspark_step *s, dspark_stream_t stream) 
     if ((st = check_workspace(s, &lay))) return st;
     if ((st = device_info(&dev))) return st;
 
+    // d-splits per request: enough CTAs to cover the GPU, every slice at
+    // most kMaxSliceVec vectors (its weight slice sits in shared memory)
     const int nvec = int(size_t(s->d) * hs / 16);
     int splits = (4 * dev->sms + s->B - 1) / s->B;
-    splits = std::min(splits, dspark::kMaxScoreSplits);
     splits = std::min(splits, std::max(1, nvec / 32));
-    splits = std::max(splits, 1);
+    splits = std::max(splits, (nvec + dspark::kMaxSliceVec - 1) / dspark::kMaxSliceVec);
+    if (splits > dspark::kMaxScoreSplits)
+        return fail(DSPARK_EINVAL, "%s: d=%d needs more than %d splits", fn, s->d,
+                    dspark::kMaxScoreSplits);
     dspark::ScoreArgs a{};
     a.B = s->B; a.gamma = s->gamma; a.d = s->d; a.splits = splits;
     a.hidden_bf16 = s->hidden_dtype == DSPARK_BF16;

@@ -19,6 +19,7 @@ constexpr int kVerifyThreads = (kConsumerWarps + 2) * 32;  // + producer and dec
 constexpr int kChunkBytes = 16384;       // one vocab tile of one row (verify)
 constexpr int kStages = 3;               // verify smem ring: kStages x (target + draft) tiles
 constexpr int kMaxScoreSplits = 32;      // d-splits per request in the score kernel
+constexpr int kMaxSliceVec = 256;        // 16-byte vectors of d per score CTA
 constexpr int kSampleBlock = 4096;       // token ids per block of the two-level draw
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // bounded waits: 2 s
 
@@ -45,7 +46,7 @@ struct WorkspaceLayout {
     size_t r1_cnt;        // int32 [B]   per-request residual tiles done
     size_t q_ctr;         // int32 [8]   queue head, tail, finished, exited, epoch, chunk
     size_t dot_part;      // float [B * gamma * kMaxScoreSplits]
-    size_t rowrec;        // float4 [B*(gamma+1) * nc * 8]  row partials per (row, chunk, warp)
+    size_t rowrec;        // float4 [B*(gamma+1) * nc]      row partials per (row, chunk)
     size_t blkrec;        // float2 [B * nblk * 8]          bonus-row block partials per warp
     size_t zrec;          // float2 [B * nblk * 8]          residual / p block masses per warp
     size_t gath;          // float2 [B * (gamma+1)]         z_p[d], z_q[d]
@@ -78,7 +79,7 @@ inline WorkspaceLayout workspace_layout(int B, int gamma, int V) {
     w.r1_cnt = off;      off = align256(off + sizeof(int32_t) * size_t(B));
     w.q_ctr = off;       off = align256(off + sizeof(int32_t) * 8);
     w.dot_part = off;    off = align256(off + sizeof(float) * size_t(B) * gamma * kMaxScoreSplits);
-    w.rowrec = off;      off = align256(off + 16 * rows * size_t(w.nc) * warps);
+    w.rowrec = off;      off = align256(off + 16 * rows * size_t(w.nc));
     w.blkrec = off;      off = align256(off + 8 * size_t(B) * w.nblk * warps);
     w.zrec = off;        off = align256(off + 8 * size_t(B) * w.nblk * warps);
     w.gath = off;        off = align256(off + 8 * rows);

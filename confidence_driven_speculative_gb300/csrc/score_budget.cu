@@ -176,7 +176,8 @@ __device__ void budget_and_scan(const ScoreArgs &a) {
             if (b < B) {
                 const int l0 = __ldcg(&a.L0[b]);
                 for (int k = 1; k <= l0; ++k) {
-                    const unsigned key = __float_as_uint(__ldcg(&a.survival[b * g + k - 1]));
+                    const unsigned key = staged ? keys[b * g + k - 1]
+                                                : __float_as_uint(__ldcg(&a.survival[b * g + k - 1]));
                     above += key > prefix;
                     equal += key == prefix;
                 }
@@ -197,52 +198,65 @@ __device__ void budget_and_scan(const ScoreArgs &a) {
 template <typename T>
 __global__ void __launch_bounds__(kThreads) score_budget_kernel(const ScoreArgs a) {
     constexpr int VE = Vec<T>::kElems;
+    constexpr int U = 8;  // 16-byte loads in flight per lane and position
+    __shared__ float4 w_s[kMaxSliceVec * VE / 4];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int b = blockIdx.x / a.splits, s = blockIdx.x - b * a.splits;
     const int g = a.gamma;
     const int nvec = a.d / VE;
     const int v0 = int((long long)nvec * s / a.splits);
     const int v1 = int((long long)nvec * (s + 1) / a.splits);
-    const float4 *w4 = reinterpret_cast<const float4 *>(a.head_w);
+    const int nv = v1 - v0;  // <= kMaxSliceVec (the host picks the splits)
+    const float4 *w4 = reinterpret_cast<const float4 *>(a.head_w) + size_t(v0) * VE / 4;
+    for (int i = tid; i < nv * VE / 4; i += kThreads) w_s[i] = __ldg(w4 + i);
+    __syncthreads();
 
-    for (int i = warp; i < g; i += kWarps) {
-        const uint4 *hv = reinterpret_cast<const uint4 *>(
-            static_cast<const char *>(a.hidden) + (size_t(b) * g + i) * size_t(a.d) * sizeof(T));
-        float acc = 0.f;
-        int v = v0 + lane;
-        // eight 16-byte loads in flight per lane
-        for (; v + 224 < v1; v += 256) {
-            uint4 h[8];
+    // Warp w takes positions w, w + 8, ...; two at a time, their loads
+    // interleaved so 2U loads per lane are in flight.
+    for (int i0 = warp; i0 < g; i0 += 2 * kWarps) {
+        const int i1 = i0 + kWarps;
+        const bool two = i1 < g;
+        const uint4 *h0 = reinterpret_cast<const uint4 *>(
+            static_cast<const char *>(a.hidden) + (size_t(b) * g + i0) * size_t(a.d) * sizeof(T)) + v0;
+        const uint4 *h1 = reinterpret_cast<const uint4 *>(
+            static_cast<const char *>(a.hidden) + (size_t(b) * g + (two ? i1 : i0)) * size_t(a.d) * sizeof(T)) + v0;
+        float acc0 = 0.f, acc1 = 0.f;
+        for (int vb = 0; vb < nv; vb += 32 * U) {
+            uint4 x0[U], x1[U];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) h[u] = __ldcs(hv + v + 32 * u);
+            for (int u = 0; u < U; ++u) {
+                const int v = vb + lane + 32 * u;
+                x0[u] = v < nv ? __ldcs(h0 + v) : make_uint4(0, 0, 0, 0);
+                x1[u] = (two && v < nv) ? __ldcs(h1 + v) : make_uint4(0, 0, 0, 0);
+            }
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                float x[VE];
-                Vec<T>::unpack(h[u], x);
+            for (int u = 0; u < U; ++u) {
+                const int v = vb + lane + 32 * u;
+                if (v < nv) {
+                    float e0[VE], e1[VE];
+                    Vec<T>::unpack(x0[u], e0);
+                    Vec<T>::unpack(x1[u], e1);
 #pragma unroll
-                for (int e = 0; e < VE; e += 4) {
-                    const float4 wv = __ldg(w4 + ((v + 32 * u) * VE + e) / 4);
-                    acc = fmaf(x[e], wv.x, acc);
-                    acc = fmaf(x[e + 1], wv.y, acc);
-                    acc = fmaf(x[e + 2], wv.z, acc);
-                    acc = fmaf(x[e + 3], wv.w, acc);
+                    for (int e = 0; e < VE; e += 4) {
+                        const float4 wv = w_s[(v * VE + e) / 4];
+                        acc0 = fmaf(e0[e], wv.x, acc0);
+                        acc0 = fmaf(e0[e + 1], wv.y, acc0);
+                        acc0 = fmaf(e0[e + 2], wv.z, acc0);
+                        acc0 = fmaf(e0[e + 3], wv.w, acc0);
+                        acc1 = fmaf(e1[e], wv.x, acc1);
+                        acc1 = fmaf(e1[e + 1], wv.y, acc1);
+                        acc1 = fmaf(e1[e + 2], wv.z, acc1);
+                        acc1 = fmaf(e1[e + 3], wv.w, acc1);
+                    }
                 }
             }
         }
-        for (; v < v1; v += 32) {
-            float x[VE];
-            Vec<T>::unpack(__ldcs(hv + v), x);
-#pragma unroll
-            for (int e = 0; e < VE; e += 4) {
-                const float4 wv = __ldg(w4 + (v * VE + e) / 4);
-                acc = fmaf(x[e], wv.x, acc);
-                acc = fmaf(x[e + 1], wv.y, acc);
-                acc = fmaf(x[e + 2], wv.z, acc);
-                acc = fmaf(x[e + 3], wv.w, acc);
-            }
+        acc0 = warp_sum(acc0);
+        acc1 = warp_sum(acc1);
+        if (lane == 0) {
+            a.dot_part[(size_t(b) * g + i0) * kMaxScoreSplits + s] = acc0;
+            if (two) a.dot_part[(size_t(b) * g + i1) * kMaxScoreSplits + s] = acc1;
         }
-        acc = warp_sum(acc);
-        if (lane == 0) a.dot_part[(size_t(b) * g + i) * kMaxScoreSplits + s] = acc;
     }
 
     __shared__ int s_last;

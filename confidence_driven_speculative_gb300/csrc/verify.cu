@@ -79,6 +79,8 @@ struct TaskInfo {
 struct VSmem {
     uint64_t full[kStages], empty[kStages];
     TaskInfo task[kStages];
+    float4 part[kStages][kCW];  // per-warp row partials of a chunk's last tile
+    int done[kStages];          // warps finished with a chunk's last tile
 };
 
 // Grid-wide shape of the stream work, the same in every thread.  Rows
@@ -107,6 +109,9 @@ __device__ __forceinline__ int ld_relaxed(const int *p) {
 }
 __device__ __forceinline__ void st_release(int *p, int v) {
     asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_relaxed(int *p, int v) {
+    asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar))
@@ -207,9 +212,9 @@ __device__ void push_resid_jobs(const VerifyArgs &a, int b, int epoch) {
     const int pos = atomicAdd(&a.q_ctr[QA_TAIL], a.nc);
     for (int i = 0; i < a.nc; ++i)
         if (pos + i < a.qcap) a.q_job[pos + i] = make_int2(b, i);
-    __threadfence();
+    __threadfence();  // every payload (and the caller's state) before any ready word
     for (int i = 0; i < a.nc; ++i)
-        if (pos + i < a.qcap) st_release(&a.q_ready[pos + i], epoch);
+        if (pos + i < a.qcap) st_relaxed(&a.q_ready[pos + i], epoch);
 }
 
 // Decider jobs, served by the decider warps: decide request b, or (with
@@ -221,7 +226,7 @@ __device__ void push_decide(const VerifyArgs &a, int job, int epoch) {
     if (pos < a.qbcap) {
         a.qb_job[pos] = job;
         __threadfence();
-        st_release(&a.qb_ready[pos], epoch);
+        st_relaxed(&a.qb_ready[pos], epoch);
     }
 }
 
@@ -525,27 +530,29 @@ __device__ __forceinline__ float pair_sum(const float (&w)[VE]) {
     return t[0];
 }
 
-// The token inside sampling block `blk` of the drawn row(s): the smallest id
-// whose running in-block weight exceeds u_tok times the block's weight.
-// Each lane owns a contiguous run of 128 ids (kRunVec 16-byte vectors),
-// loaded four vectors at a time; per-vector weights are summed pairwise and
-// kept in registers, runs are combined in fp64, and the lane holding the
-// crossing finds its vector from the kept sums (same fp32 association) and
-// reloads only that vector.  The rows were streamed moments earlier, so the
-// loads hit L2.
+// The token of a draw inside one slot -- the ids [y0, y0 + n) that one
+// consumer warp covers in a tile: the smallest id whose running weight,
+// counted from the slot's start, exceeds `target`.  Each lane owns a
+// contiguous run of n/32 ids (kRunVec 16-byte vectors, one batch of loads);
+// per-vector weights are summed pairwise and kept in registers; runs are
+// combined in fp64; the lane holding the crossing finds its vector from the
+// kept sums and reloads only that vector.  If rounding leaves no crossing,
+// the last id with positive weight.  The rows were streamed moments
+// earlier, so the loads hit L2.
 template <typename T>
-__device__ int inline_pick(const VerifyArgs &a, const DecideState &st, int b, int blk, int lane) {
+__device__ int slot_pick(const VerifyArgs &a, const DecideState &st, int b, int y0, int n,
+                         double target, int lane) {
     constexpr int VE = Vec<T>::kElems;
-    constexpr int kRunVec = kSampleBlock / 32 / VE;  // vectors per lane run
+    constexpr int kRunVec = 4;  // n = 32 lanes x 4 vectors (1024 bf16 / 512 fp32 ids)
     const int r = a.row_off[b] + (st.mode == D_BONUS ? verify_len(a, b) : st.a);
     const uint4 *tv = reinterpret_cast<const uint4 *>(static_cast<const char *>(a.target_logits) +
                                                       size_t(r) * a.row_bytes);
     const uint4 *dv = reinterpret_cast<const uint4 *>(
         static_cast<const char *>(a.draft_logits) + (size_t(b) * a.gamma + st.a) * a.row_bytes);
-    const int nvec_row = a.row_bytes / 16;
+    const int v_end = min(a.row_bytes / 16, (y0 + n) / VE);
     const float scale = a.scale, iSp = 1.f / st.Sp, iSq = 1.f / st.Sq;
     const bool resid = st.mode == D_RESID;
-    const int v0 = blk * (kSampleBlock / VE) + lane * kRunVec;
+    const int v0 = y0 / VE + lane * kRunVec;
     auto weights = [&](const uint4 &xv, const uint4 &yv, float (&w)[VE]) {
         float x[VE];
         Vec<T>::unpack(xv, x);
@@ -561,41 +568,32 @@ __device__ int inline_pick(const VerifyArgs &a, const DecideState &st, int b, in
             for (int e = 0; e < VE; ++e) w[e] = exp2_approx((x[e] - st.Mp) * scale);
         }
     };
-    constexpr int kBatch = 4;
-    float vs[kRunVec];
+    uint4 xv[kRunVec], yv[kRunVec];
 #pragma unroll
-    for (int q0 = 0; q0 < kRunVec; q0 += kBatch) {
-        uint4 xv[kBatch], yv[kBatch];
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-            const int v = v0 + q0 + u;
-            const bool in = v < nvec_row;
-            xv[u] = in ? __ldcg(tv + v) : make_uint4(0, 0, 0, 0);
-            yv[u] = in && resid ? __ldcg(dv + v) : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-            float w[VE];
-            weights(xv[u], yv[u], w);
-            vs[q0 + u] = v0 + q0 + u < nvec_row ? pair_sum<VE>(w) : 0.f;
-        }
+    for (int q = 0; q < kRunVec; ++q) {
+        const int v = v0 + q;
+        const bool in = v < v_end;
+        xv[q] = in ? __ldcg(tv + v) : make_uint4(0, 0, 0, 0);
+        yv[q] = in && resid ? __ldcg(dv + v) : make_uint4(0, 0, 0, 0);
     }
+    float vs[kRunVec];
     float ls = 0.f;
 #pragma unroll
-    for (int q = 0; q < kRunVec; ++q) ls += vs[q];
+    for (int q = 0; q < kRunVec; ++q) {
+        float w[VE];
+        weights(xv[q], yv[q], w);
+        vs[q] = v0 + q < v_end ? pair_sum<VE>(w) : 0.f;
+        ls += vs[q];
+    }
     const double incl = warp_scan_incl(double(ls), lane);
-    const double total = __shfl_sync(0xffffffffu, incl, 31);
-    const double target = double(st.u_tok) * total;
     const double prev = __shfl_up_sync(0xffffffffu, incl, 1);
     const double excl = lane > 0 ? prev : 0.0;
     const unsigned hit = __ballot_sync(0xffffffffu, ls > 0.f && incl > target);
     const unsigned pos = __ballot_sync(0xffffffffu, ls > 0.f);
     const int lsel = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : -1);
-    if (lsel < 0) return blk * kSampleBlock;  // a block without weight (not drawn in practice)
+    if (lsel < 0) return y0;  // a slot without weight (not drawn in practice)
     int pick = -1;
     if (lane == lsel) {
-        // the vector that crosses, from the kept sums (the last positive one
-        // if rounding leaves no crossing)
         float run = 0.f, run_at = 0.f;
         int qsel = -1, qlast = -1;
 #pragma unroll
@@ -608,32 +606,67 @@ __device__ int inline_pick(const VerifyArgs &a, const DecideState &st, int b, in
             run += vs[q];
         }
         if (qsel < 0) qsel = qlast;
-        if (qsel >= 0) {
-            const int v = v0 + qsel;
+        int lastpos = -1;
+#pragma unroll
+        for (int q = 0; q < kRunVec; ++q) {
+            if (q != qsel) continue;
             float w[VE];
-            weights(__ldcg(tv + v), resid ? __ldcg(dv + v) : make_uint4(0, 0, 0, 0), w);
+            weights(xv[q], yv[q], w);
             float re = run_at;
-            int lastpos = -1;
 #pragma unroll
             for (int e = 0; e < VE; ++e) {
                 re += w[e];
                 if (pick < 0 && w[e] > 0.f) {
-                    lastpos = v * VE + e;
-                    if (excl + double(re) > target) pick = v * VE + e;
+                    lastpos = (v0 + q) * VE + e;
+                    if (excl + double(re) > target) pick = (v0 + q) * VE + e;
                 }
             }
-            if (pick < 0) pick = lastpos;
         }
-        if (pick < 0) pick = v0 * VE;
+        if (pick < 0) pick = lastpos >= 0 ? lastpos : v0 * VE;
     }
     return __shfl_sync(0xffffffffu, pick, lsel);
 }
 
-// Fold the record slots of packed row r (chunk slots x warps, fixed order).
+// The token inside sampling block `blk`, given the block's per-warp slot
+// masses sm_w (w < wpb, in every lane): the slot whose running mass crosses
+// u_tok times the block mass, then the id inside that slot.
+template <typename T>
+__device__ int block_pick(const VerifyArgs &a, const DecideState &st, int b, int blk,
+                          const double (&slot_mass)[kCW], int wpb, int tpw, int lane) {
+    double total = 0.0;
+#pragma unroll
+    for (int w = 0; w < kCW; ++w)
+        if (w < wpb) total += slot_mass[w];
+    const double target = double(st.u_tok) * total;
+    double cum = 0.0, before = 0.0;
+    int wsel = -1, wlast = 0;
+#pragma unroll
+    for (int w = 0; w < kCW; ++w) {
+        if (w >= wpb || wsel >= 0) continue;
+        if (slot_mass[w] > 0.0) {
+            wlast = w;
+            if (cum + slot_mass[w] > target) {
+                wsel = w;
+                before = cum;
+            }
+        }
+        cum += slot_mass[w];
+    }
+    if (wsel < 0) {
+        wsel = wlast;
+        before = 0.0;
+#pragma unroll
+        for (int w = 0; w < kCW; ++w)
+            if (w < wsel) before += slot_mass[w];
+    }
+    return slot_pick<T>(a, st, b, blk * kSampleBlock + wsel * tpw, tpw, target - before, lane);
+}
+
+// Fold the chunk records of packed row r (fixed order).
 __device__ __forceinline__ float4 fold_row(const VerifyArgs &a, const StreamShape &sh, int r,
                                            float scale) {
-    const float4 *rec = a.rowrec + size_t(r) * a.grp_stride * kCW;
-    const int n = (r < sh.nA ? 1 : sh.gprb) * kCW;
+    const float4 *rec = a.rowrec + size_t(r) * a.grp_stride;
+    const int n = r < sh.nA ? 1 : sh.gprb;
     float4 acc = a.greedy ? make_float4(-INFINITY, __int_as_float(INT_MAX), 0.f, 0.f)
                           : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
     for (int i0 = 0; i0 < n; i0 += 8) {
@@ -738,42 +771,68 @@ __device__ void decide_request(const VerifyArgs &a, const StreamShape &sh, int b
     st.u_blk = ub;
     st.u_tok = ut;
     if (ab == Lb) {
-        // Bonus draw from p of row L_b, done here: block masses from its
-        // slots, then the token inside the chosen block.
-        constexpr int kCache = 4;  // blocks per lane kept in registers
-        float2 bm[kCache];
+        // Bonus draw from p of row L_b, done here: block and slot masses from
+        // its per-warp slots (lane-owned blocks cached in registers).
+        constexpr int kCache = 2;  // blocks per lane kept in registers (nblk <= 64)
+        float2 sl[kCache][kCW];
         float mb = -INFINITY;
 #pragma unroll
         for (int q = 0; q < kCache; ++q) {
             const int i = q * 32 + lane;
-            bm[q] = i < a.nblk ? bonus_block(a, b, i, wpb, scale) : make_float2(-INFINITY, 0.f);
-            if (bm[q].y > 0.f) mb = fmaxf(mb, bm[q].x);
+            const float2 *p = a.blkrec + (size_t(b) * a.nblk + (i < a.nblk ? i : 0)) * kCW;
+#pragma unroll
+            for (int w = 0; w < kCW; ++w)
+                sl[q][w] = i < a.nblk && w < wpb ? __ldcg(p + w) : make_float2(-INFINITY, 0.f);
+#pragma unroll
+            for (int w = 0; w < kCW; ++w)
+                if (sl[q][w].y > 0.f) mb = fmaxf(mb, sl[q][w].x);
         }
         for (int i = kCache * 32 + lane; i < a.nblk; i += 32) {
             const float2 x = bonus_block(a, b, i, wpb, scale);
             if (x.y > 0.f) mb = fmaxf(mb, x.x);
         }
         const float M = warp_max(mb);
+        // slot mass in the units of 2^((z - M) s)
+        auto smass = [&](float2 x) { return x.y > 0.f ? x.y * exp2_approx((x.x - M) * scale) : 0.f; };
         auto mass = [&](int i) {
             const int q = i >> 5;
-            float2 x;
+            float m = 0.f;
             if (q < kCache) {
-                x = bm[0];
 #pragma unroll
-                for (int c = 1; c < kCache; ++c)
-                    if (q == c) x = bm[c];
+                for (int c = 0; c < kCache; ++c)
+                    if (q == c)
+#pragma unroll
+                        for (int w = 0; w < kCW; ++w) m += smass(sl[c][w]);
             } else {
-                x = bonus_block(a, b, i, wpb, scale);
+                const float2 *p = a.blkrec + (size_t(b) * a.nblk + i) * kCW;
+                for (int w = 0; w < wpb; ++w) m += smass(__ldcg(p + w));
             }
-            return x.y > 0.f ? x.y * exp2_approx((x.x - M) * scale) : 0.f;
+            return m;
         };
         const int blk = choose_block(a.nblk, ub, mass, lane);
+        double slot_mass[kCW];
+        {
+            const int q = blk >> 5, owner = blk & 31;
+#pragma unroll
+            for (int w = 0; w < kCW; ++w) {
+                float m = 0.f;
+                if (q < kCache) {
+#pragma unroll
+                    for (int c = 0; c < kCache; ++c)
+                        if (q == c) m = smass(sl[c][w]);
+                    m = __shfl_sync(0xffffffffu, m, owner);
+                } else if (w < wpb) {
+                    m = smass(__ldcg(a.blkrec + (size_t(b) * a.nblk + blk) * kCW + w));
+                }
+                slot_mass[w] = w < wpb ? double(m) : 0.0;
+            }
+        }
         st.mode = D_BONUS;
         st.Mp = M;
         st.Sp = 1.f;
         st.Mq = 0.f;
         st.Sq = 1.f;
-        const int token = inline_pick<T>(a, st, b, blk, lane);
+        const int token = block_pick<T>(a, st, b, blk, slot_mass, wpb, kSampleBlock / wpb, lane);
         finish_request(a, b, ab, token, lane);
     } else {
         st.mode = D_RESID;
@@ -788,17 +847,35 @@ __device__ void decide_request(const VerifyArgs &a, const StreamShape &sh, int b
     }
 }
 
-// Every residual slot of request b is in: choose the block from the masses
-// and draw the token inside it.
+// Every residual slot of request b is in: choose the block from the masses,
+// then the slot, then the token.
 template <typename T>
 __device__ void finish_residual(const VerifyArgs &a, int b, int wpb, int lane) {
     DecideState st = load_state(a, b);
     const float2 *z = a.zrec + size_t(b) * a.nblk * kCW;
+    constexpr int kCache = 2;  // blocks per lane kept in registers (nblk <= 64)
+    float2 sl[kCache][kCW];
+#pragma unroll
+    for (int q = 0; q < kCache; ++q) {
+        const int i = q * 32 + lane;
+#pragma unroll
+        for (int w = 0; w < kCW; ++w)
+            sl[q][w] = i < a.nblk && w < wpb ? __ldcg(z + size_t(i) * kCW + w) : make_float2(0.f, 0.f);
+    }
     auto mass = [&](int i, bool residual) {
+        const int q = i >> 5;
         double m = 0.0;
-        for (int w = 0; w < wpb; ++w) {
-            const float2 x = __ldcg(z + size_t(i) * kCW + w);
-            m += double(residual ? x.x : x.y);
+        if (q < kCache) {
+#pragma unroll
+            for (int c = 0; c < kCache; ++c)
+                if (q == c)
+#pragma unroll
+                    for (int w = 0; w < kCW; ++w) m += double(residual ? sl[c][w].x : sl[c][w].y);
+        } else {
+            for (int w = 0; w < wpb; ++w) {
+                const float2 x = __ldcg(z + size_t(i) * kCW + w);
+                m += double(residual ? x.x : x.y);
+            }
         }
         return m;
     };
@@ -807,16 +884,32 @@ __device__ void finish_residual(const VerifyArgs &a, int b, int wpb, int lane) {
         const int i = t0 + lane;
         total += warp_sum_d(i < a.nblk ? mass(i, true) : 0.0);
     }
-    int blk;
-    if (total > 0.0) {
-        blk = choose_block(a.nblk, st.u_blk, [&](int i) { return mass(i, true); }, lane);
-    } else {
+    const bool residual = total > 0.0;
+    if (!residual) {
         // No residual mass: draw from p of the same row instead.
-        blk = choose_block(a.nblk, st.u_blk, [&](int i) { return mass(i, false); }, lane);
         st.mode = D_FALLBACK;
         st.Sp = 1.f;
     }
-    const int token = inline_pick<T>(a, st, b, blk, lane);
+    const int blk = choose_block(a.nblk, st.u_blk, [&](int i) { return mass(i, residual); }, lane);
+    double slot_mass[kCW];
+    {
+        const int q = blk >> 5, owner = blk & 31;
+#pragma unroll
+        for (int w = 0; w < kCW; ++w) {
+            float m = 0.f;
+            if (q < kCache) {
+#pragma unroll
+                for (int c = 0; c < kCache; ++c)
+                    if (q == c) m = residual ? sl[c][w].x : sl[c][w].y;
+                m = __shfl_sync(0xffffffffu, m, owner);
+            } else if (w < wpb) {
+                const float2 x = __ldcg(z + size_t(blk) * kCW + w);
+                m = residual ? x.x : x.y;
+            }
+            slot_mass[w] = w < wpb ? double(m) : 0.0;
+        }
+    }
+    const int token = block_pick<T>(a, st, b, blk, slot_mass, wpb, kSampleBlock / wpb, lane);
     finish_request(a, b, st.a, token, lane);
 }
 
@@ -891,19 +984,41 @@ __device__ void consumer(const VerifyArgs &a, VSmem &sm, const uint8_t *ring,
                         make_float2(bm, bs);
             }
             if (t.flush && (a.greedy || t.pair)) {
-                float4 rec;
+                // End of the chunk: the eight warp partials become one record.
                 if (a.greedy) {
                     warp_am_reduce(bv, bi);
-                    rec = make_float4(bv, __int_as_float(bi), 0.f, 0.f);
+                    if (lane == 0) sm.part[s][warp] = make_float4(bv, __int_as_float(bi), 0.f, 0.f);
                 } else {
                     warp_ms_reduce(mp, sp, scale);
                     warp_ms_reduce(mq, sq, scale);
-                    rec = make_float4(mp, sp, mq, sq);
+                    if (lane == 0) sm.part[s][warp] = make_float4(mp, sp, mq, sq);
                 }
-                if (lane == 0) a.rowrec[(size_t(t.r) * a.grp_stride + t.g) * kCW + warp] = rec;
                 mp = mq = bv = -INFINITY;
                 sp = sq = 0.f;
                 bi = INT_MAX;
+                int last = 0;
+                if (lane == 0) {
+                    __threadfence_block();
+                    last = atomicAdd(&sm.done[s], 1) == kCW - 1;
+                }
+                if (__shfl_sync(0xffffffffu, last, 0)) {
+                    __threadfence_block();
+                    float4 x = lane < kCW ? sm.part[s][lane]
+                                          : (a.greedy ? make_float4(-INFINITY, __int_as_float(INT_MAX), 0.f, 0.f)
+                                                      : make_float4(-INFINITY, 0.f, -INFINITY, 0.f));
+                    if (a.greedy) {
+                        int xi = __float_as_int(x.y);
+                        warp_am_reduce(x.x, xi);
+                        x.y = __int_as_float(xi);
+                    } else {
+                        warp_ms_reduce(x.x, x.y, scale);
+                        warp_ms_reduce(x.z, x.w, scale);
+                    }
+                    if (lane == 0) {
+                        sm.done[s] = 0;
+                        a.rowrec[size_t(t.r) * a.grp_stride + t.g] = x;
+                    }
+                }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.empty[s]);
@@ -986,6 +1101,7 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(const VerifyA
     if (tid < kStages) {
         mbar_init(&sm.full[tid], 1);
         mbar_init(&sm.empty[tid], kCW);
+        sm.done[tid] = 0;
     }
     if (tid == 0) fence_barrier_init();
     __syncthreads();

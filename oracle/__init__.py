@@ -197,7 +197,7 @@ def compact(L, draft_tokens, last_tokens=None, seq_lens=None) -> dict:
     return out
 
 
-EPS_U, EPS_BLK, EPS_TOK = 1e-5, 1e-6, 5e-7
+EPS_U, EPS_BLK, EPS_TOK = 1e-5, 1e-6, 2e-6
 
 
 def verify_request(L: int, drafts, tgt, dft, Tm: float, u, u2, u3, eps: float = EPS_U,
