@@ -34,6 +34,7 @@ struct DeviceInfo {
     bool ready = false;
     int sms = 0;
     int verify_blocks[2] = {0, 0};  // per logit dtype (0 = fp32, 1 = bf16)
+    int score_blocks[2] = {0, 0};   // per hidden dtype
 };
 constexpr int kMaxDevices = 64;
 DeviceInfo g_dev[kMaxDevices];
@@ -60,6 +61,9 @@ dspark_status device_info(DeviceInfo **out) {
             if (d.verify_blocks[bf] <= 0)
                 return fail(DSPARK_ECUDA, "verify kernel cannot be resident (smem %zu bytes)",
                             dspark::verify_smem_bytes());
+            d.score_blocks[bf] = dspark::score_blocks_per_sm(bf);
+            if (d.score_blocks[bf] <= 0)
+                return fail(DSPARK_ECUDA, "score kernel cannot be resident");
         }
         d.ready = true;
     }
@@ -162,27 +166,21 @@ dspark_status dspark_score_budget(const dspark_step *s, dspark_stream_t stream) 
     if ((st = check_workspace(s, &lay))) return st;
     if ((st = device_info(&dev))) return st;
 
-    // d-splits per request: enough CTAs to cover the GPU, every slice at
-    // most kMaxSliceVec vectors (its weight slice sits in shared memory)
-    const int nvec = int(size_t(s->d) * hs / 16);
-    int splits = (4 * dev->sms + s->B - 1) / s->B;
-    splits = std::min(splits, std::max(1, nvec / 32));
-    splits = std::max(splits, (nvec + dspark::kMaxSliceVec - 1) / dspark::kMaxSliceVec);
-    if (splits > dspark::kMaxScoreSplits)
-        return fail(DSPARK_EINVAL, "%s: d=%d needs more than %d splits", fn, s->d,
-                    dspark::kMaxScoreSplits);
+    // One CTA per resident slot, each a contiguous range of the B*gamma rows.
+    const long long rows = (long long)s->B * s->gamma;
+    const int hb = s->hidden_dtype == DSPARK_BF16;
+    const int grid = int(std::min<long long>(rows, (long long)dev->sms * dev->score_blocks[hb]));
     dspark::ScoreArgs a{};
-    a.B = s->B; a.gamma = s->gamma; a.d = s->d; a.splits = splits;
+    a.B = s->B; a.gamma = s->gamma; a.d = s->d;
     a.hidden_bf16 = s->hidden_dtype == DSPARK_BF16;
     a.hidden = s->hidden; a.head_w = s->head_w; a.head_bias = s->head_bias; a.sts_tau = s->sts_tau;
     a.cost_c = s->cost_c; a.cap_T = s->cap_T;
     a.conf = s->conf; a.survival = s->survival; a.L0 = s->L0; a.L = s->L;
     a.draft_off = s->draft_off; a.row_off = s->row_off;
-    a.dot_part = ws_at<float>(s, lay.dot_part);
-    a.req_cnt = ws_at<int32_t>(s, lay.score_cnt);
     a.done_cnt = ws_at<int32_t>(s, lay.score_done);
+    a.row_ctr = ws_at<int32_t>(s, lay.score_rows);
     a.status = ws_at<int32_t>(s, lay.status);
-    cudaError_t e = dspark::launch_score_budget(a, s->B * splits, cs);
+    cudaError_t e = dspark::launch_score_budget(a, grid, cs);
     if (e != cudaSuccess) return cuda_fail(e, "score_budget_kernel launch");
     return DSPARK_OK;
 }

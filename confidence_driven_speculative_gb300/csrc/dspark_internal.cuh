@@ -18,8 +18,6 @@ constexpr int kConsumerWarps = 8;        // verify: consumer warps per CTA
 constexpr int kVerifyThreads = (kConsumerWarps + 2) * 32;  // + producer and decider warps
 constexpr int kChunkBytes = 16384;       // one vocab tile of one row (verify)
 constexpr int kStages = 3;               // verify smem ring: kStages x (target + draft) tiles
-constexpr int kMaxScoreSplits = 32;      // d-splits per request in the score kernel
-constexpr int kMaxSliceVec = 256;        // 16-byte vectors of d per score CTA
 constexpr int kSampleBlock = 4096;       // token ids per block of the two-level draw
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // bounded waits: 2 s
 
@@ -40,12 +38,11 @@ struct DecideState {
 // ---------------------------------------------------------------------------
 struct WorkspaceLayout {
     size_t status;        // int32
-    size_t score_cnt;     // int32 [B]   per-request split counter
-    size_t score_done;    // int32 [1]   requests finished
+    size_t score_done;    // int32 [1]   hidden rows published
+    size_t score_rows;    // int32 [1]   hidden rows claimed
     size_t verify_cnt;    // int32 [B]   per-request stream tiles done
     size_t r1_cnt;        // int32 [B]   per-request residual tiles done
     size_t q_ctr;         // int32 [8]   queue head, tail, finished, exited, epoch, chunk
-    size_t dot_part;      // float [B * gamma * kMaxScoreSplits]
     size_t rowrec;        // float4 [B*(gamma+1) * nc]      row partials per (row, chunk)
     size_t blkrec;        // float2 [B * nblk * 8]          bonus-row block partials per warp
     size_t zrec;          // float2 [B * nblk * 8]          residual / p block masses per warp
@@ -73,12 +70,11 @@ inline WorkspaceLayout workspace_layout(int B, int gamma, int V) {
     const size_t warps = kConsumerWarps;
     size_t off = 0;
     w.status = off;      off = align256(off + sizeof(int32_t));
-    w.score_cnt = off;   off = align256(off + sizeof(int32_t) * size_t(B));
     w.score_done = off;  off = align256(off + sizeof(int32_t));
+    w.score_rows = off;  off = align256(off + sizeof(int32_t));
     w.verify_cnt = off;  off = align256(off + sizeof(int32_t) * size_t(B));
     w.r1_cnt = off;      off = align256(off + sizeof(int32_t) * size_t(B));
     w.q_ctr = off;       off = align256(off + sizeof(int32_t) * 8);
-    w.dot_part = off;    off = align256(off + sizeof(float) * size_t(B) * gamma * kMaxScoreSplits);
     w.rowrec = off;      off = align256(off + 16 * rows * size_t(w.nc));
     w.blkrec = off;      off = align256(off + 8 * size_t(B) * w.nblk * warps);
     w.zrec = off;        off = align256(off + 8 * size_t(B) * w.nblk * warps);
@@ -232,6 +228,11 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  ::"r"(smem_addr(bar)), "r"(bytes) : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar))
+                 : "memory");
+}
+
 // Global -> shared bulk copy; completion is signalled on `bar` as bytes.
 // dst, src and bytes must be multiples of 16.
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
@@ -281,7 +282,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
 // Kernel argument blocks and launchers (defined in the .cu files).
 // ---------------------------------------------------------------------------
 struct ScoreArgs {
-    int B, gamma, d, splits;
+    int B, gamma, d;
     int hidden_bf16;
     const void *hidden;
     const float *head_w, *head_bias, *sts_tau;
@@ -289,8 +290,7 @@ struct ScoreArgs {
     int cap_T;
     float *conf, *survival;
     int32_t *L0, *L, *draft_off, *row_off;
-    float *dot_part;
-    int32_t *req_cnt, *done_cnt, *status;
+    int32_t *done_cnt, *row_ctr, *status;
 };
 
 struct FixedArgs {
@@ -333,6 +333,7 @@ struct VerifyArgs {
 };
 
 cudaError_t launch_score_budget(const ScoreArgs &a, int grid, cudaStream_t s);
+int score_blocks_per_sm(int hidden_bf16);
 cudaError_t launch_fixed_budget(const FixedArgs &a, cudaStream_t s);
 cudaError_t launch_compact(const CompactArgs &a, cudaStream_t s);
 cudaError_t launch_verify(const VerifyArgs &a, int logit_bf16, int grid, cudaStream_t s);

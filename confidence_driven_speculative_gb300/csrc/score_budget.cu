@@ -9,24 +9,33 @@
 // "Zero-overhead scheduling and kernels": a verify-length top-k schedule
 // bounds the batch.
 //
-// Work split.  Grid = B x splits CTAs of 256 threads.  CTA (b, s) streams the
-// s-th slice of the d-vector of every draft position of request b (16-byte
-// loads, one warp per position, fp32 FMAs) and writes partial dot products.
-// The last CTA of request b (per-request counter) sums the slices in a fixed
-// order, applies bias, 1/tau_i and the sigmoid, forms the cumulative product
-// S and the pre-cap length L0_b.  The last request to finish (batch counter)
-// runs the cap in that one CTA: an MSB-first radix select over the fp32 bit
-// patterns of the candidate gains S_{b,k} (non-negative floats order like
-// their bit patterns), ties resolved by request then position, followed by
-// the exclusive scans.  Counters reset themselves, so nothing waits and the
-// kernel is safe to replay.
+// Work split.  One CTA per resident slot.  A producer warp claims hidden rows
+// one at a time from a device counter and streams them through a ring of
+// 16 KB shared-memory stages with 1-D bulk TMA copies; eight consumer warps
+// take the stages in the same order, 16-byte vectors interleaved over their
+// 256 threads, and accumulate fp32 dot products against the head weight.
+// When a row fits one stage every row puts the same vectors of d on a thread,
+// so the thread keeps its slice of the weight in registers; longer rows read
+// it through L1.  At a row's last tile the last warp to finish sums the eight
+// warp partials in a fixed order and writes the row's confidence (bias,
+// 1/tau_i, sigmoid).  The CTA that publishes the batch's last rows (row
+// counter) then forms, one thread per request, the cumulative product S and
+// the pre-cap length L0_b, and runs the cap: an
+// MSB-first radix select over the fp32 bit patterns of the candidate gains
+// S_{b,k} (non-negative floats order like their bit patterns), ties resolved
+// by request then position, followed by the exclusive scans.  Counters reset
+// themselves, so no CTA waits on another and the kernel is safe to replay.
 #include "dspark_internal.cuh"
 
 namespace dspark {
 namespace {
 
+// Barrier of the 256 threads (warps 0-7) that run the scans and the cap; in
+// the streaming kernel the producer warp does not take part.
+__device__ __forceinline__ void sync256() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
 // Block-wide exclusive scan of one int per thread; *total gets the sum.
-// `sh` needs kWarps + 1 ints.  Contains __syncthreads.
+// `sh` needs kWarps + 1 ints.  Called by warps 0-7 together (sync256).
 __device__ int block_excl_scan_int(int v, int *total, int *sh) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int incl = v;
@@ -36,7 +45,7 @@ __device__ int block_excl_scan_int(int v, int *total, int *sh) {
         if (lane >= o) incl += n;
     }
     if (lane == 31) sh[warp] = incl;
-    __syncthreads();
+    sync256();
     if (warp == 0) {
         int x = lane < kWarps ? sh[lane] : 0;
 #pragma unroll
@@ -46,10 +55,10 @@ __device__ int block_excl_scan_int(int v, int *total, int *sh) {
         }
         if (lane < kWarps) sh[lane] = x;
     }
-    __syncthreads();
+    sync256();
     const int before = warp > 0 ? sh[warp - 1] : 0;
     *total = sh[kWarps - 1];
-    __syncthreads();
+    sync256();
     return before + incl - v;
 }
 
@@ -74,97 +83,415 @@ __device__ void write_offsets(int B, const int32_t *L, int32_t *draft_off, int32
     }
 }
 
-// The cap, run by one CTA once every L0 and S of the batch is written.
-constexpr int kSmemKeys = 4096;  // candidate keys the cap stages in shared memory
+constexpr int kScoreStages = 4;
+constexpr int kScoreTile = 16384;                   // bytes per stage
+constexpr int kScoreThreads = (kWarps + 1) * 32;    // 8 consumer warps + producer
+constexpr int kScoreVecPerThread = kScoreTile / 16 / kThreads;
+constexpr size_t kScoreSmemBytes = size_t(kScoreStages) * kScoreTile;
 
-__device__ void budget_and_scan(const ScoreArgs &a) {
-    __shared__ unsigned keys[kSmemKeys];
-    __shared__ int sh[kWarps + 1];
-    __shared__ unsigned hist[256];
-    __shared__ int sel[2];
-    const int B = a.B, g = a.gamma, tid = threadIdx.x;
+struct ScoreSmem {
+    uint64_t full[kScoreStages], empty[kScoreStages];
+    int row[kScoreStages];             // hidden row of the stage (-1: no more rows)
+    int tile[kScoreStages];            // its tile within the row
+    float part[kScoreStages][kWarps];  // warp partials of a row's last tile
+    int done[kScoreStages];            // warps past a row's last tile
+    int run_cap;                       // this CTA finished the batch
+    float tau[DSPARK_MAX_GAMMA];       // STS temperatures
+};
 
-    int part = 0;
-    for (int b = tid; b < B; b += kThreads) part += __ldcg(&a.L0[b]);
-    int sum;
-    block_excl_scan_int(part, &sum, sh);
+struct RowShape {
+    int rows;       // B * gamma
+    int ntr;        // tiles per row
+    int row_bytes;
+};
+
+__device__ __forceinline__ RowShape row_shape(const ScoreArgs &a, int elem_bytes) {
+    RowShape rs;
+    rs.rows = a.B * a.gamma;
+    rs.row_bytes = a.d * elem_bytes;
+    rs.ntr = (rs.row_bytes + kScoreTile - 1) / kScoreTile;
+    return rs;
+}
+
+// Lane 0 of warp 8.  Starts on row blockIdx.x, then claims rows one at a
+// time from a device counter (the next claim is in flight while the current
+// row is copied), so every CTA streams until the batch runs out.
+__device__ void score_producer(const ScoreArgs &a, ScoreSmem &sm, uint8_t *ring,
+                               const RowShape &rs) {
+    const char *hidden = static_cast<const char *>(a.hidden);
+    int next = blockIdx.x;  // the first row needs no claim
+    for (int fill = 0;;) {
+        const int r = next;
+        if (r < rs.rows) next = int(gridDim.x) + atomicAdd(a.row_ctr, 1);
+        for (int q = 0; q < (r < rs.rows ? rs.ntr : 1); ++q, ++fill) {
+            const int s = fill % kScoreStages, n = fill / kScoreStages;
+            if (n > 0 && !mbar_wait_bounded(&sm.empty[s], (n - 1) & 1)) {
+                atomicOr(a.status, kStatusWaitTimeout);
+                return;
+            }
+            if (r >= rs.rows) {
+                sm.row[s] = -1;
+                mbar_arrive(&sm.full[s]);
+                return;
+            }
+            sm.row[s] = r;
+            sm.tile[s] = q;
+            const int bytes = min(kScoreTile, rs.row_bytes - q * kScoreTile);
+            mbar_arrive_expect_tx(&sm.full[s], uint32_t(bytes));
+            bulk_g2s(ring + size_t(s) * kScoreTile,
+                     hidden + size_t(r) * rs.row_bytes + size_t(q) * kScoreTile, uint32_t(bytes),
+                     &sm.full[s]);
+        }
+    }
+}
+
+// Warps 0-7.  Returns the number of rows this CTA published.
+template <typename T>
+__device__ int score_consumer(const ScoreArgs &a, ScoreSmem &sm, const uint8_t *ring,
+                              const RowShape &rs, int warp, int lane) {
+    constexpr int VE = Vec<T>::kElems;
+    constexpr int NV = kScoreVecPerThread;
+    constexpr int kTileElems = kScoreTile / int(sizeof(T));
+    const int tid = warp * 32 + lane;
+    // A row that fits one tile puts the same vectors of d on this thread in
+    // every row: its slice of the head weight then stays in registers.
+    const bool w_regs = rs.ntr == 1;
+    float wr[NV][VE];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int v = tid + kThreads * i;
+#pragma unroll
+        for (int j = 0; j < VE; j += 4) {
+            float4 wv = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (w_regs && v * VE < a.d)
+                wv = __ldg(reinterpret_cast<const float4 *>(a.head_w) + (v * VE + j) / 4);
+            wr[i][j] = wv.x;
+            wr[i][j + 1] = wv.y;
+            wr[i][j + 2] = wv.z;
+            wr[i][j + 3] = wv.w;
+        }
+    }
+    int nrows = 0;
+    float acc = 0.f;
+    for (int fill = 0;; ++fill) {
+        const int s = fill % kScoreStages, n = fill / kScoreStages;
+        if (!mbar_wait_bounded(&sm.full[s], n & 1)) {
+            if (lane == 0) atomicOr(a.status, kStatusWaitTimeout);
+            return nrows;
+        }
+        const int r = sm.row[s], q = sm.tile[s];
+        if (r < 0) return nrows;
+        if (q == 0) acc = 0.f;
+        // The row's bias is needed at its end; load it now, behind the FMAs.
+        const int rb = r / a.gamma;
+        const float bias = q + 1 == rs.ntr ? __ldg(&a.head_bias[rb]) : 0.f;
+        const int nvec = min(kScoreTile, rs.row_bytes - q * kScoreTile) / 16;
+        const uint4 *tv = reinterpret_cast<const uint4 *>(ring + size_t(s) * kScoreTile);
+        uint4 x[NV];
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            const int v = tid + kThreads * i;
+            x[i] = v < nvec ? tv[v] : make_uint4(0, 0, 0, 0);
+        }
+        if (w_regs) {
+            // Vectors past the row are zero in both x and wr.
+#pragma unroll
+            for (int i = 0; i < NV; ++i) {
+                float e[VE];
+                Vec<T>::unpack(x[i], e);
+#pragma unroll
+                for (int j = 0; j < VE; ++j) acc = fmaf(e[j], wr[i][j], acc);
+            }
+        } else {
+            const float4 *w4 = reinterpret_cast<const float4 *>(a.head_w + size_t(q) * kTileElems);
+#pragma unroll
+            for (int i = 0; i < NV; ++i) {
+                const int v = tid + kThreads * i;
+                if (v < nvec) {
+                    float e[VE];
+                    Vec<T>::unpack(x[i], e);
+#pragma unroll
+                    for (int j = 0; j < VE; j += 4) {
+                        const float4 wv = __ldg(w4 + (v * VE + j) / 4);
+                        acc = fmaf(e[j], wv.x, acc);
+                        acc = fmaf(e[j + 1], wv.y, acc);
+                        acc = fmaf(e[j + 2], wv.z, acc);
+                        acc = fmaf(e[j + 3], wv.w, acc);
+                    }
+                }
+            }
+        }
+        if (q + 1 < rs.ntr) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.empty[s]);
+            continue;
+        }
+        // Last tile of row r: the last warp here sums the eight partials.
+        ++nrows;
+        const float wsum = warp_sum(acc);
+        int last = 0;
+        if (lane == 0) {
+            sm.part[s][warp] = wsum;
+            __threadfence_block();
+            last = atomicAdd(&sm.done[s], 1) == kWarps - 1;
+        }
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (!last) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.empty[s]);
+            continue;
+        }
+        __threadfence_block();
+        float dot = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) dot += sm.part[s][w];
+        __syncwarp();
+        if (lane == 0) {
+            sm.done[s] = 0;
+            mbar_arrive(&sm.empty[s]);
+            // conf = sigmoid((w . h + bias_b) / tau_i) of this row
+            const float x = (dot + bias) / sm.tau[r - rb * a.gamma];
+            a.conf[r] = 1.f / (1.f + expf(-x));
+        }
+        __syncwarp();
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Request curves and the cap, run by the CTA that publishes the batch's last
+// row (warps 0-7).  Its 64 KB ring is free by then.  When B * pitch <=
+// kOnChip (pitch = gamma rounded up to odd, so a thread per request reads
+// its row without bank conflicts) it holds
+//   [0, 32 KB)   confidences, [b * pitch + k];
+//   [32, 64 KB)  S_{b,k+1}, same layout;
+// and once the confidences are written out, the radix select's two lists of
+// kListCap keys take [0, 32 KB).  Larger batches work from global memory.
+// ---------------------------------------------------------------------------
+constexpr int kListCap = 4096;
+constexpr int kOnChip = 8192;
+static_assert(2 * kListCap * 4 <= kOnChip * 4 && 2 * kOnChip * 4 <= int(kScoreSmemBytes),
+              "the finishing CTA's ring layout");
+
+struct FinishSmem {
+    int sh[kWarps + 1];
+    unsigned hist[256];
+    int sel[2];
+    int cnt;
+};
+
+// Thread-per-request survival curve: S_0 = 1, S_k = S_{k-1} * conf_k, and
+// L0_b = max{k : S_k >= c} (0 if none).  With sC/sS the confidences come
+// from and the curve goes to shared memory (the caller writes it out);
+// otherwise global memory is used directly.
+__device__ int request_curve(const ScoreArgs &a, int b, const float *sC, float *sS, int pitch) {
+    const int g = a.gamma;
+    float S = 1.f;
+    int L = 1.f >= a.cost_c ? 0 : -1;
+    for (int k0 = 0; k0 < g; k0 += 8) {
+        float cv[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int k = k0 + j;
+            cv[j] = k >= g ? 0.f : sC ? sC[b * pitch + k] : __ldcg(&a.conf[size_t(b) * g + k]);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int k = k0 + j;
+            if (k < g) {
+                S *= cv[j];
+                if (sS) sS[b * pitch + k] = S;
+                else a.survival[size_t(b) * g + k] = S;
+                if (S >= a.cost_c) L = k + 1;
+            }
+        }
+    }
+    const int l0 = L < 0 ? 0 : L;
+    a.L0[b] = l0;
+    return l0;
+}
+
+// L0_b recounted from the shared curve: S does not increase with k (each
+// factor is at most 1 and rounding is monotone), so the k with S_k >= c are
+// exactly 1..L0_b.
+__device__ __forceinline__ int l0_of(const ScoreArgs &a, const float *sS, int pitch, int b) {
+    if (!sS) return __ldcg(&a.L0[b]);
+    int n = 0;
+    for (int k = 0; k < a.gamma; ++k) n += sS[b * pitch + k] >= a.cost_c;
+    return n;
+}
+
+// Bit pattern of S_{b,k+1}, from the shared copy when there is one.
+__device__ __forceinline__ unsigned s_key(const ScoreArgs &a, const float *sS, int pitch, int b,
+                                          int k) {
+    return __float_as_uint(sS ? sS[b * pitch + k] : __ldcg(&a.survival[size_t(b) * a.gamma + k]));
+}
+
+// Warp-aggregated histogram add: the lanes of the first two bins present
+// add once per bin (keys cluster in a few bins in the first passes), the
+// rest one by one (then they are spread over many bins).
+__device__ __forceinline__ void hist_add(unsigned *hist, bool hit, unsigned bin, int lane) {
+    unsigned rem = __ballot_sync(0xffffffffu, hit);
+#pragma unroll
+    for (int round = 0; round < 2; ++round) {
+        if (rem == 0u) return;
+        const int lead = __ffs(rem) - 1;
+        const unsigned lb = __shfl_sync(0xffffffffu, bin, lead);
+        const unsigned same = __ballot_sync(0xffffffffu, hit && bin == lb);
+        if (lane == lead) atomicAdd(&hist[lb], unsigned(__popc(same)));
+        rem &= ~same;
+    }
+    if (rem & (1u << lane)) atomicAdd(&hist[bin], 1u);
+}
+
+// Warp 0 finds the digit holding the need-th largest key; fs.sel gets the
+// digit and the rank still to place within it.
+__device__ void select_digit(FinishSmem &fs, int need, int tid) {
+    if (tid >= 32) return;
+    // lane l owns bins 8l .. 8l+7; suffix sums from the top bin down
+    unsigned local = 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) local += fs.hist[tid * 8 + q];
+    unsigned suf = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned n = __shfl_down_sync(0xffffffffu, suf, o);
+        if (tid + o < 32) suf += n;
+    }
+    const unsigned above = suf - local;  // keys in bins above this lane's
+    if (above < unsigned(need) && unsigned(need) <= suf) {
+        unsigned cum = above;
+        for (int q = 7; q >= 0; --q) {
+            const unsigned c = fs.hist[tid * 8 + q];
+            if (cum + c >= unsigned(need)) {
+                fs.sel[0] = tid * 8 + q;
+                fs.sel[1] = need - int(cum);
+                break;
+            }
+            cum += c;
+        }
+    }
+}
+
+__device__ void finish_and_budget(const ScoreArgs &a, uint8_t *ring) {
+    __shared__ FinishSmem fs;
+    const int B = a.B, g = a.gamma, tid = threadIdx.x, lane = tid & 31;
+    const int pitch = g | 1;
+    const bool on_chip = (long long)B * pitch <= kOnChip;
+    float *sC = on_chip ? reinterpret_cast<float *>(ring) : nullptr;
+    float *sS = on_chip ? reinterpret_cast<float *>(ring) + kOnChip : nullptr;
+    unsigned *listA = reinterpret_cast<unsigned *>(ring);
+    unsigned *listB = listA + kListCap;
+    const int n_rows = B * g;
+    if (on_chip) {
+        // Coalesced read of every confidence into the per-request layout.
+        for (int base = 0; base < n_rows; base += 16 * kThreads) {
+            float v[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int i = base + j * kThreads + tid;
+                v[j] = i < n_rows ? __ldcg(&a.conf[i]) : 0.f;
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int i = base + j * kThreads + tid;
+                if (i < n_rows) {
+                    const int b = i / g;
+                    sC[b * pitch + (i - b * g)] = v[j];
+                }
+            }
+        }
+    }
+    sync256();
+    for (int b = tid; b < B; b += kThreads) request_curve(a, b, sC, sS, pitch);
+    sync256();
+    if (on_chip) {
+        // Coalesced write of the survival curves.
+        for (int i = tid; i < n_rows; i += kThreads) {
+            const int b = i / g;
+            a.survival[i] = sS[b * pitch + (i - b * g)];
+        }
+    }
+
+    // Each request's candidate keys S_{b,1..L0_b} go to listA at the
+    // exclusive scan of L0 (while they fit); listA overwrites the staged
+    // confidences, which the barrier inside the scan retires.
+    int sum = 0;
+    for (int base = 0; base < B; base += kThreads) {
+        const int b = base + tid;
+        const int l0 = b < B ? l0_of(a, sS, pitch, b) : 0;
+        int total;
+        const int off = sum + block_excl_scan_int(l0, &total, fs.sh);
+        for (int k = 0; k < l0 && off + k < kListCap; ++k) listA[off + k] = s_key(a, sS, pitch, b, k);
+        sum += total;
+    }
+    sync256();
 
     if (a.cap_T < 0 || sum <= a.cap_T) {
-        for (int b = tid; b < B; b += kThreads) a.L[b] = __ldcg(&a.L0[b]);
+        for (int b = tid; b < B; b += kThreads) a.L[b] = l0_of(a, sS, pitch, b);
     } else if (a.cap_T == 0) {
         for (int b = tid; b < B; b += kThreads) a.L[b] = 0;
     } else {
-        // Find the cap_T-th largest candidate key, 8 bits per pass from the top.
-        // Up to kSmemKeys candidate keys are staged in shared memory (one
-        // round of loads, non-candidates marked 0xffffffff); larger batches
-        // are re-read from L2 each pass.
-        const int nkeys = B * g;
-        const bool staged = nkeys <= kSmemKeys;
-        if (staged) {
-            for (int f = tid; f < nkeys; f += kThreads) {
-                const int b = f / g, k = f - b * g + 1;
-                const int l0 = __ldcg(&a.L0[b]);
-                const unsigned kv = __float_as_uint(__ldcg(&a.survival[f]));
-                keys[f] = k <= l0 ? kv : 0xffffffffu;
-            }
-        }
+        // The cap_T-th largest key, 8 bits per pass from the top.
         unsigned prefix = 0, mask = 0;
         int need = a.cap_T;  // rank still to place within keys matching `prefix`
+        const bool listed = sum <= kListCap;
+        unsigned *src = listA, *dst = listB;
+        int n = sum;
         for (int pass = 0; pass < 4; ++pass) {
             const int shift = 24 - 8 * pass;
-            for (int i = tid; i < 256; i += kThreads) hist[i] = 0;
+            for (int i = tid; i < 256; i += kThreads) fs.hist[i] = 0;
             if (tid == 0) {
-                sel[0] = 0;
-                sel[1] = need;
+                fs.sel[0] = 0;
+                fs.sel[1] = need;
+                fs.cnt = 0;
             }
-            __syncthreads();
-            if (staged) {
-                for (int f = tid; f < nkeys; f += kThreads) {
-                    const unsigned kv = keys[f];
-                    if (kv != 0xffffffffu && (kv & mask) == prefix)
-                        atomicAdd(&hist[(kv >> shift) & 255u], 1u);
+            sync256();
+            if (listed) {
+                // The list holds exactly the keys that match `prefix`.
+                for (int base = 0; base < n; base += kThreads) {
+                    const int i = base + tid;
+                    const unsigned kv = i < n ? src[i] : 0u;
+                    hist_add(fs.hist, i < n, (kv >> shift) & 255u, lane);
                 }
             } else {
-                for (int f = tid; f < nkeys; f += kThreads) {
-                    const int b = f / g, k = f - b * g + 1;
-                    if (k <= __ldcg(&a.L0[b])) {
-                        const unsigned kv = __float_as_uint(__ldcg(&a.survival[f]));
-                        if ((kv & mask) == prefix) atomicAdd(&hist[(kv >> shift) & 255u], 1u);
+                for (int base = 0; base < B; base += kThreads) {
+                    const int b = base + tid;
+                    const int l0 = b < B ? l0_of(a, sS, pitch, b) : 0;
+                    for (int k = 0; k < g; ++k) {
+                        const unsigned kv = k < l0 ? s_key(a, sS, pitch, b, k) : 0u;
+                        hist_add(fs.hist, k < l0 && (kv & mask) == prefix, (kv >> shift) & 255u, lane);
                     }
                 }
             }
-            __syncthreads();
-            if (tid < 32) {
-                // lane l owns bins 8l .. 8l+7; suffix sums from the top bin down
-                unsigned local = 0;
-#pragma unroll
-                for (int q = 0; q < 8; ++q) local += hist[tid * 8 + q];
-                unsigned suf = local;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const unsigned n = __shfl_down_sync(0xffffffffu, suf, o);
-                    if (tid + o < 32) suf += n;
-                }
-                const unsigned above = suf - local;  // keys in bins above this lane's
-                const bool hit = above < unsigned(need) && unsigned(need) <= suf;
-                if (hit) {
-                    unsigned cum = above;
-                    for (int q = 7; q >= 0; --q) {
-                        const unsigned c = hist[tid * 8 + q];
-                        if (cum + c >= unsigned(need)) {
-                            sel[0] = tid * 8 + q;
-                            sel[1] = need - int(cum);
-                            break;
-                        }
-                        cum += c;
-                    }
-                }
-            }
-            __syncthreads();
-            prefix |= unsigned(sel[0]) << shift;
+            sync256();
+            select_digit(fs, need, tid);
+            sync256();
+            const unsigned d = unsigned(fs.sel[0]);
+            need = fs.sel[1];
+            prefix |= d << shift;
             mask |= 255u << shift;
-            need = sel[1];
-            __syncthreads();
+            if (listed && pass < 3) {
+                // Keep the keys of the chosen digit for the next pass.
+                for (int base = 0; base < n; base += kThreads) {
+                    const int i = base + tid;
+                    const unsigned kv = i < n ? src[i] : 0u;
+                    const bool keep = i < n && ((kv >> shift) & 255u) == d;
+                    const unsigned bal = __ballot_sync(0xffffffffu, keep);
+                    if (bal) {
+                        const int lead = __ffs(bal) - 1;
+                        int pos = 0;
+                        if (lane == lead) pos = atomicAdd(&fs.cnt, __popc(bal));
+                        pos = __shfl_sync(0xffffffffu, pos, lead);
+                        if (keep) dst[pos + __popc(bal & ((1u << lane) - 1u))] = kv;
+                    }
+                }
+                sync256();
+                n = fs.cnt;
+                unsigned *t = src;
+                src = dst;
+                dst = t;
+            }
+            sync256();
         }
         // prefix is the threshold key; `need` keys equal to it are kept, the
         // lowest (b, k) first.  Within a request keys do not increase with k,
@@ -174,16 +501,15 @@ __device__ void budget_and_scan(const ScoreArgs &a) {
             const int b = base + tid;
             int above = 0, equal = 0;
             if (b < B) {
-                const int l0 = __ldcg(&a.L0[b]);
-                for (int k = 1; k <= l0; ++k) {
-                    const unsigned key = staged ? keys[b * g + k - 1]
-                                                : __float_as_uint(__ldcg(&a.survival[b * g + k - 1]));
+                const int l0 = l0_of(a, sS, pitch, b);
+                for (int k = 0; k < l0; ++k) {
+                    const unsigned key = s_key(a, sS, pitch, b, k);
                     above += key > prefix;
                     equal += key == prefix;
                 }
             }
             int total;
-            const int ex = block_excl_scan_int(equal, &total, sh);
+            const int ex = block_excl_scan_int(equal, &total, fs.sh);
             if (b < B) {
                 const int keep = min(max(need - (carry + ex), 0), equal);
                 a.L[b] = above + keep;
@@ -191,114 +517,47 @@ __device__ void budget_and_scan(const ScoreArgs &a) {
             carry += total;
         }
     }
-    __syncthreads();
-    write_offsets(B, a.L, a.draft_off, a.row_off, sh);
+    sync256();
+    write_offsets(B, a.L, a.draft_off, a.row_off, fs.sh);
 }
 
+// Steps a1-a3: streaming confidence head, survival curve, pre-cap lengths,
+// then (in the CTA that finishes the batch) the cap and the scans.
 template <typename T>
-__global__ void __launch_bounds__(kThreads) score_budget_kernel(const ScoreArgs a) {
-    constexpr int VE = Vec<T>::kElems;
-    constexpr int U = 8;  // 16-byte loads in flight per lane and position
-    __shared__ float4 w_s[kMaxSliceVec * VE / 4];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int b = blockIdx.x / a.splits, s = blockIdx.x - b * a.splits;
-    const int g = a.gamma;
-    const int nvec = a.d / VE;
-    const int v0 = int((long long)nvec * s / a.splits);
-    const int v1 = int((long long)nvec * (s + 1) / a.splits);
-    const int nv = v1 - v0;  // <= kMaxSliceVec (the host picks the splits)
-    const float4 *w4 = reinterpret_cast<const float4 *>(a.head_w) + size_t(v0) * VE / 4;
-    for (int i = tid; i < nv * VE / 4; i += kThreads) w_s[i] = __ldg(w4 + i);
-    __syncthreads();
-
-    // Warp w takes positions w, w + 8, ...; two at a time, their loads
-    // interleaved so 2U loads per lane are in flight.
-    for (int i0 = warp; i0 < g; i0 += 2 * kWarps) {
-        const int i1 = i0 + kWarps;
-        const bool two = i1 < g;
-        const uint4 *h0 = reinterpret_cast<const uint4 *>(
-            static_cast<const char *>(a.hidden) + (size_t(b) * g + i0) * size_t(a.d) * sizeof(T)) + v0;
-        const uint4 *h1 = reinterpret_cast<const uint4 *>(
-            static_cast<const char *>(a.hidden) + (size_t(b) * g + (two ? i1 : i0)) * size_t(a.d) * sizeof(T)) + v0;
-        float acc0 = 0.f, acc1 = 0.f;
-        for (int vb = 0; vb < nv; vb += 32 * U) {
-            uint4 x0[U], x1[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int v = vb + lane + 32 * u;
-                x0[u] = v < nv ? __ldcs(h0 + v) : make_uint4(0, 0, 0, 0);
-                x1[u] = (two && v < nv) ? __ldcs(h1 + v) : make_uint4(0, 0, 0, 0);
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int v = vb + lane + 32 * u;
-                if (v < nv) {
-                    float e0[VE], e1[VE];
-                    Vec<T>::unpack(x0[u], e0);
-                    Vec<T>::unpack(x1[u], e1);
-#pragma unroll
-                    for (int e = 0; e < VE; e += 4) {
-                        const float4 wv = w_s[(v * VE + e) / 4];
-                        acc0 = fmaf(e0[e], wv.x, acc0);
-                        acc0 = fmaf(e0[e + 1], wv.y, acc0);
-                        acc0 = fmaf(e0[e + 2], wv.z, acc0);
-                        acc0 = fmaf(e0[e + 3], wv.w, acc0);
-                        acc1 = fmaf(e1[e], wv.x, acc1);
-                        acc1 = fmaf(e1[e + 1], wv.y, acc1);
-                        acc1 = fmaf(e1[e + 2], wv.z, acc1);
-                        acc1 = fmaf(e1[e + 3], wv.w, acc1);
-                    }
-                }
-            }
-        }
-        acc0 = warp_sum(acc0);
-        acc1 = warp_sum(acc1);
-        if (lane == 0) {
-            a.dot_part[(size_t(b) * g + i0) * kMaxScoreSplits + s] = acc0;
-            if (two) a.dot_part[(size_t(b) * g + i1) * kMaxScoreSplits + s] = acc1;
-        }
+__global__ void __launch_bounds__(kScoreThreads, 3) score_budget_kernel(const ScoreArgs a) {
+    extern __shared__ __align__(1024) uint8_t ring[];
+    __shared__ ScoreSmem sm;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid < kScoreStages) {
+        mbar_init(&sm.full[tid], 1);
+        mbar_init(&sm.empty[tid], kWarps);
+        sm.done[tid] = 0;
     }
-
-    __shared__ int s_last;
-    __shared__ float s_conf[DSPARK_MAX_GAMMA];
-    __syncthreads();
     if (tid == 0) {
-        __threadfence();
-        s_last = atomicAdd(&a.req_cnt[b], 1) == a.splits - 1;
+        sm.run_cap = 0;
+        fence_barrier_init();
     }
+    if (tid < a.gamma) sm.tau[tid] = a.sts_tau[tid];
     __syncthreads();
-    if (!s_last) return;
+    const RowShape rs = row_shape(a, int(sizeof(T)));
+    if (warp == kWarps) {
+        if (lane == 0) score_producer(a, sm, ring, rs);
+        return;
+    }
+    const int nrows = score_consumer<T>(a, sm, ring, rs, warp, lane);
+    // Publish this CTA's confidences; the CTA that adds the batch's last
+    // rows finishes every request and runs the cap.
     __threadfence();
-
-    // Last slice of request b: finish the head and the survival curve.
-    if (tid < g) {
-        float dot = 0.f;
-        for (int q = 0; q < a.splits; ++q)
-            dot += __ldcg(&a.dot_part[(size_t(b) * g + tid) * kMaxScoreSplits + q]);
-        const float x = (dot + a.head_bias[b]) / a.sts_tau[tid];
-        const float c = 1.f / (1.f + expf(-x));
-        a.conf[size_t(b) * g + tid] = c;
-        s_conf[tid] = c;
-    }
-    __syncthreads();
+    sync256();
+    if (tid == 0) sm.run_cap = atomicAdd(a.done_cnt, nrows) + nrows == rs.rows;
+    sync256();
+    if (!sm.run_cap) return;
+    __threadfence();
+    finish_and_budget(a, ring);
     if (tid == 0) {
-        float S = 1.f;  // S_0
-        int L = 1.f >= a.cost_c ? 0 : -1;
-        for (int k = 1; k <= g; ++k) {
-            S *= s_conf[k - 1];
-            a.survival[size_t(b) * g + k - 1] = S;
-            if (S >= a.cost_c) L = k;
-        }
-        a.L0[b] = L < 0 ? 0 : L;
-        a.req_cnt[b] = 0;
-        __threadfence();
-        s_last = atomicAdd(a.done_cnt, 1) == a.B - 1;
+        *a.done_cnt = 0;
+        *a.row_ctr = 0;
     }
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    budget_and_scan(a);
-    if (tid == 0) *a.done_cnt = 0;
 }
 
 __global__ void __launch_bounds__(kThreads) fixed_budget_kernel(const FixedArgs a) {
@@ -311,11 +570,27 @@ __global__ void __launch_bounds__(kThreads) fixed_budget_kernel(const FixedArgs 
 
 }  // namespace
 
+int score_blocks_per_sm(int hidden_bf16) {
+    const int bytes = int(kScoreSmemBytes);
+    cudaError_t e =
+        hidden_bf16 ? cudaFuncSetAttribute(score_budget_kernel<uint16_t>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)
+                    : cudaFuncSetAttribute(score_budget_kernel<float>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return -1;
+    int n = 0;
+    e = hidden_bf16 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, score_budget_kernel<uint16_t>,
+                                                                    kScoreThreads, kScoreSmemBytes)
+                    : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, score_budget_kernel<float>,
+                                                                    kScoreThreads, kScoreSmemBytes);
+    return e == cudaSuccess ? n : -1;
+}
+
 cudaError_t launch_score_budget(const ScoreArgs &a, int grid, cudaStream_t s) {
     if (a.hidden_bf16)
-        score_budget_kernel<uint16_t><<<grid, kThreads, 0, s>>>(a);
+        score_budget_kernel<uint16_t><<<grid, kScoreThreads, kScoreSmemBytes, s>>>(a);
     else
-        score_budget_kernel<float><<<grid, kThreads, 0, s>>>(a);
+        score_budget_kernel<float><<<grid, kScoreThreads, kScoreSmemBytes, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -113,10 +113,6 @@ __device__ __forceinline__ void st_release(int *p, int v) {
 __device__ __forceinline__ void st_relaxed(int *p, int v) {
     asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar))
-                 : "memory");
-}
 
 // Cross-CTA state is read through L2 only (never a possibly stale L1 line).
 __device__ __forceinline__ DecideState load_state(const VerifyArgs &a, int b) {

@@ -55,6 +55,20 @@ def test_fixed_budget(cuda_lib, F):
     assert np.all(gpu["L"] == min(F, 8))
 
 
+# The cap's candidate sets on either side of the kernel's shared-memory
+# limits: 4096 listed keys, 8192 survival values held on chip.
+@pytest.mark.parametrize("B,T,c", [
+    (256, 1000, 0.0),    # exactly 4096 candidates: the listed select
+    (400, 2000, 0.0),    # 6400 candidates, curves on chip: the unlisted select
+    (600, 5000, 0.0),    # 9600 candidates, curves re-read from memory
+    (600, 700, 0.45),    # curves re-read from memory, fewer candidates
+])
+def test_cap_candidate_sets(cuda_lib, B, T, c):
+    inp = W.make_inputs(W.MIXED_B256, 20, B=B, V=256, d=64, cap_T=T, cost_c=c)
+    gpu, _, _ = run_and_compare(inp)
+    assert gpu["L"].sum() <= T
+
+
 # Small shapes: several vocab tiles (16 KB each) with a ragged tail, odd B and
 # gamma, both dtypes, both modes.
 SHAPES = [
