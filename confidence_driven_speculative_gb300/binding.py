@@ -69,6 +69,8 @@ def load():
             fn = getattr(lib, name)
             fn.argtypes = [SP, _P]
             fn.restype = ctypes.c_int
+        lib.dspark_verify_noalloc.argtypes = [SP, ctypes.c_int32, _P, _P]
+        lib.dspark_verify_noalloc.restype = ctypes.c_int
         lib.dspark_workspace_size.argtypes = [ctypes.c_int32] * 4
         lib.dspark_workspace_size.restype = ctypes.c_size_t
         lib.dspark_workspace_init.argtypes = [_P, ctypes.c_size_t, _P]
@@ -113,6 +115,21 @@ def dspark_compact(step: DsparkStep, stream=None, check: bool = True) -> int:
 
 def dspark_verify(step: DsparkStep, stream=None, check: bool = True) -> int:
     return _call("dspark_verify", step, stream, check)
+
+
+DSPARK_NOALLOC_SCRATCH_BYTES = 8 << 20
+
+
+def dspark_verify_noalloc(step: DsparkStep, reset: bool = False, status_out=None, stream=None,
+                          check: bool = True) -> int:
+    """dspark_verify on the library's fixed scratch (no workspace, no device
+    allocation); ``step.workspace`` is ignored.  ``status_out`` is a device
+    int32 tensor or None."""
+    rc = load().dspark_verify_noalloc(ctypes.byref(step), int(bool(reset)), _ptr(status_out),
+                                      _stream(stream))
+    if check and rc != DSPARK_OK:
+        raise DsparkError(rc, "dspark_verify_noalloc")
+    return rc
 
 
 def dspark_workspace_size(B: int, gamma: int, V: int, d: int) -> int:

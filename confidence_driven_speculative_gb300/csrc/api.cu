@@ -297,3 +297,88 @@ const char *dspark_last_error(void) { return g_err; }
 const char *dspark_version(void) { return "dspark-gb300 0.1.0 (sm_103a)"; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// dspark_verify_noalloc: dspark_verify with its scratch in a fixed array of
+// this library's device image instead of a caller workspace, for callers
+// that cannot allocate device memory at the call site.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kNoallocScratchBytes = size_t(8) << 20;
+static_assert(DSPARK_NOALLOC_SCRATCH_BYTES == kNoallocScratchBytes, "header and library agree");
+
+// One copy per device, created when the device loads this library's module
+// and held until the process exits.  In host code this name is only a
+// handle: the device address comes from cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
+
+// Per device: the array's device address and the shape of the last call.
+// The layout of the scratch follows (B, gamma, V); a new shape finds other
+// data where its counters go.
+struct NoallocSlot {
+    void *ptr = nullptr;
+    int32_t B = -1, gamma = -1, V = -1;
+};
+NoallocSlot g_noalloc[kMaxDevices];
+std::mutex g_noalloc_mu;
+
+}  // namespace
+
+extern "C" dspark_status dspark_verify_noalloc(const dspark_step *s, int32_t reset,
+                                               int32_t *status_out, dspark_stream_t stream) {
+    const char *fn = "dspark_verify_noalloc";
+    dspark_status st = check_shape(s);
+    if (st) return st;
+    const size_t need = dspark::workspace_layout(s->B, s->gamma, s->V).total;
+    if (need > kNoallocScratchBytes)
+        return fail(DSPARK_EWORKSPACE,
+                    "%s: B=%d gamma=%d V=%d needs %zu bytes of scratch; the static scratch holds %zu",
+                    fn, s->B, s->gamma, s->V, need, kNoallocScratchBytes);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(DSPARK_EDEVICE, "device index %d out of range", dev);
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    void *ptr = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_noalloc_mu);
+        NoallocSlot &slot = g_noalloc[dev];
+        if (!slot.ptr) {
+            // First call on this device (current now): find this device's
+            // copy of the array.
+            e = cudaGetSymbolAddress(&slot.ptr, g_noalloc_scratch);
+            if (e != cudaSuccess) {
+                slot.ptr = nullptr;
+                return cuda_fail(e, "cudaGetSymbolAddress(g_noalloc_scratch)");
+            }
+            if (!aligned(slot.ptr, 256)) {
+                slot.ptr = nullptr;
+                return fail(DSPARK_EWORKSPACE, "%s: static scratch misaligned", fn);
+            }
+        }
+        ptr = slot.ptr;
+        if (reset || s->B != slot.B || s->gamma != slot.gamma || s->V != slot.V) {
+            // The counters and queue flags of this shape must start at zero.
+            e = cudaMemsetAsync(ptr, 0, need, cs);
+            if (e != cudaSuccess) {
+                slot.B = slot.gamma = slot.V = -1;
+                return cuda_fail(e, "cudaMemsetAsync(static scratch)");
+            }
+            slot.B = s->B;
+            slot.gamma = s->gamma;
+            slot.V = s->V;
+        }
+    }
+    dspark_step local = *s;
+    local.workspace = ptr;
+    local.workspace_bytes = kNoallocScratchBytes;
+    if ((st = dspark_verify(&local, stream))) return st;
+    if (status_out) {
+        const dspark::WorkspaceLayout lay = dspark::workspace_layout(s->B, s->gamma, s->V);
+        e = cudaMemcpyAsync(status_out, static_cast<char *>(ptr) + lay.status, sizeof(int32_t),
+                            cudaMemcpyDeviceToDevice, cs);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync(status_out)");
+    }
+    return DSPARK_OK;
+}

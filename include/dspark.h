@@ -28,7 +28,8 @@
  * Conventions for every call:
  *   - Ownership: the caller owns all memory.  Every pointer in dspark_step is
  *     device memory of the current CUDA device unless marked otherwise.  The
- *     library allocates nothing and keeps no pointer after a call returns.
+ *     library allocates nothing and keeps no pointer after a call returns
+ *     (dspark_verify_noalloc's scratch is a fixed array of the library).
  *   - Asynchrony: calls enqueue kernels on `stream` and return; no call
  *     synchronises with the host.  Totals that depend on data (sum of L,
  *     number of packed rows) stay on the device; grids are sized for the
@@ -211,6 +212,52 @@ dspark_status dspark_verify(const dspark_step *step, dspark_stream_t stream);
  */
 dspark_status dspark_read_device_status(const void *workspace, int32_t *status_out,
                                         dspark_stream_t stream);
+
+/*
+ * Bytes of the fixed scratch that dspark_verify_noalloc uses instead of a
+ * workspace: 8 MiB, enough for B = 512 at gamma = 16 and V = 151936.
+ */
+#define DSPARK_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+
+/*
+ * dspark_verify without a caller workspace.  The pages have no counterpart:
+ * this is a calling convention of this library, not a step of the method.
+ *
+ * For callers that cannot allocate device memory where they call the verify
+ * step: a serving runtime whose device memory belongs to its own caching
+ * allocator, with no hook to borrow a buffer from it at this call site, or a
+ * step loop that must not allocate between its set-up and its steps.  The
+ * scratch is one array of DSPARK_NOALLOC_SCRATCH_BYTES in this library's
+ * device image, one copy per device, held until the process exits.  No call
+ * allocates or frees device memory.
+ *
+ * Inputs, outputs, errors and results are those of dspark_verify;
+ * step->workspace and step->workspace_bytes are ignored.  A shape whose
+ * workspace (dspark_workspace_size) exceeds DSPARK_NOALLOC_SCRATCH_BYTES is
+ * rejected with DSPARK_EWORKSPACE before anything is enqueued.
+ *
+ * The first call on a device sets up: with that device current it looks up
+ * the device's copy of the array.  Make that first call before any stream
+ * capture.  The scratch's counters and queue flags must start at zero, and
+ * where they sit depends on (B, gamma, V): the first call on a device, and
+ * every call whose (B, gamma, V) differs from the previous call's there,
+ * zeroes the first dspark_workspace_size() bytes of the scratch
+ * (cudaMemsetAsync on `stream`) before the launch.  A launch that ends with
+ * a zero device status leaves them at zero for the next call of that shape.
+ *
+ * reset:      nonzero zeroes them in any case.  Pass it after a call whose
+ *             status was nonzero.
+ * status_out: device int32, or NULL.  When set, it receives the scratch's
+ *             device status word after the launch (meaning as in
+ *             dspark_read_device_status: 0 = healthy).
+ *
+ * Every call on a device shares the one array and finds the last call's
+ * contents in it.  Calls whose kernels may overlap on the GPU (other
+ * streams, other host threads) race on it and give wrong results: order
+ * them on one stream or synchronise between them.
+ */
+dspark_status dspark_verify_noalloc(const dspark_step *step, int32_t reset,
+                                    int32_t *status_out, dspark_stream_t stream);
 
 /* Thread-local message for the last failing call on this thread ("" if none). */
 const char *dspark_last_error(void);
