@@ -84,13 +84,16 @@ struct VSmem {
 };
 
 // Grid-wide shape of the stream work, the same in every thread.  Rows
-// below nA are one chunk each; the remaining rows are cut into chunks of Cb
-// tiles (gprb per row) so the last wave of work balances finely.
+// below nA are one chunk each; rows [nA, nB) are cut into chunks of Cb
+// tiles (gprb per row); rows from nB on go out tile by tile, so the last
+// wave of work balances finely.
 struct StreamShape {
     int n_rows;    // packed rows
     int nA;        // rows handed out whole
-    int Cb;        // tiles per chunk in the remaining rows
-    int gprb;      // chunks per remaining row
+    int nB;        // first row handed out in single tiles
+    int Cb;        // tiles per chunk in rows [nA, nB)
+    int gprb;      // chunks per row in rows [nA, nB)
+    int nq;        // chunks of rows [nA, nB)
     int n_chunks;
 };
 
@@ -141,16 +144,20 @@ __device__ __forceinline__ StreamShape stream_shape(const VerifyArgs &a) {
     sh.n_rows = min(max(a.row_off[a.B], 0), a.B * (a.gamma + 1));
     const long long n_tiles = (long long)sh.n_rows * a.nc;
     if (n_tiles >= 32LL * gridDim.x) {
-        // many rows: whole rows, except the last gridDim.x rows in quarters
+        // many rows: whole rows, then the last gridDim.x rows in quarters
+        // (single-tile chunks would outrun the producer's metadata fetches)
         sh.nA = max(0, sh.n_rows - int(gridDim.x));
+        sh.nB = sh.n_rows;
         sh.Cb = max(1, a.nc / 4);
     } else {
         // few rows: single tiles
         sh.nA = 0;
+        sh.nB = 0;
         sh.Cb = 1;
     }
     sh.gprb = (a.nc + sh.Cb - 1) / sh.Cb;
-    sh.n_chunks = sh.nA + (sh.n_rows - sh.nA) * sh.gprb;
+    sh.nq = (sh.nB - sh.nA) * sh.gprb;
+    sh.n_chunks = sh.nA + sh.nq + (sh.n_rows - sh.nB) * a.nc;
     return sh;
 }
 
@@ -266,10 +273,14 @@ __device__ __forceinline__ void fetch_step(const VerifyArgs &a, const StreamShap
         if (f.c < sh.nA) {
             f.r = f.c;
             f.g = 0;
-        } else {
+        } else if (f.c < sh.nA + sh.nq) {
             const int cc = f.c - sh.nA;
             f.r = sh.nA + cc / sh.gprb;
             f.g = cc - (f.r - sh.nA) * sh.gprb;
+        } else {
+            const int cc = f.c - sh.nA - sh.nq;
+            f.r = sh.nB + cc / a.nc;
+            f.g = cc - (f.r - sh.nB) * a.nc;
         }
         f.b = a.row_req[f.r];
         f.k = a.row_k[f.r];
@@ -359,7 +370,7 @@ __device__ void producer(const VerifyArgs &a, VSmem &sm, uint8_t *ring, const St
                 ck = nextc.k;
                 cLb = nextc.Lb;
                 cd = nextc.d;
-                const int C = cr < sh.nA ? a.nc : sh.Cb;
+                const int C = cr < sh.nA ? a.nc : cr < sh.nB ? sh.Cb : 1;
                 cj = cg * C;
                 cj_end = min(a.nc, cj + C);
                 in_chunk = true;
@@ -446,11 +457,31 @@ __device__ void producer(const VerifyArgs &a, VSmem &sm, uint8_t *ring, const St
 // ---------------------------------------------------------------------------
 // decisions (warp-level)
 // ---------------------------------------------------------------------------
-__device__ void finish_request(const VerifyArgs &a, int b, int acc, int token, int lane) {
+// Draft tokens d_{b, lane} and d_{b, lane + 32} of a request, loaded once per
+// decision (gamma <= 64).
+struct Drafts {
+    int t[2];
+};
+
+__device__ __forceinline__ Drafts load_drafts(const VerifyArgs &a, int b, int lane) {
+    Drafts d;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int k = lane + 32 * i;
+        d.t[i] = k < a.gamma ? __ldcg(a.draft_tokens + size_t(b) * a.gamma + k) : -1;
+    }
+    return d;
+}
+
+__device__ void finish_request(const VerifyArgs &a, int b, int acc, int token, const Drafts &dr,
+                               int lane) {
     const int g1 = a.gamma + 1;
-    for (int j = lane; j < g1; j += 32) {
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+        const int j = lane + 32 * i;
+        if (j >= g1) continue;
         int v = -1;
-        if (j < acc) v = a.draft_tokens[size_t(b) * a.gamma + j];
+        if (j < acc) v = dr.t[i < 2 ? i : 1];
         else if (j == acc) v = token;
         a.out_tokens[size_t(b) * g1 + j] = v;
     }
@@ -536,11 +567,10 @@ __device__ __forceinline__ float pair_sum(const float (&w)[VE]) {
 // the last id with positive weight.  The rows were streamed moments
 // earlier, so the loads hit L2.
 template <typename T>
-__device__ int slot_pick(const VerifyArgs &a, const DecideState &st, int b, int y0, int n,
+__device__ int slot_pick(const VerifyArgs &a, const DecideState &st, int b, int r, int y0, int n,
                          double target, int lane) {
     constexpr int VE = Vec<T>::kElems;
     constexpr int kRunVec = 4;  // n = 32 lanes x 4 vectors (1024 bf16 / 512 fp32 ids)
-    const int r = a.row_off[b] + (st.mode == D_BONUS ? verify_len(a, b) : st.a);
     const uint4 *tv = reinterpret_cast<const uint4 *>(static_cast<const char *>(a.target_logits) +
                                                       size_t(r) * a.row_bytes);
     const uint4 *dv = reinterpret_cast<const uint4 *>(
@@ -623,11 +653,11 @@ __device__ int slot_pick(const VerifyArgs &a, const DecideState &st, int b, int 
     return __shfl_sync(0xffffffffu, pick, lsel);
 }
 
-// The token inside sampling block `blk`, given the block's per-warp slot
-// masses sm_w (w < wpb, in every lane): the slot whose running mass crosses
-// u_tok times the block mass, then the id inside that slot.
+// The token inside sampling block `blk` of packed target row r, given the
+// block's per-warp slot masses sm_w (w < wpb, in every lane): the slot whose
+// running mass crosses u_tok times the block mass, then the id inside it.
 template <typename T>
-__device__ int block_pick(const VerifyArgs &a, const DecideState &st, int b, int blk,
+__device__ int block_pick(const VerifyArgs &a, const DecideState &st, int b, int r, int blk,
                           const double (&slot_mass)[kCW], int wpb, int tpw, int lane) {
     double total = 0.0;
 #pragma unroll
@@ -655,34 +685,7 @@ __device__ int block_pick(const VerifyArgs &a, const DecideState &st, int b, int
         for (int w = 0; w < kCW; ++w)
             if (w < wsel) before += slot_mass[w];
     }
-    return slot_pick<T>(a, st, b, blk * kSampleBlock + wsel * tpw, tpw, target - before, lane);
-}
-
-// Fold the chunk records of packed row r (fixed order).
-__device__ __forceinline__ float4 fold_row(const VerifyArgs &a, const StreamShape &sh, int r,
-                                           float scale) {
-    const float4 *rec = a.rowrec + size_t(r) * a.grp_stride;
-    const int n = r < sh.nA ? 1 : sh.gprb;
-    float4 acc = a.greedy ? make_float4(-INFINITY, __int_as_float(INT_MAX), 0.f, 0.f)
-                          : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
-    for (int i0 = 0; i0 < n; i0 += 8) {
-        float4 x[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) x[u] = i0 + u < n ? __ldcg(rec + i0 + u) : acc;
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            if (i0 + u >= n) continue;
-            if (a.greedy) {
-                int bi = __float_as_int(acc.y);
-                am_combine(acc.x, bi, x[u].x, __float_as_int(x[u].y));
-                acc.y = __int_as_float(bi);
-            } else {
-                ms_combine(acc.x, acc.y, x[u].x, x[u].y, scale);
-                ms_combine(acc.z, acc.w, x[u].z, x[u].w, scale);
-            }
-        }
-    }
-    return acc;
+    return slot_pick<T>(a, st, b, r, blk * kSampleBlock + wsel * tpw, tpw, target - before, lane);
 }
 
 // (max, sum) of p over sampling block i of request b's bonus row, from the
@@ -700,44 +703,88 @@ __device__ __forceinline__ float2 bonus_block(const VerifyArgs &a, int b, int i,
 }
 
 // Request b's stream tiles are all in: accept tests, outputs of the draft
-// rows, and either the whole bonus draw or the residual jobs.
+// rows, and either the whole bonus draw or the residual jobs.  Loads that do
+// not depend on one another are issued together: a decision runs while the
+// streaming keeps L2 busy, and each dependent round trip costs microseconds.
 template <typename T>
 __device__ void decide_request(const VerifyArgs &a, const StreamShape &sh, int b, int wpb,
                                int epoch, int lane) {
+    // Round 1: lengths, offsets, draft tokens and the bonus row's slots.
     const int Lb = verify_len(a, b), r0 = a.row_off[b], d0 = a.draft_off[b];
+    const Drafts dr = load_drafts(a, b, lane);
     const float scale = a.scale;
+    constexpr int kCache = 2;  // blocks per lane kept in registers (nblk <= 64)
+    float2 sl[kCache][kCW];
+#pragma unroll
+    for (int q = 0; q < kCache; ++q) {
+        const int i = q * 32 + lane;
+        const float2 *p = a.blkrec + (size_t(b) * a.nblk + (i < a.nblk ? i : 0)) * kCW;
+#pragma unroll
+        for (int w = 0; w < kCW; ++w)
+            sl[q][w] = !a.greedy && i < a.nblk && w < wpb ? __ldcg(p + w)
+                                                           : make_float2(-INFINITY, 0.f);
+    }
     int ab = Lb;                                   // first rejected draft (L_b: none)
     float Mp = 0.f, Sp = 0.f, Mq = 0.f, Sq = 0.f;  // normalisers of row a_b (sampling)
+    float ub = 0.f, ut = 0.f;                      // block / token uniforms of row a_b
     int g_tok = 0;
-    // One lane per row k (two rounds when gamma >= 32).  In sampling mode
-    // the bonus row has no row record; it is drawn from its block slots.
+    // Round 2, one lane per row k (more rounds when gamma >= 32): the row's
+    // chunk records and its gathered z values.  In sampling mode the bonus
+    // row has no row record; it is drawn from its block slots.
     for (int base = 0; base <= Lb; base += 32) {
         const int k = base + lane;
         const bool live = a.greedy ? k <= Lb : k < Lb;
-        float4 rr = make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
-        bool accept = false;
+        const int r = r0 + k;
+        const int nrec = r < sh.nA ? 1 : r < sh.nB ? sh.gprb : a.nc;
+        const float4 *rec = a.rowrec + size_t(live ? r : r0) * a.grp_stride;
+        float4 x[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            x[u] = live && u < nrec ? __ldcg(rec + u) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float2 z = !a.greedy && live ? __ldcg(a.gath + r) : make_float2(0.f, 0.f);
+        // the uniforms of every row this round could stop at (k == L_b: bonus)
+        float u = 1.f, u1 = 0.f, u2 = 0.f;
+        if (!a.greedy && k <= Lb) step_uniforms(a.seed, b, k, u, u1, u2);
+        float4 rr = a.greedy ? make_float4(-INFINITY, __int_as_float(INT_MAX), 0.f, 0.f)
+                             : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
         if (live) {
-            rr = fold_row(a, sh, r0 + k, scale);
-            if (k < Lb) {
-                const int dt = a.draft_tokens[size_t(b) * a.gamma + k];
-                if (a.greedy) {
-                    accept = dt == __float_as_int(rr.y);
-                    a.p_tok[d0 + k] = 0.f;
-                    a.q_tok[d0 + k] = 0.f;
-                } else {
-                    float p = 0.f, q = 0.f, ratio = 0.f;
-                    if (dt >= 0 && dt < a.V) {
-                        const float2 z = __ldcg(a.gath + r0 + k);
-                        p = exp2_approx((z.x - rr.x) * scale) / rr.y;
-                        q = exp2_approx((z.y - rr.z) * scale) / rr.w;
-                        ratio = q > 0.f ? fminf(1.f, p / q) : 1.f;
-                    }
-                    float u, ub, ut;
-                    step_uniforms(a.seed, b, k, u, ub, ut);
-                    accept = u < ratio;
-                    a.p_tok[d0 + k] = p;
-                    a.q_tok[d0 + k] = q;
+            for (int i0 = 0; i0 < nrec; i0 += 4) {
+                if (i0 > 0) {
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        if (i0 + v < nrec) x[v] = __ldcg(rec + i0 + v);
                 }
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    if (i0 + v >= nrec) continue;
+                    if (a.greedy) {
+                        int bi = __float_as_int(rr.y);
+                        am_combine(rr.x, bi, x[v].x, __float_as_int(x[v].y));
+                        rr.y = __int_as_float(bi);
+                    } else {
+                        ms_combine(rr.x, rr.y, x[v].x, x[v].y, scale);
+                        ms_combine(rr.z, rr.w, x[v].z, x[v].w, scale);
+                    }
+                }
+            }
+        }
+        bool accept = false;
+        if (live && k < Lb) {
+            const int dt = base == 0 ? dr.t[0] : dr.t[1];
+            if (a.greedy) {
+                accept = dt == __float_as_int(rr.y);
+                a.p_tok[d0 + k] = 0.f;
+                a.q_tok[d0 + k] = 0.f;
+            } else {
+                float p = 0.f, q = 0.f, ratio = 0.f;
+                if (dt >= 0 && dt < a.V) {
+                    p = exp2_approx((z.x - rr.x) * scale) / rr.y;
+                    q = exp2_approx((z.y - rr.z) * scale) / rr.w;
+                    ratio = q > 0.f ? fminf(1.f, p / q) : 1.f;
+                }
+                accept = u < ratio;
+                a.p_tok[d0 + k] = p;
+                a.q_tok[d0 + k] = q;
             }
         }
         const unsigned acc = __ballot_sync(0xffffffffu, live && k < Lb && accept);
@@ -745,44 +792,37 @@ __device__ void decide_request(const VerifyArgs &a, const StreamShape &sh, int b
         const unsigned rej = rows & ~acc;
         if (ab == Lb && rej) ab = base + __ffs(rej) - 1;
         const int src = ab - base;
-        const int sl = src >= 0 && src < 32 ? src : 0;
-        const float m1 = __shfl_sync(0xffffffffu, rr.x, sl), s1 = __shfl_sync(0xffffffffu, rr.y, sl);
-        const float m2 = __shfl_sync(0xffffffffu, rr.z, sl), s2 = __shfl_sync(0xffffffffu, rr.w, sl);
+        const int sl_ = src >= 0 && src < 32 ? src : 0;
+        const float m1 = __shfl_sync(0xffffffffu, rr.x, sl_), s1 = __shfl_sync(0xffffffffu, rr.y, sl_);
+        const float m2 = __shfl_sync(0xffffffffu, rr.z, sl_), s2 = __shfl_sync(0xffffffffu, rr.w, sl_);
+        const float v1 = __shfl_sync(0xffffffffu, u1, sl_), v2 = __shfl_sync(0xffffffffu, u2, sl_);
         if (src >= 0 && src < 32) {
             Mp = m1;
             Sp = s1;
             Mq = m2;
             Sq = s2;
+            ub = v1;
+            ut = v2;
             g_tok = __float_as_int(s1);  // greedy: the row's argmax
         }
     }
     if (a.greedy) {
-        finish_request(a, b, ab, g_tok, lane);
+        finish_request(a, b, ab, g_tok, dr, lane);
         return;
     }
-    float u, ub, ut;
-    step_uniforms(a.seed, b, ab, u, ub, ut);
     DecideState st;
     st.a = ab;
     st.u_blk = ub;
     st.u_tok = ut;
     if (ab == Lb) {
-        // Bonus draw from p of row L_b, done here: block and slot masses from
-        // its per-warp slots (lane-owned blocks cached in registers).
-        constexpr int kCache = 2;  // blocks per lane kept in registers (nblk <= 64)
-        float2 sl[kCache][kCW];
+        // Bonus draw from p of row L_b: block and slot masses from its
+        // per-warp slots (lane-owned blocks already in registers).
         float mb = -INFINITY;
 #pragma unroll
-        for (int q = 0; q < kCache; ++q) {
-            const int i = q * 32 + lane;
-            const float2 *p = a.blkrec + (size_t(b) * a.nblk + (i < a.nblk ? i : 0)) * kCW;
-#pragma unroll
-            for (int w = 0; w < kCW; ++w)
-                sl[q][w] = i < a.nblk && w < wpb ? __ldcg(p + w) : make_float2(-INFINITY, 0.f);
+        for (int q = 0; q < kCache; ++q)
 #pragma unroll
             for (int w = 0; w < kCW; ++w)
                 if (sl[q][w].y > 0.f) mb = fmaxf(mb, sl[q][w].x);
-        }
         for (int i = kCache * 32 + lane; i < a.nblk; i += 32) {
             const float2 x = bonus_block(a, b, i, wpb, scale);
             if (x.y > 0.f) mb = fmaxf(mb, x.x);
@@ -828,8 +868,9 @@ __device__ void decide_request(const VerifyArgs &a, const StreamShape &sh, int b
         st.Sp = 1.f;
         st.Mq = 0.f;
         st.Sq = 1.f;
-        const int token = block_pick<T>(a, st, b, blk, slot_mass, wpb, kSampleBlock / wpb, lane);
-        finish_request(a, b, ab, token, lane);
+        const int token =
+            block_pick<T>(a, st, b, r0 + Lb, blk, slot_mass, wpb, kSampleBlock / wpb, lane);
+        finish_request(a, b, ab, token, dr, lane);
     } else {
         st.mode = D_RESID;
         st.Mp = Mp;
@@ -847,7 +888,10 @@ __device__ void decide_request(const VerifyArgs &a, const StreamShape &sh, int b
 // then the slot, then the token.
 template <typename T>
 __device__ void finish_residual(const VerifyArgs &a, int b, int wpb, int lane) {
+    // One round of independent loads: state, row offset, drafts, masses.
     DecideState st = load_state(a, b);
+    const int r0 = a.row_off[b];
+    const Drafts dr = load_drafts(a, b, lane);
     const float2 *z = a.zrec + size_t(b) * a.nblk * kCW;
     constexpr int kCache = 2;  // blocks per lane kept in registers (nblk <= 64)
     float2 sl[kCache][kCW];
@@ -905,8 +949,9 @@ __device__ void finish_residual(const VerifyArgs &a, int b, int wpb, int lane) {
             slot_mass[w] = w < wpb ? double(m) : 0.0;
         }
     }
-    const int token = block_pick<T>(a, st, b, blk, slot_mass, wpb, kSampleBlock / wpb, lane);
-    finish_request(a, b, st.a, token, lane);
+    const int token =
+        block_pick<T>(a, st, b, r0 + st.a, blk, slot_mass, wpb, kSampleBlock / wpb, lane);
+    finish_request(a, b, st.a, token, dr, lane);
 }
 
 // ---------------------------------------------------------------------------
