@@ -272,6 +272,9 @@ dspark_status dspark_verify(const dspark_step *s, dspark_stream_t stream) {
     a.qb_ready = ws_at<int32_t>(s, lay.qb_ready);
     a.req_cnt = ws_at<int32_t>(s, lay.verify_cnt);
     a.r1_cnt = ws_at<int32_t>(s, lay.r1_cnt);
+    a.bon_cnt = ws_at<int32_t>(s, lay.bon_cnt);
+    a.join = ws_at<int32_t>(s, lay.join);
+    a.rejflag = ws_at<int32_t>(s, lay.rejflag);
     a.status = ws_at<int32_t>(s, lay.status);
     // One CTA per resident slot: the cooperative launch requires it, and the
     // work is spread over the grid inside the kernel.

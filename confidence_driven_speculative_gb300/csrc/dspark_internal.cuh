@@ -42,6 +42,9 @@ struct WorkspaceLayout {
     size_t score_rows;    // int32 [1]   hidden rows claimed
     size_t verify_cnt;    // int32 [B]   per-request stream tiles done
     size_t r1_cnt;        // int32 [B]   per-request residual tiles done
+    size_t bon_cnt;       // int32 [B]   per-request bonus-row tiles done
+    size_t join;          // int32 [B]   drafts all accepted + bonus row streamed
+    size_t rejflag;       // int32 [B]   launch epoch of a found rejection
     size_t q_ctr;         // int32 [8]   queue head, tail, finished, exited, epoch, chunk
     size_t rowrec;        // float4 [B*(gamma+1) * nc]      row partials per (row, chunk)
     size_t blkrec;        // float2 [B * nblk * 8]          bonus-row block partials per warp
@@ -74,6 +77,9 @@ inline WorkspaceLayout workspace_layout(int B, int gamma, int V) {
     w.score_rows = off;  off = align256(off + sizeof(int32_t));
     w.verify_cnt = off;  off = align256(off + sizeof(int32_t) * size_t(B));
     w.r1_cnt = off;      off = align256(off + sizeof(int32_t) * size_t(B));
+    w.bon_cnt = off;     off = align256(off + sizeof(int32_t) * size_t(B));
+    w.join = off;        off = align256(off + sizeof(int32_t) * size_t(B));
+    w.rejflag = off;     off = align256(off + sizeof(int32_t) * size_t(B));
     w.q_ctr = off;       off = align256(off + sizeof(int32_t) * 8);
     w.rowrec = off;      off = align256(off + 16 * rows * size_t(w.nc));
     w.blkrec = off;      off = align256(off + 8 * size_t(B) * w.nblk * warps);
@@ -330,6 +336,7 @@ struct VerifyArgs {
     int32_t *q_ready, *q_ctr;
     int32_t *qb_job, *qb_ready;
     int32_t *req_cnt, *r1_cnt, *status;
+    int32_t *bon_cnt, *join, *rejflag;
 };
 
 cudaError_t launch_score_budget(const ScoreArgs &a, int grid, cudaStream_t s);

@@ -12,32 +12,36 @@
 // unchanged.
 //
 // Design (GB300).  The pass is HBM-bound: every packed target row (sum L + B)
-// and every kept draft row (sum L) is read once, V logits each.
+// and every kept draft row (sum L) is read at most once, V logits each.
 //
-//  * One persistent cooperative grid, 2 CTAs per SM; each CTA is one producer
-//    warp and 8 consumer warps.  The producer's lane 0 fills a 3-stage
-//    shared-memory ring with 1-D bulk TMA copies (cp.async.bulk) completing
-//    on "full" mbarriers with byte counts; each consumer warp releases a
-//    stage on its "empty" mbarrier.  No block-wide barrier in the loop.
-//  * Stream work is a queue of chunks -- whole packed rows (or single 16 KB
-//    tiles for small batches) -- handed out in row order by an atomic
-//    counter, so requests finish progressively while the grid streams.  Row
-//    r of request b at index k < L_b is a pair (target row, draft row
-//    (b, k)); k = L_b is the bonus row.
+//  * One persistent cooperative grid, 2 CTAs per SM; each CTA is a producer
+//    warp, 8 consumer warps and a decider warp.  The producer's lane 0 fills
+//    a 3-stage shared-memory ring with 1-D bulk TMA copies (cp.async.bulk)
+//    completing on "full" mbarriers with byte counts; each consumer warp
+//    releases a stage on its "empty" mbarrier.  No block-wide barrier in the
+//    loop.
+//  * Stream work is a queue of chunks handed out by an atomic counter, in
+//    two phases.  Phase P streams the decision rows (k < L_b: target row k
+//    with draft row (b, k) in sampling) in packed-row order, whole rows and
+//    then quarter rows for the last wave (single 16 KB tiles for small
+//    batches).  Phase Q streams each request's bonus row (k = L_b), skipping
+//    requests already known to reject: the method never reads past the
+//    first rejection.
 //  * A consumer warp owns one eighth of every tile.  For a pair row its
 //    lanes keep online (max, sum of 2^(z log2(e)/Tm - max)) accumulators for
-//    p and q across all tiles of the chunk and reduce once, at the chunk's
-//    end, into the warp's own record slot (plain stores: deterministic).  A
+//    p and q across the tiles of the chunk and reduce once, at the chunk's
+//    end, into a record slot of the row (plain stores: deterministic).  A
 //    bonus row stores one slot per tile and warp, which gives the per-block
 //    masses of the draw.  Greedy rows keep (max, lowest argmax).
 //  * The producer books the stages it gets back: tiles are counted per
-//    request locally and published with one fenced atomic per request
-//    change; a completed request becomes a "decide" job on a device-wide
-//    queue that every producer serves before its own chunks.  Jobs: decide
-//    (accept tests with Philox uniforms, p(d)/q(d), the bonus block choice),
-//    residual mass (one tile of the rejecting row pair, read again while it
-//    is still in L2), block choice, and pick (one 4096-id block).  All flow
-//    through the same TMA ring, spread over the whole GPU.
+//    (request, decision / bonus) locally and published with one fenced
+//    atomic per change.  A request whose decision rows are in becomes a
+//    decide job; its bonus row being in, together with every draft accepted
+//    (a join counter), makes the bonus-draw job.  Decider warps serve these
+//    jobs from a device-wide queue.  A rejection queues residual-mass jobs
+//    (one tile of the rejecting row pair, read again while it is still in
+//    L2), which producers serve through their rings before their own chunks;
+//    the last of them queues the residual draw.
 //  * Draws are two-level: a 4096-id block by mass (u'), then an id inside it
 //    (u''); in-block running sums are fp32 over short lane runs combined in
 //    fp64.
@@ -83,10 +87,14 @@ struct VSmem {
     int done[kStages];          // warps finished with a chunk's last tile
 };
 
-// Grid-wide shape of the stream work, the same in every thread.  Rows
-// below nA are one chunk each; rows [nA, nB) are cut into chunks of Cb
-// tiles (gprb per row); rows from nB on go out tile by tile, so the last
-// wave of work balances finely.
+// Grid-wide shape of the stream work, the same in every thread.  Two
+// phases.  Phase P walks the packed rows and streams the decision rows
+// (k < L_b; a bonus row's chunks are claimed and skipped): rows below nA are
+// one chunk each, rows [nA, nB) are cut into chunks of Cb tiles (gprb per
+// row), rows from nB on go out tile by tile.  Phase Q streams each
+// request's bonus row (k = L_b) in chunks of CbQ tiles, skipping requests
+// already known to reject.  So the accept tests -- and the residual draws
+// they start -- run while the bonus rows are still streaming.
 struct StreamShape {
     int n_rows;    // packed rows
     int nA;        // rows handed out whole
@@ -94,7 +102,10 @@ struct StreamShape {
     int Cb;        // tiles per chunk in rows [nA, nB)
     int gprb;      // chunks per row in rows [nA, nB)
     int nq;        // chunks of rows [nA, nB)
-    int n_chunks;
+    int nP;        // chunks of phase P
+    int CbQ;       // tiles per chunk of a bonus row
+    int gprbQ;     // chunks per bonus row
+    int n_chunks;  // phase P and phase Q
 };
 
 // ---------------------------------------------------------------------------
@@ -145,19 +156,24 @@ __device__ __forceinline__ StreamShape stream_shape(const VerifyArgs &a) {
     const long long n_tiles = (long long)sh.n_rows * a.nc;
     if (n_tiles >= 32LL * gridDim.x) {
         // many rows: whole rows, then the last gridDim.x rows in quarters
-        // (single-tile chunks would outrun the producer's metadata fetches)
+        // (quarters everywhere, or single-tile chunks, cost more in chunk
+        // overhead than they gain in balance)
         sh.nA = max(0, sh.n_rows - int(gridDim.x));
         sh.nB = sh.n_rows;
         sh.Cb = max(1, a.nc / 4);
+        sh.CbQ = sh.Cb;
     } else {
         // few rows: single tiles
         sh.nA = 0;
         sh.nB = 0;
         sh.Cb = 1;
+        sh.CbQ = 1;
     }
     sh.gprb = (a.nc + sh.Cb - 1) / sh.Cb;
     sh.nq = (sh.nB - sh.nA) * sh.gprb;
-    sh.n_chunks = sh.nA + sh.nq + (sh.n_rows - sh.nB) * a.nc;
+    sh.nP = sh.nA + sh.nq + (sh.n_rows - sh.nB) * a.nc;
+    sh.gprbQ = (a.nc + sh.CbQ - 1) / sh.CbQ;
+    sh.n_chunks = sh.nP + a.B * sh.gprbQ;
     return sh;
 }
 
@@ -221,9 +237,8 @@ __device__ void push_resid_jobs(const VerifyArgs &a, int b, int epoch) {
 }
 
 // Decider jobs, served by the decider warps: decide request b, or (with
-// kFinishResidual set) finish its residual draw.
-constexpr int kFinishResidual = 1 << 30;
-
+// kFinishResidual / kBonusDraw set) finish its residual draw / make its
+// bonus draw.
 __device__ void push_decide(const VerifyArgs &a, int job, int epoch) {
     const int pos = atomicAdd(&a.q_ctr[QB_TAIL], 1);
     if (pos < a.qbcap) {
@@ -256,64 +271,102 @@ __device__ TaskInfo resid_task(const VerifyArgs &a, int2 jb) {
 // The next chunk, fetched over several fills so that its global loads
 // (counter, row ids, request metadata) never stall the issue of a tile.
 struct ChunkFetch {
-    int stage;  // 0: claim an index, 1: row ids, 2: request data, 3: ready, 4: none left
-    int c, r, g, b, k, Lb, d;
+    // 0: claim an index, 1: row ids, 2: request data, 3: keep or skip,
+    // 4: ready, 5: none left
+    int stage;
+    int c, q, r, g, b, k, Lb, d, rej;
 };
 
 __device__ __forceinline__ void fetch_step(const VerifyArgs &a, const StreamShape &sh,
-                                           ChunkFetch &f) {
+                                           ChunkFetch &f, int epoch) {
     if (f.stage == 0) {
         f.c = int(gridDim.x) + atomicAdd(&a.q_ctr[Q_CHUNK], 1);
         f.stage = 1;
     } else if (f.stage == 1) {
         if (f.c >= sh.n_chunks) {
-            f.stage = 4;
+            f.stage = 5;
             return;
         }
-        if (f.c < sh.nA) {
-            f.r = f.c;
-            f.g = 0;
-        } else if (f.c < sh.nA + sh.nq) {
-            const int cc = f.c - sh.nA;
-            f.r = sh.nA + cc / sh.gprb;
-            f.g = cc - (f.r - sh.nA) * sh.gprb;
+        f.q = f.c >= sh.nP;
+        if (f.q) {
+            // phase Q: the bonus row of request b
+            const int cc = f.c - sh.nP;
+            f.b = cc / sh.gprbQ;
+            f.g = cc - f.b * sh.gprbQ;
+            f.r = a.row_off[f.b + 1] - 1;
+            f.rej = ld_relaxed(&a.rejflag[f.b]);
         } else {
-            const int cc = f.c - sh.nA - sh.nq;
-            f.r = sh.nB + cc / a.nc;
-            f.g = cc - (f.r - sh.nB) * a.nc;
+            if (f.c < sh.nA) {
+                f.r = f.c;
+                f.g = 0;
+            } else if (f.c < sh.nA + sh.nq) {
+                const int cc = f.c - sh.nA;
+                f.r = sh.nA + cc / sh.gprb;
+                f.g = cc - (f.r - sh.nA) * sh.gprb;
+            } else {
+                const int cc = f.c - sh.nA - sh.nq;
+                f.r = sh.nB + cc / a.nc;
+                f.g = cc - (f.r - sh.nB) * a.nc;
+            }
+            f.b = a.row_req[f.r];
+            f.k = a.row_k[f.r];
+            f.rej = 0;
         }
-        f.b = a.row_req[f.r];
-        f.k = a.row_k[f.r];
         f.stage = 2;
     } else if (f.stage == 2) {
         f.Lb = verify_len(a, f.b);
-        f.d = f.k < a.gamma ? a.draft_tokens[size_t(f.b) * a.gamma + f.k] : -1;
+        if (f.q) {
+            f.k = f.Lb;
+            f.d = -1;
+        } else {
+            f.d = f.k < a.gamma ? a.draft_tokens[size_t(f.b) * a.gamma + f.k] : -1;
+        }
         f.stage = 3;
+    } else if (f.stage == 3) {
+        // phase P skips bonus rows; phase Q skips requests already rejected
+        const bool skip = f.q ? f.rej == epoch : f.k >= f.Lb;
+        f.stage = skip ? 0 : 4;
     }
 }
 
 // Books of the stages the producer gets back: stream tiles are counted per
-// request locally and published with one fenced atomic per request change;
-// a request whose count completes goes to the decide queue.
+// (request, kind) locally and published with one fenced atomic per change.
+// Decision-row tiles complete a request's decide job.  Bonus-row tiles
+// complete its bonus row; the bonus draw then runs once the decide has
+// accepted every draft (join counter), at once when there are no drafts.
+constexpr int kFinishResidual = 1 << 30;  // decider job: finish the residual draw
+constexpr int kBonusDraw = 1 << 29;       // decider job: the bonus draw
+
 struct Books {
-    int acc_b, acc_n, acc_total;
+    int acc_b, acc_kind, acc_n, acc_total, acc_Lb;
 };
 
 __device__ void flush_books(const VerifyArgs &a, Books &bk, int epoch) {
     if (bk.acc_n == 0) return;
     __threadfence();
-    const int old = atomicAdd(&a.req_cnt[bk.acc_b], bk.acc_n);
-    if (old + bk.acc_n == bk.acc_total) push_decide(a, bk.acc_b, epoch);
+    const int b = bk.acc_b;
+    if (bk.acc_kind == 0) {
+        const int old = atomicAdd(&a.req_cnt[b], bk.acc_n);
+        if (old + bk.acc_n == bk.acc_total) push_decide(a, b, epoch);
+    } else {
+        const int old = atomicAdd(&a.bon_cnt[b], bk.acc_n);
+        if (old + bk.acc_n == bk.acc_total &&
+            (bk.acc_Lb == 0 || atomicAdd(&a.join[b], 1) == 1))
+            push_decide(a, b | kBonusDraw, epoch);
+    }
     bk.acc_n = 0;
 }
 
 __device__ __forceinline__ void account(const VerifyArgs &a, Books &bk, const TaskInfo &t,
                                         int epoch) {
     if (t.type != T_STREAM) return;
-    if (t.b != bk.acc_b) {
+    const int kind = t.k < t.Lb ? 0 : 1;
+    if (t.b != bk.acc_b || kind != bk.acc_kind) {
         flush_books(a, bk, epoch);
         bk.acc_b = t.b;
-        bk.acc_total = (t.Lb + 1) * a.nc;
+        bk.acc_kind = kind;
+        bk.acc_Lb = t.Lb;
+        bk.acc_total = (kind == 0 ? t.Lb : 1) * a.nc;
     }
     ++bk.acc_n;
 }
@@ -339,7 +392,7 @@ __device__ void producer(const VerifyArgs &a, VSmem &sm, uint8_t *ring, const St
     nextc.c = blockIdx.x;  // hands out the rest from gridDim.x on
     int cr = 0, cg = 0, cb = 0, ck = 0, cLb = 0, cd = -1, cj = 0, cj_end = 0;
     bool in_chunk = false;
-    Books bk{-1, 0, 0};
+    Books bk{-1, 0, 0, 0, 0};
     int booked = 0;
     // Residual-tile queue, polled one fill ahead: the values read at the end
     // of a fill are used at the start of the next.
@@ -362,15 +415,15 @@ __device__ void producer(const VerifyArgs &a, VSmem &sm, uint8_t *ring, const St
         }
         // 2. then the stream chunks
         if (!have && !in_chunk) {
-            while (nextc.stage < 3) fetch_step(a, sh, nextc);
-            if (nextc.stage == 3) {
+            while (nextc.stage < 4) fetch_step(a, sh, nextc, epoch);
+            if (nextc.stage == 4) {
                 cr = nextc.r;
                 cg = nextc.g;
                 cb = nextc.b;
                 ck = nextc.k;
                 cLb = nextc.Lb;
                 cd = nextc.d;
-                const int C = cr < sh.nA ? a.nc : cr < sh.nB ? sh.Cb : 1;
+                const int C = nextc.q ? sh.CbQ : cr < sh.nA ? a.nc : cr < sh.nB ? sh.Cb : 1;
                 cj = cg * C;
                 cj_end = min(a.nc, cj + C);
                 in_chunk = true;
@@ -393,7 +446,7 @@ __device__ void producer(const VerifyArgs &a, VSmem &sm, uint8_t *ring, const St
             if (++cj == cj_end) in_chunk = false;
             have = true;
         }
-        if (nextc.stage < 3) fetch_step(a, sh, nextc);  // keep the next chunk coming
+        if (nextc.stage < 4) fetch_step(a, sh, nextc, epoch);  // keep the next chunk coming
         // 3. nothing of our own left: book everything, then serve the
         //    residual queue until every request has finished
         if (!have) {
@@ -702,16 +755,25 @@ __device__ __forceinline__ float2 bonus_block(const VerifyArgs &a, int b, int i,
     return make_float2(m, s);
 }
 
-// Request b's stream tiles are all in: accept tests, outputs of the draft
-// rows, and either the whole bonus draw or the residual jobs.  Loads that do
-// not depend on one another are issued together: a decision runs while the
-// streaming keeps L2 busy, and each dependent round trip costs microseconds.
+// The bonus draw of request b, every draft accepted: from p of row L_b
+// (sampling; block and slot masses from the row's per-warp slots), or the
+// argmax of row L_b (greedy; from its chunk records).
 template <typename T>
-__device__ void decide_request(const VerifyArgs &a, const StreamShape &sh, int b, int wpb,
-                               int epoch, int lane) {
-    // Round 1: lengths, offsets, draft tokens and the bonus row's slots.
-    const int Lb = verify_len(a, b), r0 = a.row_off[b], d0 = a.draft_off[b];
+__device__ void bonus_draw(const VerifyArgs &a, const StreamShape &sh, int b, int wpb, int lane) {
+    const int Lb = verify_len(a, b), r = a.row_off[b] + Lb;
     const Drafts dr = load_drafts(a, b, lane);
+    if (a.greedy) {
+        float v = -INFINITY;
+        int id = INT_MAX;
+        const float4 *rec = a.rowrec + size_t(r) * a.grp_stride;
+        for (int g = lane; g < sh.gprbQ; g += 32) {
+            const float4 x = __ldcg(rec + g);
+            am_combine(v, id, x.x, __float_as_int(x.y));
+        }
+        warp_am_reduce(v, id);
+        finish_request(a, b, Lb, id, dr, lane);
+        return;
+    }
     const float scale = a.scale;
     constexpr int kCache = 2;  // blocks per lane kept in registers (nblk <= 64)
     float2 sl[kCache][kCW];
@@ -721,19 +783,93 @@ __device__ void decide_request(const VerifyArgs &a, const StreamShape &sh, int b
         const float2 *p = a.blkrec + (size_t(b) * a.nblk + (i < a.nblk ? i : 0)) * kCW;
 #pragma unroll
         for (int w = 0; w < kCW; ++w)
-            sl[q][w] = !a.greedy && i < a.nblk && w < wpb ? __ldcg(p + w)
-                                                           : make_float2(-INFINITY, 0.f);
+            sl[q][w] = i < a.nblk && w < wpb ? __ldcg(p + w) : make_float2(-INFINITY, 0.f);
     }
+    float u, ub, ut;
+    step_uniforms(a.seed, b, Lb, u, ub, ut);
+    float mb = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < kCache; ++q)
+#pragma unroll
+        for (int w = 0; w < kCW; ++w)
+            if (sl[q][w].y > 0.f) mb = fmaxf(mb, sl[q][w].x);
+    for (int i = kCache * 32 + lane; i < a.nblk; i += 32) {
+        const float2 x = bonus_block(a, b, i, wpb, scale);
+        if (x.y > 0.f) mb = fmaxf(mb, x.x);
+    }
+    const float M = warp_max(mb);
+    // slot mass in the units of 2^((z - M) s)
+    auto smass = [&](float2 x) { return x.y > 0.f ? x.y * exp2_approx((x.x - M) * scale) : 0.f; };
+    auto mass = [&](int i) {
+        const int q = i >> 5;
+        float m = 0.f;
+        if (q < kCache) {
+#pragma unroll
+            for (int c = 0; c < kCache; ++c)
+                if (q == c)
+#pragma unroll
+                    for (int w = 0; w < kCW; ++w) m += smass(sl[c][w]);
+        } else {
+            const float2 *p = a.blkrec + (size_t(b) * a.nblk + i) * kCW;
+            for (int w = 0; w < wpb; ++w) m += smass(__ldcg(p + w));
+        }
+        return m;
+    };
+    const int blk = choose_block(a.nblk, ub, mass, lane);
+    double slot_mass[kCW];
+    {
+        const int q = blk >> 5, owner = blk & 31;
+#pragma unroll
+        for (int w = 0; w < kCW; ++w) {
+            float m = 0.f;
+            if (q < kCache) {
+#pragma unroll
+                for (int c = 0; c < kCache; ++c)
+                    if (q == c) m = smass(sl[c][w]);
+                m = __shfl_sync(0xffffffffu, m, owner);
+            } else if (w < wpb) {
+                m = smass(__ldcg(a.blkrec + (size_t(b) * a.nblk + blk) * kCW + w));
+            }
+            slot_mass[w] = w < wpb ? double(m) : 0.0;
+        }
+    }
+    DecideState st;
+    st.a = Lb;
+    st.mode = D_BONUS;
+    st.Mp = M;
+    st.Sp = 1.f;
+    st.Mq = 0.f;
+    st.Sq = 1.f;
+    st.u_blk = ub;
+    st.u_tok = ut;
+    const int token = block_pick<T>(a, st, b, r, blk, slot_mass, wpb, kSampleBlock / wpb, lane);
+    finish_request(a, b, Lb, token, dr, lane);
+}
+
+// Request b's decision rows (k < L_b) are all in: accept tests and outputs
+// of the draft rows.  A rejection starts the residual draw (sampling) or
+// emits the row's argmax (greedy) and marks the request so its bonus row is
+// not streamed; with every draft accepted the bonus draw runs once the bonus
+// row is in too (join counter: whichever comes second runs it).  Loads that
+// do not depend on one another are issued together: a decision runs while
+// the streaming keeps L2 busy, and each dependent round trip costs
+// microseconds.
+template <typename T>
+__device__ void decide_request(const VerifyArgs &a, const StreamShape &sh, int b, int wpb,
+                               int epoch, int lane) {
+    // Round 1: lengths, offsets and draft tokens.
+    const int Lb = verify_len(a, b), r0 = a.row_off[b], d0 = a.draft_off[b];
+    const Drafts dr = load_drafts(a, b, lane);
+    const float scale = a.scale;
     int ab = Lb;                                   // first rejected draft (L_b: none)
     float Mp = 0.f, Sp = 0.f, Mq = 0.f, Sq = 0.f;  // normalisers of row a_b (sampling)
     float ub = 0.f, ut = 0.f;                      // block / token uniforms of row a_b
     int g_tok = 0;
-    // Round 2, one lane per row k (more rounds when gamma >= 32): the row's
-    // chunk records and its gathered z values.  In sampling mode the bonus
-    // row has no row record; it is drawn from its block slots.
-    for (int base = 0; base <= Lb; base += 32) {
+    // Round 2, one lane per row k (two rounds when gamma > 32): the row's
+    // chunk records and its gathered z values.
+    for (int base = 0; base < Lb; base += 32) {
         const int k = base + lane;
-        const bool live = a.greedy ? k <= Lb : k < Lb;
+        const bool live = k < Lb;
         const int r = r0 + k;
         const int nrec = r < sh.nA ? 1 : r < sh.nB ? sh.gprb : a.nc;
         const float4 *rec = a.rowrec + size_t(live ? r : r0) * a.grp_stride;
@@ -742,9 +878,8 @@ __device__ void decide_request(const VerifyArgs &a, const StreamShape &sh, int b
         for (int u = 0; u < 4; ++u)
             x[u] = live && u < nrec ? __ldcg(rec + u) : make_float4(0.f, 0.f, 0.f, 0.f);
         const float2 z = !a.greedy && live ? __ldcg(a.gath + r) : make_float2(0.f, 0.f);
-        // the uniforms of every row this round could stop at (k == L_b: bonus)
         float u = 1.f, u1 = 0.f, u2 = 0.f;
-        if (!a.greedy && k <= Lb) step_uniforms(a.seed, b, k, u, u1, u2);
+        if (!a.greedy && live) step_uniforms(a.seed, b, k, u, u1, u2);
         float4 rr = a.greedy ? make_float4(-INFINITY, __int_as_float(INT_MAX), 0.f, 0.f)
                              : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
         if (live) {
@@ -769,7 +904,7 @@ __device__ void decide_request(const VerifyArgs &a, const StreamShape &sh, int b
             }
         }
         bool accept = false;
-        if (live && k < Lb) {
+        if (live) {
             const int dt = base == 0 ? dr.t[0] : dr.t[1];
             if (a.greedy) {
                 accept = dt == __float_as_int(rr.y);
@@ -787,8 +922,8 @@ __device__ void decide_request(const VerifyArgs &a, const StreamShape &sh, int b
                 a.q_tok[d0 + k] = q;
             }
         }
-        const unsigned acc = __ballot_sync(0xffffffffu, live && k < Lb && accept);
-        const unsigned rows = __ballot_sync(0xffffffffu, live && k < Lb);
+        const unsigned acc = __ballot_sync(0xffffffffu, live && accept);
+        const unsigned rows = __ballot_sync(0xffffffffu, live);
         const unsigned rej = rows & ~acc;
         if (ab == Lb && rej) ab = base + __ffs(rej) - 1;
         const int src = ab - base;
@@ -806,81 +941,36 @@ __device__ void decide_request(const VerifyArgs &a, const StreamShape &sh, int b
             g_tok = __float_as_int(s1);  // greedy: the row's argmax
         }
     }
-    if (a.greedy) {
-        finish_request(a, b, ab, g_tok, dr, lane);
-        return;
-    }
-    DecideState st;
-    st.a = ab;
-    st.u_blk = ub;
-    st.u_tok = ut;
-    if (ab == Lb) {
-        // Bonus draw from p of row L_b: block and slot masses from its
-        // per-warp slots (lane-owned blocks already in registers).
-        float mb = -INFINITY;
-#pragma unroll
-        for (int q = 0; q < kCache; ++q)
-#pragma unroll
-            for (int w = 0; w < kCW; ++w)
-                if (sl[q][w].y > 0.f) mb = fmaxf(mb, sl[q][w].x);
-        for (int i = kCache * 32 + lane; i < a.nblk; i += 32) {
-            const float2 x = bonus_block(a, b, i, wpb, scale);
-            if (x.y > 0.f) mb = fmaxf(mb, x.x);
+    if (ab < Lb) {
+        if (lane == 0) st_relaxed(&a.rejflag[b], epoch);  // phase Q skips the bonus row
+        if (a.greedy) {
+            finish_request(a, b, ab, g_tok, dr, lane);
+            return;
         }
-        const float M = warp_max(mb);
-        // slot mass in the units of 2^((z - M) s)
-        auto smass = [&](float2 x) { return x.y > 0.f ? x.y * exp2_approx((x.x - M) * scale) : 0.f; };
-        auto mass = [&](int i) {
-            const int q = i >> 5;
-            float m = 0.f;
-            if (q < kCache) {
-#pragma unroll
-                for (int c = 0; c < kCache; ++c)
-                    if (q == c)
-#pragma unroll
-                        for (int w = 0; w < kCW; ++w) m += smass(sl[c][w]);
-            } else {
-                const float2 *p = a.blkrec + (size_t(b) * a.nblk + i) * kCW;
-                for (int w = 0; w < wpb; ++w) m += smass(__ldcg(p + w));
-            }
-            return m;
-        };
-        const int blk = choose_block(a.nblk, ub, mass, lane);
-        double slot_mass[kCW];
-        {
-            const int q = blk >> 5, owner = blk & 31;
-#pragma unroll
-            for (int w = 0; w < kCW; ++w) {
-                float m = 0.f;
-                if (q < kCache) {
-#pragma unroll
-                    for (int c = 0; c < kCache; ++c)
-                        if (q == c) m = smass(sl[c][w]);
-                    m = __shfl_sync(0xffffffffu, m, owner);
-                } else if (w < wpb) {
-                    m = smass(__ldcg(a.blkrec + (size_t(b) * a.nblk + blk) * kCW + w));
-                }
-                slot_mass[w] = w < wpb ? double(m) : 0.0;
-            }
-        }
-        st.mode = D_BONUS;
-        st.Mp = M;
-        st.Sp = 1.f;
-        st.Mq = 0.f;
-        st.Sq = 1.f;
-        const int token =
-            block_pick<T>(a, st, b, r0 + Lb, blk, slot_mass, wpb, kSampleBlock / wpb, lane);
-        finish_request(a, b, ab, token, dr, lane);
-    } else {
+        DecideState st;
+        st.a = ab;
         st.mode = D_RESID;
         st.Mp = Mp;
         st.Sp = Sp;
         st.Mq = Mq;
         st.Sq = Sq;
+        st.u_blk = ub;
+        st.u_tok = ut;
         if (lane == 0) {
             a.dstate[b] = st;
             push_resid_jobs(a, b, epoch);
         }
+        return;
+    }
+    // Every draft accepted: the bonus draw, if the bonus row is in already.
+    int go = 0;
+    if (lane == 0) {
+        __threadfence();
+        go = atomicAdd(&a.join[b], 1) == 1;
+    }
+    if (__shfl_sync(0xffffffffu, go, 0)) {
+        __threadfence();
+        bonus_draw<T>(a, sh, b, wpb, lane);
     }
 }
 
@@ -1129,6 +1219,7 @@ __device__ void decider(const VerifyArgs &a, const StreamShape &sh, int epoch, i
         if (b < 0) return;
         __threadfence();
         if (b & kFinishResidual) finish_residual<T>(a, b & ~kFinishResidual, wpb, lane);
+        else if (b & kBonusDraw) bonus_draw<T>(a, sh, b & ~kBonusDraw, wpb, lane);
         else decide_request<T>(a, sh, b, wpb, epoch, lane);
     }
 }
@@ -1155,10 +1246,21 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(const VerifyA
         consumer<T>(a, sm, ring, sh, warp, lane, epoch);
     }
     __syncthreads();
+    __shared__ int s_last;
     if (tid == 0) {
         __threadfence();
-        if (atomicAdd(&a.q_ctr[Q_EXITED], 1) == int(gridDim.x) - 1) {
-            // Every CTA is done: reset the queues for the next launch.
+        s_last = atomicAdd(&a.q_ctr[Q_EXITED], 1) == int(gridDim.x) - 1;
+    }
+    __syncthreads();
+    if (s_last) {
+        // Every CTA is done.  Bonus-row counts of requests that rejected can
+        // arrive after the request finished, so these reset here.
+        for (int b = tid; b < a.B; b += kVerifyThreads) {
+            a.bon_cnt[b] = 0;
+            a.join[b] = 0;
+        }
+        if (tid == 0) {
+            // Reset the queues for the next launch.
             a.q_ctr[QA_HEAD] = 0;
             a.q_ctr[QA_TAIL] = 0;
             a.q_ctr[QB_HEAD] = 0;
@@ -1167,8 +1269,8 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(const VerifyA
             a.q_ctr[Q_CHUNK] = 0;
             a.q_ctr[Q_EXITED] = 0;
             a.q_ctr[Q_EPOCH] = epoch;
-            __threadfence();
         }
+        __threadfence();
     }
 }
 
