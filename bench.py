@@ -10,7 +10,10 @@ gamma=16, V=129280, d=7168, bf16, c=0.35, cap T=768, sampling at Tm=1.
   (256 MiB write, outside the events) before every timed step.
 * roofline: the verify kernel's algorithmic bytes per launch (ragged target
   rows + kept draft rows, read once) over its event-timed duration, against
-  the measured HBM copy bandwidth.
+  the measured HBM copy bandwidth.  The early-exit count (rows only up to
+  each request's first rejection) is reported beside it: the kernel skips
+  bonus rows of requests it already knows to reject, so its reads fall
+  between the two.
 * e2e: the same metric through the C ABI with host inputs: every step copies
   its inputs from pinned host memory and reads the results back.
 * cpu_baseline: the CPU oracle (single thread) on the same workload.
@@ -176,6 +179,17 @@ def verify_bytes(B: int, sum_L: int, V: int, logit_size: int, sampling: bool, ga
     return rows * V * logit_size + small
 
 
+def early_exit_bytes(accept_len, L, V: int, logit_size: int, sampling: bool) -> int:
+    """The secondary, early-exit count of a verify launch's logit bytes: rows
+    only up to each request's first rejection.  Target rows 0..a_b; when
+    sampling, the draft rows of the drafts tested (min(a_b + 1, L_b))."""
+    import torch
+    a = accept_len.to(torch.int64)
+    tgt = int((a + 1).sum().item())
+    drf = int(torch.minimum(a + 1, L.to(torch.int64)).sum().item()) if sampling else 0
+    return (tgt + drf) * V * logit_size
+
+
 def score_bytes(B: int, gamma: int, d: int, hidden_size: int) -> int:
     """Algorithmic bytes of one score_budget launch: the hidden block once,
     the head weight, and the small outputs."""
@@ -240,7 +254,9 @@ def prepare_set(W, binding, w, step: int, fixed_budget: int = -1):
     binding.dspark_verify(bufs.step)
     torch.cuda.synchronize()
     sum_L = int(bufs.L.sum().item())
-    return {"inp": inp, "bufs": bufs, "tgt": tgt, "sum_L": sum_L,
+    ee = early_exit_bytes(bufs.accept_len, bufs.L, inp["V"], tgt.element_size(),
+                          inp["temperature"] > 0)
+    return {"inp": inp, "bufs": bufs, "tgt": tgt, "sum_L": sum_L, "early_exit_bytes": ee,
             "L_ref": bufs.L.clone(), "commit": commit}
 
 
@@ -275,7 +291,8 @@ def timed_loop(binding, sets, ev, flush, stream):
 
 def run_e2e(binding, W, st, steps, stream):
     """Steps through the C ABI with host inputs: H2D of every input from pinned
-    memory, the three calls, D2H of the results, inside the timed region."""
+    memory, the three calls, D2H of the results, inside the timed region.
+    (Spreading the copies over several streams measured no faster.)"""
     import torch
     inp, bufs = st["inp"], st["bufs"]
     names = ["hidden", "head_w", "head_bias", "sts_tau", "draft_tokens", "draft_logits",
@@ -419,7 +436,9 @@ def run_ours(args, rank, world, local):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": profiled_traffic(),
                      "kernel": "verify_kernel", "peak_kind": peak_kind,
-                     "bytes_per_launch": statistics.mean(vb), "launch_us": ver_mean * 1000.0},
+                     "bytes_per_launch": statistics.mean(vb), "launch_us": ver_mean * 1000.0,
+                     "early_exit_logit_bytes_per_launch": statistics.mean(
+                         sets[i % P]["early_exit_bytes"] for i in range(args.steps))},
         "score_budget_compact_us": statistics.mean(sb_ms) * 1000.0,
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 3 * args.steps, "clocks": clocks,
         "mean_L": mean_L,
