@@ -191,14 +191,20 @@ dspark_status dspark_compact(const dspark_step *step, dspark_stream_t stream);
  * Decoding" (speculative sampling).  For draft k < L_b of request b:
  * p = softmax(z_p[row_off[b]+k] / Tm), q = softmax(z_q[b,k] / Tm),
  * r = min(1, p(d)/q(d)) (1 when q(d) = 0, 0 when d is outside [0, V));
- * accept iff u_{b,k} < r, with (u, u') the top 24 bits / 2^24 of words 0 and
- * 1 of Philox4x64-10 at counter (b, k, 0, 0), key (seed, 0).  a_b is the
- * first rejected k (L_b if none).  A rejection draws the emitted token from
+ * accept iff u_{b,k} < r, with (u, u', u'') the top 24 bits / 2^24 of
+ * words 0, 1 and 2 of Philox4x64-10 at counter (b, k, 0, 0), key (seed, 0).
+ * a_b is the first rejected k (L_b if none).  A rejection draws the emitted token from
  * norm(max(0, p - q)) at row a_b (from p when that mass is 0); otherwise the
- * bonus token is drawn from p at row L_b.  Draws are the inverse CDF over
- * ascending token id: the smallest y whose running weight exceeds u' times
- * the total.  Tm = 0 is greedy: accept iff d == argmax z_p (lowest id on
- * ties); the emitted token is that argmax at row a_b.
+ * bonus token is drawn from p at row L_b.  Draws are a two-level inverse
+ * CDF over ascending token id: the ids are cut into blocks of 4096; u'
+ * (word 1) picks the smallest block whose running mass exceeds u' times the
+ * total, and u'' (word 2) the smallest id of that block whose running weight
+ * exceeds u'' times the block's mass.  That draws id y with probability
+ * weight(y) / total.  Tm = 0 is greedy: accept iff d == argmax z_p (lowest
+ * id on ties); the emitted token is that argmax at row a_b.
+ * p_tok and q_tok are written for every verified draft k < L_b.  Rows are
+ * read only as far as the method needs: the bonus row of a request known to
+ * reject may be skipped.
  * Reads draft_tokens, draft_logits, target_logits, L, draft_off, row_off,
  * row_req, row_k.  Writes accept_len, num_emitted, out_tokens, p_tok, q_tok,
  * and seq_lens_commit[b] += a_b + 1 when not NULL.
