@@ -274,6 +274,20 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
+// Wait for phase `parity` of `bar`, sleeping between polls once the wait
+// has lasted a while: a warp that idles this way (a consumer with no tile
+// coming) leaves its issue slots to the warps that still work.  Gives up
+// after kWaitTimeoutNs.
+__device__ __forceinline__ bool mbar_wait_backoff(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (it >= 8) __nanosleep(it >= 64 ? 256u : 64u);
+        if ((it & 15u) == 0 && global_timer_ns() - t0 > kWaitTimeoutNs) return false;
+    }
+}
+
 // Wait for phase `parity` of `bar`, giving up after kWaitTimeoutNs.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;

@@ -44,7 +44,7 @@
 //    the last of them queues the residual draw.
 //  * Draws are two-level: a 4096-id block by mass (u'), then an id inside it
 //    (u''); in-block running sums are fp32 over short lane runs combined in
-//    fp64.
+//    two-float (TwoSum) arithmetic, as exact as fp64 on the fast fp32 pipe.
 //  * Every wait is bounded (2 s) and sets a status bit when it gives up;
 //    counters reset themselves at the end of the launch.
 #include <climits>
@@ -200,19 +200,61 @@ __device__ __forceinline__ void online_update(float &m, float &s, const float (&
     s += t[0];
 }
 
-// Inclusive warp scan in double (lane order).
-__device__ __forceinline__ double warp_scan_incl(double v, int lane) {
+// Two-float numbers: the unevaluated sum hi + lo, |lo| <= ulp(hi) / 2.
+// The draws' running sums use them instead of fp64, whose rate on this chip
+// is a small fraction of fp32's: Knuth's TwoSum keeps each addition's
+// rounding error, so sums of fp32 masses come out as exact as in fp64 while
+// staying on the fp32 pipe (no contraction applies: there is no product).
+struct F2 {
+    float hi, lo;
+};
+
+__device__ __forceinline__ F2 f2(float x) { return F2{x, 0.f}; }
+
+__device__ __forceinline__ F2 operator+(F2 a, F2 b) {
+    const float s = a.hi + b.hi;
+    const float bb = s - a.hi;
+    const float e = (a.hi - (s - bb)) + (b.hi - bb) + (a.lo + b.lo);
+    const float h = s + e;
+    return F2{h, e - (h - s)};
+}
+
+__device__ __forceinline__ F2 operator-(F2 a, F2 b) { return a + F2{-b.hi, -b.lo}; }
+
+// a * u for 0 <= u <= 1 (the product's error kept by an FMA)
+__device__ __forceinline__ F2 f2_scale(F2 a, float u) {
+    const float p = a.hi * u;
+    const float e = fmaf(a.hi, u, -p) + a.lo * u;
+    const float h = p + e;
+    return F2{h, e - (h - p)};
+}
+
+__device__ __forceinline__ bool f2_gt(F2 a, F2 b) {
+    return (a.hi - b.hi) + (a.lo - b.lo) > 0.f;
+}
+
+__device__ __forceinline__ F2 f2_shfl_up(F2 v, int o) {
+    return F2{__shfl_up_sync(0xffffffffu, v.hi, o), __shfl_up_sync(0xffffffffu, v.lo, o)};
+}
+
+__device__ __forceinline__ F2 f2_shfl(F2 v, int src) {
+    return F2{__shfl_sync(0xffffffffu, v.hi, src), __shfl_sync(0xffffffffu, v.lo, src)};
+}
+
+// Inclusive warp scan (lane order).
+__device__ __forceinline__ F2 warp_scan_incl(F2 v, int lane) {
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const double n = __shfl_up_sync(0xffffffffu, v, o);
-        if (lane >= o) v += n;
+        const F2 n = f2_shfl_up(v, o);
+        if (lane >= o) v = v + n;
     }
     return v;
 }
 
-__device__ __forceinline__ double warp_sum_d(double v) {
+__device__ __forceinline__ F2 warp_sum_f2(F2 v) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    for (int o = 16; o > 0; o >>= 1)
+        v = v + F2{__shfl_xor_sync(0xffffffffu, v.hi, o), __shfl_xor_sync(0xffffffffu, v.lo, o)};
     return v;
 }
 
@@ -555,23 +597,23 @@ __device__ void finish_request(const VerifyArgs &a, int b, int acc, int token, c
 // crossing.  mass(i) is evaluated by the lane that owns i.
 template <typename F>
 __device__ int choose_block(int nblk, float u, F mass, int lane) {
-    double total = 0.0;
+    F2 total = f2(0.f);
     for (int t0 = 0; t0 < nblk; t0 += 32) {
         const int i = t0 + lane;
-        total += warp_sum_d(i < nblk ? double(mass(i)) : 0.0);
+        total = total + warp_sum_f2(i < nblk ? mass(i) : f2(0.f));
     }
-    const double target = double(u) * total;
-    double run = 0.0;
+    const F2 target = f2_scale(total, u);
+    F2 run = f2(0.f);
     int last_pos = 0;
     for (int t0 = 0; t0 < nblk; t0 += 32) {
         const int i = t0 + lane;
-        const double v = i < nblk ? double(mass(i)) : 0.0;
-        const double incl = run + warp_scan_incl(v, lane);
-        const unsigned hit = __ballot_sync(0xffffffffu, i < nblk && incl > target);
+        const F2 v = i < nblk ? mass(i) : f2(0.f);
+        const F2 incl = run + warp_scan_incl(v, lane);
+        const unsigned hit = __ballot_sync(0xffffffffu, i < nblk && f2_gt(incl, target));
         if (hit) return t0 + __ffs(hit) - 1;
-        const unsigned pos = __ballot_sync(0xffffffffu, i < nblk && v > 0.0);
+        const unsigned pos = __ballot_sync(0xffffffffu, i < nblk && v.hi > 0.f);
         if (pos) last_pos = t0 + 31 - __clz(pos);
-        run = __shfl_sync(0xffffffffu, incl, 31);
+        run = f2_shfl(incl, 31);
     }
     return last_pos;
 }
@@ -615,13 +657,13 @@ __device__ __forceinline__ float pair_sum(const float (&w)[VE]) {
 // counted from the slot's start, exceeds `target`.  Each lane owns a
 // contiguous run of n/32 ids (kRunVec 16-byte vectors, one batch of loads);
 // per-vector weights are summed pairwise and kept in registers; runs are
-// combined in fp64; the lane holding the crossing finds its vector from the
+// combined in two-float sums; the lane holding the crossing finds its vector from the
 // kept sums and reloads only that vector.  If rounding leaves no crossing,
 // the last id with positive weight.  The rows were streamed moments
 // earlier, so the loads hit L2.
 template <typename T>
 __device__ int slot_pick(const VerifyArgs &a, const DecideState &st, int b, int r, int y0, int n,
-                         double target, int lane) {
+                         F2 target, int lane) {
     constexpr int VE = Vec<T>::kElems;
     constexpr int kRunVec = 4;  // n = 32 lanes x 4 vectors (1024 bf16 / 512 fp32 ids)
     const uint4 *tv = reinterpret_cast<const uint4 *>(static_cast<const char *>(a.target_logits) +
@@ -664,10 +706,10 @@ __device__ int slot_pick(const VerifyArgs &a, const DecideState &st, int b, int 
         vs[q] = v0 + q < v_end ? pair_sum<VE>(w) : 0.f;
         ls += vs[q];
     }
-    const double incl = warp_scan_incl(double(ls), lane);
-    const double prev = __shfl_up_sync(0xffffffffu, incl, 1);
-    const double excl = lane > 0 ? prev : 0.0;
-    const unsigned hit = __ballot_sync(0xffffffffu, ls > 0.f && incl > target);
+    const F2 incl = warp_scan_incl(f2(ls), lane);
+    const F2 prev = f2_shfl_up(incl, 1);
+    const F2 excl = lane > 0 ? prev : f2(0.f);
+    const unsigned hit = __ballot_sync(0xffffffffu, ls > 0.f && f2_gt(incl, target));
     const unsigned pos = __ballot_sync(0xffffffffu, ls > 0.f);
     const int lsel = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : -1);
     if (lsel < 0) return y0;  // a slot without weight (not drawn in practice)
@@ -680,7 +722,7 @@ __device__ int slot_pick(const VerifyArgs &a, const DecideState &st, int b, int 
             if (qsel < 0 && vs[q] > 0.f) {
                 qlast = q;
                 run_at = run;
-                if (excl + double(run + vs[q]) > target) qsel = q;
+                if (f2_gt(excl + f2(run + vs[q]), target)) qsel = q;
             }
             run += vs[q];
         }
@@ -697,7 +739,7 @@ __device__ int slot_pick(const VerifyArgs &a, const DecideState &st, int b, int 
                 re += w[e];
                 if (pick < 0 && w[e] > 0.f) {
                     lastpos = (v0 + q) * VE + e;
-                    if (excl + double(re) > target) pick = (v0 + q) * VE + e;
+                    if (f2_gt(excl + f2(re), target)) pick = (v0 + q) * VE + e;
                 }
             }
         }
@@ -711,32 +753,32 @@ __device__ int slot_pick(const VerifyArgs &a, const DecideState &st, int b, int 
 // running mass crosses u_tok times the block mass, then the id inside it.
 template <typename T>
 __device__ int block_pick(const VerifyArgs &a, const DecideState &st, int b, int r, int blk,
-                          const double (&slot_mass)[kCW], int wpb, int tpw, int lane) {
-    double total = 0.0;
+                          const float (&slot_mass)[kCW], int wpb, int tpw, int lane) {
+    F2 total = f2(0.f);
 #pragma unroll
     for (int w = 0; w < kCW; ++w)
-        if (w < wpb) total += slot_mass[w];
-    const double target = double(st.u_tok) * total;
-    double cum = 0.0, before = 0.0;
+        if (w < wpb) total = total + f2(slot_mass[w]);
+    const F2 target = f2_scale(total, st.u_tok);
+    F2 cum = f2(0.f), before = f2(0.f);
     int wsel = -1, wlast = 0;
 #pragma unroll
     for (int w = 0; w < kCW; ++w) {
         if (w >= wpb || wsel >= 0) continue;
-        if (slot_mass[w] > 0.0) {
+        if (slot_mass[w] > 0.f) {
             wlast = w;
-            if (cum + slot_mass[w] > target) {
+            if (f2_gt(cum + f2(slot_mass[w]), target)) {
                 wsel = w;
                 before = cum;
             }
         }
-        cum += slot_mass[w];
+        cum = cum + f2(slot_mass[w]);
     }
     if (wsel < 0) {
         wsel = wlast;
-        before = 0.0;
+        before = f2(0.f);
 #pragma unroll
         for (int w = 0; w < kCW; ++w)
-            if (w < wsel) before += slot_mass[w];
+            if (w < wsel) before = before + f2(slot_mass[w]);
     }
     return slot_pick<T>(a, st, b, r, blk * kSampleBlock + wsel * tpw, tpw, target - before, lane);
 }
@@ -802,21 +844,21 @@ __device__ void bonus_draw(const VerifyArgs &a, const StreamShape &sh, int b, in
     auto smass = [&](float2 x) { return x.y > 0.f ? x.y * exp2_approx((x.x - M) * scale) : 0.f; };
     auto mass = [&](int i) {
         const int q = i >> 5;
-        float m = 0.f;
+        F2 m = f2(0.f);
         if (q < kCache) {
 #pragma unroll
             for (int c = 0; c < kCache; ++c)
                 if (q == c)
 #pragma unroll
-                    for (int w = 0; w < kCW; ++w) m += smass(sl[c][w]);
+                    for (int w = 0; w < kCW; ++w) m = m + f2(smass(sl[c][w]));
         } else {
             const float2 *p = a.blkrec + (size_t(b) * a.nblk + i) * kCW;
-            for (int w = 0; w < wpb; ++w) m += smass(__ldcg(p + w));
+            for (int w = 0; w < wpb; ++w) m = m + f2(smass(__ldcg(p + w)));
         }
         return m;
     };
     const int blk = choose_block(a.nblk, ub, mass, lane);
-    double slot_mass[kCW];
+    float slot_mass[kCW];
     {
         const int q = blk >> 5, owner = blk & 31;
 #pragma unroll
@@ -830,7 +872,7 @@ __device__ void bonus_draw(const VerifyArgs &a, const StreamShape &sh, int b, in
             } else if (w < wpb) {
                 m = smass(__ldcg(a.blkrec + (size_t(b) * a.nblk + blk) * kCW + w));
             }
-            slot_mass[w] = w < wpb ? double(m) : 0.0;
+            slot_mass[w] = w < wpb ? m : 0.f;
         }
     }
     DecideState st;
@@ -994,34 +1036,34 @@ __device__ void finish_residual(const VerifyArgs &a, int b, int wpb, int lane) {
     }
     auto mass = [&](int i, bool residual) {
         const int q = i >> 5;
-        double m = 0.0;
+        F2 m = f2(0.f);
         if (q < kCache) {
 #pragma unroll
             for (int c = 0; c < kCache; ++c)
                 if (q == c)
 #pragma unroll
-                    for (int w = 0; w < kCW; ++w) m += double(residual ? sl[c][w].x : sl[c][w].y);
+                    for (int w = 0; w < kCW; ++w) m = m + f2(residual ? sl[c][w].x : sl[c][w].y);
         } else {
             for (int w = 0; w < wpb; ++w) {
                 const float2 x = __ldcg(z + size_t(i) * kCW + w);
-                m += double(residual ? x.x : x.y);
+                m = m + f2(residual ? x.x : x.y);
             }
         }
         return m;
     };
-    double total = 0.0;
+    F2 total = f2(0.f);
     for (int t0 = 0; t0 < a.nblk; t0 += 32) {
         const int i = t0 + lane;
-        total += warp_sum_d(i < a.nblk ? mass(i, true) : 0.0);
+        total = total + warp_sum_f2(i < a.nblk ? mass(i, true) : f2(0.f));
     }
-    const bool residual = total > 0.0;
+    const bool residual = total.hi > 0.f;
     if (!residual) {
         // No residual mass: draw from p of the same row instead.
         st.mode = D_FALLBACK;
         st.Sp = 1.f;
     }
     const int blk = choose_block(a.nblk, st.u_blk, [&](int i) { return mass(i, residual); }, lane);
-    double slot_mass[kCW];
+    float slot_mass[kCW];
     {
         const int q = blk >> 5, owner = blk & 31;
 #pragma unroll
@@ -1036,7 +1078,7 @@ __device__ void finish_residual(const VerifyArgs &a, int b, int wpb, int lane) {
                 const float2 x = __ldcg(z + size_t(blk) * kCW + w);
                 m = residual ? x.x : x.y;
             }
-            slot_mass[w] = w < wpb ? double(m) : 0.0;
+            slot_mass[w] = w < wpb ? m : 0.f;
         }
     }
     const int token =
@@ -1062,7 +1104,7 @@ __device__ void consumer(const VerifyArgs &a, VSmem &sm, const uint8_t *ring,
     int bi = INT_MAX;
     for (int fill = 0;; ++fill) {
         const int s = fill % kStages, n = fill / kStages;
-        if (!mbar_wait_bounded(&sm.full[s], n & 1)) {
+        if (!mbar_wait_backoff(&sm.full[s], n & 1)) {
             if (lane == 0) atomicOr(a.status, kStatusWaitTimeout);
             return;
         }
@@ -1169,7 +1211,7 @@ __device__ void consumer(const VerifyArgs &a, VSmem &sm, const uint8_t *ring,
                     zr += fmaxf(0.f, pw * iSp - exp2_approx((y[e] - st.Mq) * scale) * iSq);
                 }
             }
-            const double dr = warp_sum_d(zr), dp = warp_sum_d(zp);
+            const F2 dr = warp_sum_f2(f2(zr)), dp = warp_sum_f2(f2(zp));
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.empty[s]);  // the stage is no longer read
             const int y = t.y0 + warp * tpw;
@@ -1178,7 +1220,7 @@ __device__ void consumer(const VerifyArgs &a, VSmem &sm, const uint8_t *ring,
             if (lane == 0) {
                 if (blk < a.nblk)
                     a.zrec[(size_t(t.b) * a.nblk + blk) * kCW + (y % kSampleBlock) / tpw] =
-                        make_float2(float(dr), float(dp));
+                        make_float2(dr.hi + dr.lo, dp.hi + dp.lo);
                 __threadfence();
                 last = atomicAdd(&a.r1_cnt[t.b], 1) == a.nc * kCW - 1;
             }
