@@ -121,9 +121,6 @@ __device__ __forceinline__ int ld_relaxed(const int *p) {
     asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
-__device__ __forceinline__ void st_release(int *p, int v) {
-    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
 __device__ __forceinline__ void st_relaxed(int *p, int v) {
     asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
@@ -1096,7 +1093,6 @@ __device__ void consumer(const VerifyArgs &a, VSmem &sm, const uint8_t *ring,
     const float scale = a.scale;
     const int tpw = a.chunk_elems / kCW;  // tokens per warp in a tile
     const int vpw = tpw / VE;             // vectors per warp in a tile
-    const int wpb = kSampleBlock / tpw;   // warps per sampling block
     // Row accumulators of pair rows (sampling) / of every row (greedy),
     // carried across the tiles of a chunk.
     float mp = -INFINITY, sp = 0.f, mq = -INFINITY, sq = 0.f;
