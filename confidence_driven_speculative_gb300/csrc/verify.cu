@@ -376,23 +376,34 @@ __device__ __forceinline__ void fetch_step(const VerifyArgs &a, const StreamShap
 constexpr int kFinishResidual = 1 << 30;  // decider job: finish the residual draw
 constexpr int kBonusDraw = 1 << 29;       // decider job: the bonus draw
 
+// The count an atomic returned is checked one flush (or one fill) later, so
+// the atomic's round trip overlaps the issue of copies instead of stalling it.
 struct Books {
     int acc_b, acc_kind, acc_n, acc_total, acc_Lb;
+    int chk_b, chk_kind, chk_end, chk_Lb, chk_old;  // a published count awaiting its check
 };
+
+// Act on the count published last: a completed request's job.
+__device__ void check_books(const VerifyArgs &a, Books &bk, int epoch) {
+    if (bk.chk_b < 0) return;
+    const int b = bk.chk_b;
+    if (bk.chk_old == bk.chk_end) {
+        if (bk.chk_kind == 0) push_decide(a, b, epoch);
+        else if (bk.chk_Lb == 0 || atomicAdd(&a.join[b], 1) == 1) push_decide(a, b | kBonusDraw, epoch);
+    }
+    bk.chk_b = -1;
+}
 
 __device__ void flush_books(const VerifyArgs &a, Books &bk, int epoch) {
     if (bk.acc_n == 0) return;
+    check_books(a, bk, epoch);
     __threadfence();
     const int b = bk.acc_b;
-    if (bk.acc_kind == 0) {
-        const int old = atomicAdd(&a.req_cnt[b], bk.acc_n);
-        if (old + bk.acc_n == bk.acc_total) push_decide(a, b, epoch);
-    } else {
-        const int old = atomicAdd(&a.bon_cnt[b], bk.acc_n);
-        if (old + bk.acc_n == bk.acc_total &&
-            (bk.acc_Lb == 0 || atomicAdd(&a.join[b], 1) == 1))
-            push_decide(a, b | kBonusDraw, epoch);
-    }
+    bk.chk_old = atomicAdd(bk.acc_kind == 0 ? &a.req_cnt[b] : &a.bon_cnt[b], bk.acc_n);
+    bk.chk_b = b;
+    bk.chk_kind = bk.acc_kind;
+    bk.chk_end = bk.acc_total - bk.acc_n;  // the count before ours when ours completes it
+    bk.chk_Lb = bk.acc_Lb;
     bk.acc_n = 0;
 }
 
@@ -431,24 +442,27 @@ __device__ void producer(const VerifyArgs &a, VSmem &sm, uint8_t *ring, const St
     nextc.c = blockIdx.x;  // hands out the rest from gridDim.x on
     int cr = 0, cg = 0, cb = 0, ck = 0, cLb = 0, cd = -1, cj = 0, cj_end = 0;
     bool in_chunk = false;
-    Books bk{-1, 0, 0, 0, 0};
+    Books bk{-1, 0, 0, 0, 0, -1, 0, 0, 0, 0};
     int booked = 0;
-    // Residual-tile queue, polled one fill ahead: the values read at the end
-    // of a fill are used at the start of the next.
+    // Residual-tile queue, polled on every fourth fill: the values read at
+    // the end of a polling fill are used at the start of the next one, so a
+    // global load does not stall the issue of a copy while the stream runs
+    // (with free stages a fill is shorter than an L2 round trip).
     int pending = -1;      // a claimed queue index
-    int pend_rdy = 0;      // its ready word, read during the previous fill
+    int pend_rdy = 0;      // its ready word, read four fills earlier
     int2 pend_job = make_int2(0, 0);
     int obs_head = 0, obs_tail = 0;
     for (int fill = 0;; ++fill) {
         TaskInfo t;
         t.type = T_EXIT;
         bool have = false, ok = true;
+        const bool poll = (fill & 3) == 0;
         // 1. residual tiles first
-        if (pending >= 0 && pend_rdy == epoch) {
+        if (poll && pending >= 0 && pend_rdy == epoch) {
             t = resid_task(a, pend_job);
             pending = -1;
             have = true;
-        } else if (pending < 0 && obs_head < obs_tail) {
+        } else if (poll && pending < 0 && obs_head < obs_tail) {
             pending = atomicAdd(&a.q_ctr[QA_HEAD], 1);
             pend_rdy = 0;
         }
@@ -485,12 +499,16 @@ __device__ void producer(const VerifyArgs &a, VSmem &sm, uint8_t *ring, const St
             if (++cj == cj_end) in_chunk = false;
             have = true;
         }
-        if (nextc.stage < 4) fetch_step(a, sh, nextc, epoch);  // keep the next chunk coming
+        // keep the next chunk coming; with many tiles of this chunk left, one
+        // fetch stage every fourth fill, so its loads are back before use
+        if (nextc.stage < 4 && (!in_chunk || cj_end - cj < 10 || (fill & 3) == 0))
+            fetch_step(a, sh, nextc, epoch);
         // 3. nothing of our own left: book everything, then serve the
         //    residual queue until every request has finished
         if (!have) {
             ok = reclaim(a, sm, bk, booked, fill, epoch);
             flush_books(a, bk, epoch);
+            check_books(a, bk, epoch);
             if (pending < 0) pending = atomicAdd(&a.q_ctr[QA_HEAD], 1);
             const uint64_t t0 = global_timer_ns();
             unsigned ns = 32;
@@ -531,17 +549,21 @@ __device__ void producer(const VerifyArgs &a, VSmem &sm, uint8_t *ring, const St
                                size_t(t.y0) * a.elem_bytes;
             bulk_g2s(dst + kChunkBytes, dsrc, uint32_t(t.bytes), bar);
         }
-        // 5. book whatever has already come back, without waiting
+        // 5. act on the count published last, then book whatever has already
+        //    come back, without waiting
+        check_books(a, bk, epoch);
         while (booked < fill && mbar_test_wait(&sm.empty[booked % kStages], (booked / kStages) & 1)) {
             account(a, bk, sm.task[booked % kStages], epoch);
             ++booked;
         }
-        // 6. look at the residual queue for the next fill
-        obs_head = ld_relaxed(&a.q_ctr[QA_HEAD]);
-        obs_tail = ld_relaxed(&a.q_ctr[QA_TAIL]);
-        if (pending >= 0 && pending < a.qcap) {
-            pend_rdy = ld_acquire(&a.q_ready[pending]);
-            pend_job = __ldcg(a.q_job + pending);
+        // 6. look at the residual queue for the next polling fill
+        if (poll) {
+            obs_head = ld_relaxed(&a.q_ctr[QA_HEAD]);
+            obs_tail = ld_relaxed(&a.q_ctr[QA_TAIL]);
+            if (pending >= 0 && pending < a.qcap) {
+                pend_rdy = ld_acquire(&a.q_ready[pending]);
+                pend_job = __ldcg(a.q_job + pending);
+            }
         }
     }
 }
