@@ -100,6 +100,28 @@ def test_draft_equals_target_accepts_everything(cuda_lib):
     assert np.array_equal(gpu["accept_len"], gpu["L"])
 
 
+@pytest.mark.parametrize("Tm", [0.0, 1.0])
+def test_first_drafts_rejected(cuda_lib, Tm):
+    """Drafts from an unrelated distribution: nearly every request rejects
+    at its first draft, so most decisions take the residual path (sampling)
+    or the argmax correction (greedy), and the bonus rows of those requests
+    are not needed -- the verify may skip them."""
+    inp = W.make_inputs(W.MIXED_B256, 7, B=64, V=20000, d=64, cap_T=-1, cost_c=0.0,
+                        temperature=Tm)
+    g = torch.Generator().manual_seed(77)
+    dl = torch.randn(inp["draft_logits"].shape, generator=g) * 4.0
+    inp["draft_logits"] = dl.to(inp["draft_logits"].dtype)
+    if Tm == 0.0:
+        # greedy drafts that are never the target's argmax
+        inp["draft_tokens"] = (inp["target_dense"][:, :-1].float().argmax(-1) + 1).to(torch.int32) % 20000
+    else:
+        gum = -torch.log(-torch.log(torch.rand(dl.shape, generator=g).clamp_min(1e-20)))
+        inp["draft_tokens"] = (dl.float() + gum).argmax(-1).to(torch.int32)
+    gpu, _, _ = run_and_compare(inp)
+    assert np.all(gpu["L"] == 16)
+    assert np.mean(gpu["accept_len"] == 0) > 0.8
+
+
 def test_out_of_range_drafts_are_rejected(cuda_lib):
     for Tm in (0.0, 1.0):
         inp = W.make_inputs(W.MIXED_B256, 4, B=8, V=4096, d=64, cap_T=-1, cost_c=0.0,
