@@ -16,6 +16,10 @@ namespace dspark {
 namespace {
 
 __global__ void __launch_bounds__(kThreads) compact_kernel(const CompactArgs a) {
+    // Launched as a programmatic dependent of the kernel before it on the
+    // stream: wait here until that grid has completed and its writes (L,
+    // row_off) are visible.  Without such a grid this returns at once.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int g1 = a.gamma + 1;
     const int cap = a.B * g1;
     const int t = blockIdx.x * kThreads + threadIdx.x;
@@ -43,9 +47,20 @@ __global__ void __launch_bounds__(kThreads) compact_kernel(const CompactArgs a) 
 }  // namespace
 
 cudaError_t launch_compact(const CompactArgs &a, cudaStream_t s) {
+    // Programmatic dependent launch: the grid is scheduled while the kernel
+    // before it (the score kernel) still runs, so its launch latency is
+    // hidden; griddepcontrol.wait above keeps the data dependency.
     const int cap = a.B * (a.gamma + 1);
-    compact_kernel<<<(cap + kThreads - 1) / kThreads, kThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((cap + kThreads - 1) / kThreads);
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, compact_kernel, a);
 }
 
 }  // namespace dspark

@@ -528,6 +528,10 @@ __global__ void __launch_bounds__(kScoreThreads, 3) score_budget_kernel(const Sc
     extern __shared__ __align__(1024) uint8_t ring[];
     __shared__ ScoreSmem sm;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // Let the next kernel on the stream (the compaction, a programmatic
+    // dependent launch) be scheduled now; it waits for this grid to complete
+    // before it reads anything.
+    asm volatile("griddepcontrol.launch_dependents;");
     if (tid < kScoreStages) {
         mbar_init(&sm.full[tid], 1);
         mbar_init(&sm.empty[tid], kWarps);
