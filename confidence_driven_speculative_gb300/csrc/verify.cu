@@ -76,6 +76,7 @@ struct TaskInfo {
     int y0;     // first token id of the stage
     int bytes;  // bytes per row in the stage
     int pair;   // a draft row sits in the second half of the stage
+    int bytes2; // target-only rows: the row's next tile in the second half (0: none)
     int d;      // stream pair: drafted id (its gather target)
     int flush;  // stream: last tile of the chunk
 };
@@ -301,6 +302,7 @@ __device__ TaskInfo resid_task(const VerifyArgs &a, int2 jb) {
     t.pair = 1;
     t.y0 = t.j * a.chunk_elems;
     t.bytes = min(kChunkBytes, a.row_bytes - t.j * kChunkBytes);
+    t.bytes2 = 0;
     return t;
 }
 
@@ -418,7 +420,7 @@ __device__ __forceinline__ void account(const VerifyArgs &a, Books &bk, const Ta
         bk.acc_Lb = t.Lb;
         bk.acc_total = (kind == 0 ? t.Lb : 1) * a.nc;
     }
-    ++bk.acc_n;
+    bk.acc_n += t.bytes2 > 0 ? 2 : 1;
 }
 
 // Wait for every fill below `upto` to come back from the consumers and book it.
@@ -495,8 +497,14 @@ __device__ void producer(const VerifyArgs &a, VSmem &sm, uint8_t *ring, const St
             t.pair = !a.greedy && ck < cLb;
             t.y0 = cj * a.chunk_elems;
             t.bytes = min(kChunkBytes, a.row_bytes - cj * kChunkBytes);
-            t.flush = cj + 1 == cj_end;
-            if (++cj == cj_end) in_chunk = false;
+            // a target-only row (greedy, or a bonus row) carries its next tile
+            // in the stage's draft half: full stages whatever the row kind
+            t.bytes2 = !t.pair && cj + 1 < cj_end
+                           ? min(kChunkBytes, a.row_bytes - (cj + 1) * kChunkBytes) : 0;
+            const int ntile = t.bytes2 > 0 ? 2 : 1;
+            t.flush = cj + ntile == cj_end;
+            cj += ntile;
+            if (cj == cj_end) in_chunk = false;
             have = true;
         }
         // keep the next chunk coming; with many tiles of this chunk left, one
@@ -541,13 +549,15 @@ __device__ void producer(const VerifyArgs &a, VSmem &sm, uint8_t *ring, const St
         uint64_t *bar = &sm.full[s];
         const char *tsrc = static_cast<const char *>(a.target_logits) +
                            size_t(t.r) * a.row_bytes + size_t(t.y0) * a.elem_bytes;
-        mbar_arrive_expect_tx(bar, uint32_t(t.bytes) * (t.pair ? 2u : 1u));
+        mbar_arrive_expect_tx(bar, uint32_t(t.bytes) * (t.pair ? 2u : 1u) + uint32_t(t.bytes2));
         bulk_g2s(dst, tsrc, uint32_t(t.bytes), bar);
         if (t.pair) {
             const char *dsrc = static_cast<const char *>(a.draft_logits) +
                                (size_t(t.b) * a.gamma + t.k) * size_t(a.row_bytes) +
                                size_t(t.y0) * a.elem_bytes;
             bulk_g2s(dst + kChunkBytes, dsrc, uint32_t(t.bytes), bar);
+        } else if (t.bytes2 > 0) {
+            bulk_g2s(dst + kChunkBytes, tsrc + kChunkBytes, uint32_t(t.bytes2), bar);
         }
         // 5. act on the count published last, then book whatever has already
         //    come back, without waiting
@@ -1135,15 +1145,21 @@ __device__ void consumer(const VerifyArgs &a, VSmem &sm, const uint8_t *ring,
 
         if (t.type == T_STREAM) {
             if (a.greedy) {
-                for (int v = v0 + lane; v < v1; v += 32) {
-                    float z[VE];
-                    Vec<T>::unpack(tv[v], z);
+                for (int h = 0; h < (t.bytes2 > 0 ? 2 : 1); ++h) {
+                    const uint4 *xv = h ? dv : tv;
+                    const int nv = (h ? t.bytes2 : t.bytes) / 16;
+                    const int va = min(nv, warp * vpw), vb = min(nv, va + vpw);
+                    const int yb = t.y0 + h * a.chunk_elems;
+                    for (int v = va + lane; v < vb; v += 32) {
+                        float z[VE];
+                        Vec<T>::unpack(xv[v], z);
 #pragma unroll
-                    for (int e = 0; e < VE; ++e)
-                        if (z[e] > bv) {
-                            bv = z[e];
-                            bi = t.y0 + v * VE + e;
-                        }
+                        for (int e = 0; e < VE; ++e)
+                            if (z[e] > bv) {
+                                bv = z[e];
+                                bi = yb + v * VE + e;
+                            }
+                    }
                 }
             } else if (t.pair) {
                 for (int v = v0 + lane; v < v1; v += 32) {
@@ -1161,18 +1177,23 @@ __device__ void consumer(const VerifyArgs &a, VSmem &sm, const uint8_t *ring,
                 }
             } else {
                 // Bonus row: one (max, sum) slot per tile and warp.
-                float bm = -INFINITY, bs = 0.f;
-                for (int v = v0 + lane; v < v1; v += 32) {
-                    float z[VE];
-                    Vec<T>::unpack(tv[v], z);
-                    online_update<VE>(bm, bs, z, scale);
+                for (int h = 0; h < (t.bytes2 > 0 ? 2 : 1); ++h) {
+                    const uint4 *xv = h ? dv : tv;
+                    const int nv = (h ? t.bytes2 : t.bytes) / 16;
+                    const int va = min(nv, warp * vpw), vb = min(nv, va + vpw);
+                    float bm = -INFINITY, bs = 0.f;
+                    for (int v = va + lane; v < vb; v += 32) {
+                        float z[VE];
+                        Vec<T>::unpack(xv[v], z);
+                        online_update<VE>(bm, bs, z, scale);
+                    }
+                    warp_ms_reduce(bm, bs, scale);
+                    const int y = t.y0 + h * a.chunk_elems + warp * tpw;
+                    const int blk = y / kSampleBlock;
+                    if (lane == 0 && blk < a.nblk)
+                        a.blkrec[(size_t(t.b) * a.nblk + blk) * kCW + (y % kSampleBlock) / tpw] =
+                            make_float2(bm, bs);
                 }
-                warp_ms_reduce(bm, bs, scale);
-                const int y = t.y0 + warp * tpw;
-                const int blk = y / kSampleBlock;
-                if (lane == 0 && blk < a.nblk)
-                    a.blkrec[(size_t(t.b) * a.nblk + blk) * kCW + (y % kSampleBlock) / tpw] =
-                        make_float2(bm, bs);
             }
             if (t.flush && (a.greedy || t.pair)) {
                 // End of the chunk: the eight warp partials become one record.
