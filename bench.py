@@ -17,6 +17,8 @@ gamma=16, V=129280, d=7168, bf16, c=0.35, cap T=768, sampling at Tm=1.
 * e2e: the same metric through the C ABI with host inputs: every step copies
   its inputs from pinned host memory and reads the results back.
 * cpu_baseline: the CPU oracle (single thread) on the same workload.
+* latency_b1: the B=1 DeepSeek-class greedy step, microseconds per step with
+  plain launches and replayed as one CUDA graph.
 * --impl reference: the CPU oracle as the reference arm (bounded samples).
 
 Multi-GPU runs are independent replicas (the step has no cross-request
@@ -58,6 +60,7 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-latency", action="store_true")
     ap.add_argument("--no-fixed-arm", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -324,6 +327,52 @@ def run_e2e(binding, W, st, steps, stream):
     return statistics.mean(times), h2d, d2h
 
 
+def run_latency(binding, W, flush, steps: int = 200):
+    """The B=1 latency step (DeepSeek-class shapes, greedy): microseconds per
+    step with plain launches and as one replayed CUDA graph, L2 flushed
+    before every step (outside the events)."""
+    import torch
+    st = prepare_set(W, binding, W.LATENCY_B1, 0)
+    step = st["bufs"].step
+
+    def one():
+        binding.dspark_score_budget(step)
+        binding.dspark_compact(step)
+        binding.dspark_verify(step)
+
+    def timed(fn):
+        for _ in range(10):
+            fn()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        torch.cuda.synchronize()
+        for e0, e1 in ev:
+            flush.zero_()
+            e0.record()
+            fn()
+            e1.record()
+        torch.cuda.synchronize()
+        return statistics.median(e0.elapsed_time(e1) for e0, e1 in ev) * 1000.0
+
+    out = {"workload": W.LATENCY_B1.name, "steps": steps, "us_per_step_plain": timed(one)}
+    try:
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            one()  # warm-up on the capture stream
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g, stream=side):
+                one()
+        torch.cuda.current_stream().wait_stream(side)
+        out["us_per_step_graph"] = timed(g.replay)
+        assert st["bufs"].device_status() == 0
+    except Exception as e:  # report the reason, not a number
+        out["us_per_step_graph"] = None
+        out["graph_error"] = str(e).splitlines()[0][:200]
+    return out
+
+
 def cpu_baseline_oracle(W, st, seconds: float):
     """The CPU oracle (single-threaded C, fp64) on full steps of input set 0."""
     import oracle
@@ -404,6 +453,10 @@ def run_ours(args, rank, world, local):
                      "committed_tokens_per_step": statistics.mean(
                          float(st["bufs"].num_emitted.sum().item()) for st in fixed)}
 
+    latency = None
+    if not args.no_latency:
+        latency = run_latency(binding, W, flush)
+
     e2e = None
     if not args.no_e2e:
         e2e_ms, h2d, d2h = run_e2e(binding, W, sets[0], args.e2e_steps, stream)
@@ -445,6 +498,7 @@ def run_ours(args, rank, world, local):
         "committed_tokens_per_step": statistics.mean(
             float(st["bufs"].num_emitted.sum().item()) for st in sets),
         "fixed_budget_arm": fixed_arm,
+        "latency_b1": latency,
     }
 
 
