@@ -145,6 +145,39 @@ def test_repeated_calls_reuse_the_workspace(cuda_lib):
     assert bufs.device_status() == 0
 
 
+@pytest.mark.parametrize("Tm", [0.0, 1.0])
+def test_graph_replay_matches_direct_calls(cuda_lib, Tm):
+    """The three calls captured as one CUDA graph (the cooperative verify and
+    the dependent compaction included) and replayed twice give the outputs of
+    direct calls, bit for bit, on the same buffers."""
+    from confidence_driven_speculative_gb300 import binding
+    inp = to_device(W.make_inputs(W.MIXED_B256, 9, B=24, V=20000, d=128, cap_T=60,
+                                  temperature=Tm))
+    ref, bufs = gpu_step(inp)  # direct calls; binds the ragged target rows
+    names = ("L", "row_off", "packed_ids", "accept_len", "num_emitted", "out_tokens",
+             "p_tok", "q_tok")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            binding.dspark_score_budget(bufs.step)
+            binding.dspark_compact(bufs.step)
+            binding.dspark_verify(bufs.step)
+    torch.cuda.current_stream().wait_stream(side)
+    commit = bufs._keep["seq_lens_commit"]
+    for _ in range(2):
+        for k in ("accept_len", "num_emitted", "out_tokens"):
+            getattr(bufs, k).fill_(-7)
+        commit.copy_(inp["seq_lens"])
+        g.replay()
+        torch.cuda.synchronize()
+        assert bufs.device_status() == 0
+        for k in names:
+            assert np.array_equal(getattr(bufs, k).cpu().numpy(), ref[k]), k
+        assert np.array_equal(commit.cpu().numpy(), ref["seq_lens_commit"])
+
+
 def test_empty_batch(cuda_lib):
     from confidence_driven_speculative_gb300 import binding
     step = binding.DsparkStep()
