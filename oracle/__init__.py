@@ -25,6 +25,9 @@ Function-to-source map (page titles and sections):
 * :func:`verify`, :func:`verify_request` -- same page, "Background"; and
   "SGLang Integrates DSpark ...", section "The Old Problem with Speculative
   Decoding: It Breaks Down at Scale" (speculative sampling).
+* :func:`verify_cap_accept` -- "DFlash to DSpark in SGLang", "The confidence
+  scheduler and verify modes" (the cap-accept audit arm) and "Scheduling
+  results" (utilization against the ceiling).
 
 Parity pins for every function are in ``tests/test_oracle_*.py``.
 """
@@ -313,3 +316,47 @@ def step(inp: dict, eps_s: float = 1e-5, eps_cap: float = 2e-5, eps_u: float = E
                res["draft_off"], inp["temperature"], inp["seed"], eps_u, inp.get("seq_lens"))
     res.update(v)
     return res
+
+
+def verify_cap_accept(draft_tokens, draft_logits, target_dense, L, W, Tm: float, seed: int,
+                      eps: float = EPS_U, seq_lens=None) -> dict:
+    """The cap-accept audit arm: verify the full block, commit only the window.
+
+    "DFlash to DSpark in SGLang", "The confidence scheduler and verify modes":
+    cap-accept pays the verify cost of the full block ``L`` (static: every
+    L_b = gamma) but commits what compact would commit with window ``W``, and
+    records what the trim gave up.  Written as its definition: two plain
+    verifies on the same target and draft logits and the same Philox stream.
+
+    * the full verify over ``L`` gives ``accept_full`` (the ceiling a_full)
+      and the per-draft ``p_tok`` / ``q_tok`` of the full layout;
+    * the window verify over ``min(max(W, 0), L)`` gives every committed
+      output (``accept_len``, ``num_emitted``, ``out_tokens``, ``seq_lens``).
+
+    ``audit_totals`` = (sum of a_full, sum of committed accept_len).  Their
+    ratio is the utilization against the ceiling of "Scheduling results",
+    read here as accepted drafts kept / accepted drafts a full verify finds.
+    ``tie`` flags a near tie in either verify.  ``target_dense`` is
+    [B, gamma+1, V]; both layouts are cut from it with :func:`ragged_target`.
+    """
+    draft_tokens = _c(draft_tokens, np.int32)
+    B, gamma = draft_tokens.shape
+    L = np.clip(_c(L, np.int32), 0, gamma).astype(np.int32)
+    Wc = np.minimum(np.maximum(_c(W, np.int32), 0), L).astype(np.int32)
+    full_lay = compact(L, draft_tokens)
+    full = verify(draft_tokens, draft_logits, ragged_target(target_dense, L, full_lay["row_off"]),
+                  L, full_lay["row_off"], full_lay["draft_off"], Tm, seed, eps)
+    win_lay = compact(Wc, draft_tokens)
+    win = verify(draft_tokens, draft_logits, ragged_target(target_dense, Wc, win_lay["row_off"]),
+                 Wc, win_lay["row_off"], win_lay["draft_off"], Tm, seed, eps, seq_lens)
+    out = {k: win[k] for k in ("accept_len", "num_emitted", "out_tokens")}
+    if "seq_lens" in win:
+        out["seq_lens"] = win["seq_lens"]
+    out["accept_full"] = full["accept_len"]
+    out["p_tok"] = full["p_tok"]
+    out["q_tok"] = full["q_tok"]
+    out["tie"] = (full["tie"] | win["tie"]).astype(np.int32)
+    out["W"] = Wc
+    out["audit_totals"] = np.array([int(full["accept_len"].sum()), int(win["accept_len"].sum())],
+                                   np.int64)
+    return out
