@@ -17,6 +17,10 @@ gamma=16, V=129280, d=7168, bf16, c=0.35, cap T=768, sampling at Tm=1.
 * e2e: the same metric through the C ABI with host inputs: every step copies
   its inputs from pinned host memory and reads the results back.
 * cpu_baseline: the CPU oracle (single thread) on the same workload.
+* cap_accept_arm: the audit arm on the same inputs -- the full block
+  verified, the confidence-driven window committed -- with its step time and
+  the utilization against the ceiling (accepted drafts kept / accepted drafts
+  the full verify finds).
 * latency_b1: the B=1 DeepSeek-class greedy step, microseconds per step with
   plain launches and replayed as one CUDA graph.
 * --impl reference: the CPU oracle as the reference arm (bounded samples).
@@ -61,6 +65,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-latency", action="store_true")
+    ap.add_argument("--no-audit-arm", action="store_true")
     ap.add_argument("--no-fixed-arm", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -263,6 +268,47 @@ def prepare_set(W, binding, w, step: int, fixed_budget: int = -1):
             "L_ref": bufs.L.clone(), "commit": commit}
 
 
+def prepare_audit(W, binding, w, step: int, window_set):
+    """The cap-accept audit arm on the same inputs: the full block (static,
+    every L_b = gamma) is verified and the window ``window_set`` (the
+    confidence-driven step on the same inputs) is committed."""
+    import torch
+    st = prepare_set(W, binding, w, step, fixed_budget=w.gamma)
+    st["window"] = window_set
+    st["accept_full"] = torch.zeros(w.B, dtype=torch.int32, device="cuda")
+    st["totals"] = torch.zeros(2, dtype=torch.int32, device="cuda")
+    binding.dspark_verify_cap_accept(st["bufs"].step, window_set["bufs"].L, st["accept_full"],
+                                     st["totals"])
+    torch.cuda.synchronize()
+    return st
+
+
+def audit_loop(binding, audit, K, W_, flush, stream):
+    """Warm-up, then K timed audit steps: the confidence-driven budget (the
+    window), the static budget and packing, the cap-accept verify."""
+    import torch
+    P = len(audit)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for i in range(W_ + K):
+        st = audit[i % P]
+        s, win = st["bufs"].step, st["window"]["bufs"]
+        flush.zero_()
+        e = ev[i - W_] if i >= W_ else None
+        if e:
+            e[0].record()
+        binding.dspark_score_budget(win.step, stream)
+        binding.dspark_score_budget(s, stream)
+        binding.dspark_compact(s, stream)
+        if e:
+            e[1].record()
+        binding.dspark_verify_cap_accept(s, win.L, st["accept_full"], st["totals"], stream)
+        if e:
+            e[2].record()
+    torch.cuda.synchronize()
+    return ev
+
+
 def run_steps(binding, sets, K, W_, flush, stream):
     """Warm up, then time exactly K steps with events (flush outside them)."""
     import torch
@@ -390,6 +436,10 @@ def cpu_baseline_oracle(W, st, seconds: float):
             "sample": f"{n} full steps of input set 0 ({npi['workload']}), {dt:.1f} s"}
 
 
+def mean_L_of(sets, B):
+    return statistics.mean(st["sum_L"] / B for st in sets)
+
+
 def run_ours(args, rank, world, local):
     import torch
     torch.cuda.set_device(local)
@@ -453,6 +503,29 @@ def run_ours(args, rank, world, local):
                      "committed_tokens_per_step": statistics.mean(
                          float(st["bufs"].num_emitted.sum().item()) for st in fixed)}
 
+    audit_arm = None
+    if not args.no_audit_arm:
+        audit = [prepare_audit(W, binding, w, s, sets[s]) for s in range(len(sets))]
+        eva = audit_loop(binding, audit, args.steps, args.warmup, flush, stream)
+        tot = [st["totals"].tolist() for st in audit]
+        same = sum(int(torch.equal(st["bufs"].out_tokens, st["window"]["bufs"].out_tokens))
+                   for st in audit)
+        same_req = sum(int((st["bufs"].out_tokens == st["window"]["bufs"].out_tokens)
+                           .all(dim=1).sum().item()) for st in audit)
+        ams = statistics.mean(e0.elapsed_time(e2) for e0, _, e2 in eva)
+        audit_arm = {
+            "mode": "cap-accept: static block (L_b = gamma) verified, confidence-driven "
+                    "window committed",
+            "ms_per_step": ams, "steps_per_s": 1000.0 / ams,
+            "verify_ms": statistics.mean(e1.elapsed_time(e2) for _, e1, e2 in eva),
+            "utilization": sum(t[1] for t in tot) / max(1, sum(t[0] for t in tot)),
+            "accepted_full_per_step": statistics.mean(t[0] for t in tot),
+            "accepted_committed_per_step": statistics.mean(t[1] for t in tot),
+            "trimmed_away_per_step": statistics.mean(t[0] - t[1] for t in tot),
+            "mean_window": mean_L_of(sets, B),
+            "commit_equals_compact_sets": f"{same}/{len(audit)}",
+            "commit_equals_compact_requests": f"{same_req}/{len(audit) * B}"}
+
     latency = None
     if not args.no_latency:
         latency = run_latency(binding, W, flush)
@@ -471,7 +544,7 @@ def run_ours(args, rank, world, local):
 
     if rank != 0:
         return None
-    mean_L = statistics.mean(st["sum_L"] / B for st in sets)
+    mean_L = mean_L_of(sets, B)
     return {
         "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -498,6 +571,7 @@ def run_ours(args, rank, world, local):
         "committed_tokens_per_step": statistics.mean(
             float(st["bufs"].num_emitted.sum().item()) for st in sets),
         "fixed_budget_arm": fixed_arm,
+        "cap_accept_arm": audit_arm,
         "latency_b1": latency,
     }
 

@@ -69,6 +69,8 @@ def load():
             fn = getattr(lib, name)
             fn.argtypes = [SP, _P]
             fn.restype = ctypes.c_int
+        lib.dspark_verify_cap_accept.argtypes = [SP, _P, _P, _P, _P]
+        lib.dspark_verify_cap_accept.restype = ctypes.c_int
         lib.dspark_verify_noalloc.argtypes = [SP, ctypes.c_int32, _P, _P]
         lib.dspark_verify_noalloc.restype = ctypes.c_int
         lib.dspark_workspace_size.argtypes = [ctypes.c_int32] * 4
@@ -115,6 +117,18 @@ def dspark_compact(step: DsparkStep, stream=None, check: bool = True) -> int:
 
 def dspark_verify(step: DsparkStep, stream=None, check: bool = True) -> int:
     return _call("dspark_verify", step, stream, check)
+
+
+def dspark_verify_cap_accept(step: DsparkStep, commit_len, accept_full=None, audit_totals=None,
+                             stream=None, check: bool = True) -> int:
+    """The cap-accept audit arm: verify the step's full block, commit the
+    window ``commit_len`` (device int32 [B]).  ``accept_full`` (device int32
+    [B]) and ``audit_totals`` (device int32 [2]) are optional outputs."""
+    rc = load().dspark_verify_cap_accept(ctypes.byref(step), _ptr(commit_len), _ptr(accept_full),
+                                         _ptr(audit_totals), _stream(stream))
+    if check and rc != DSPARK_OK:
+        raise DsparkError(rc, "dspark_verify_cap_accept")
+    return rc
 
 
 DSPARK_NOALLOC_SCRATCH_BYTES = 8 << 20

@@ -206,8 +206,13 @@ dspark_status dspark_compact(const dspark_step *s, dspark_stream_t stream) {
     return DSPARK_OK;
 }
 
-dspark_status dspark_verify(const dspark_step *s, dspark_stream_t stream) {
-    const char *fn = "dspark_verify";
+}  // extern "C"
+
+// The verify launch shared by dspark_verify (audit pointers NULL) and
+// dspark_verify_cap_accept.
+static dspark_status verify_impl(const dspark_step *s, const int32_t *commit_len,
+                                 int32_t *accept_full, int32_t *audit_totals,
+                                 dspark_stream_t stream, const char *fn) {
     dspark_status st = check_shape(s);
     if (st) return st;
     if (s->B == 0) return DSPARK_OK;
@@ -276,12 +281,29 @@ dspark_status dspark_verify(const dspark_step *s, dspark_stream_t stream) {
     a.join = ws_at<int32_t>(s, lay.join);
     a.rejflag = ws_at<int32_t>(s, lay.rejflag);
     a.status = ws_at<int32_t>(s, lay.status);
+    a.commit_len = commit_len;
+    a.accept_full = accept_full;
+    a.audit_totals = audit_totals;
     // One CTA per resident slot: the cooperative launch requires it, and the
     // work is spread over the grid inside the kernel.
     const int grid = dev->sms * dev->verify_blocks[bf];
     cudaError_t e = dspark::launch_verify(a, bf, grid, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "verify_kernel launch");
     return DSPARK_OK;
+}
+
+extern "C" {
+
+dspark_status dspark_verify(const dspark_step *s, dspark_stream_t stream) {
+    return verify_impl(s, nullptr, nullptr, nullptr, stream, "dspark_verify");
+}
+
+dspark_status dspark_verify_cap_accept(const dspark_step *s, const int32_t *commit_len,
+                                       int32_t *accept_full, int32_t *audit_totals,
+                                       dspark_stream_t stream) {
+    const char *fn = "dspark_verify_cap_accept";
+    if (s && s->B > 0 && !commit_len) return fail(DSPARK_EINVAL, "%s: commit_len is NULL", fn);
+    return verify_impl(s, commit_len, accept_full, audit_totals, stream, fn);
 }
 
 dspark_status dspark_read_device_status(const void *workspace, int32_t *status_out,

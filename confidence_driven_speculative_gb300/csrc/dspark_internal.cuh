@@ -45,7 +45,8 @@ struct WorkspaceLayout {
     size_t bon_cnt;       // int32 [B]   per-request bonus-row tiles done
     size_t join;          // int32 [B]   drafts all accepted + bonus row streamed
     size_t rejflag;       // int32 [B]   launch epoch of a found rejection
-    size_t q_ctr;         // int32 [8]   queue head, tail, finished, exited, epoch, chunk
+    size_t q_ctr;         // int32 [16]  queue heads / tails, finished, exited, epoch, chunk,
+                          //             audit totals
     size_t rowrec;        // float4 [B*(gamma+1) * nc]      row partials per (row, chunk)
     size_t blkrec;        // float2 [B * nblk * 8]          bonus-row block partials per warp
     size_t zrec;          // float2 [B * nblk * 8]          residual / p block masses per warp
@@ -80,7 +81,7 @@ inline WorkspaceLayout workspace_layout(int B, int gamma, int V) {
     w.bon_cnt = off;     off = align256(off + sizeof(int32_t) * size_t(B));
     w.join = off;        off = align256(off + sizeof(int32_t) * size_t(B));
     w.rejflag = off;     off = align256(off + sizeof(int32_t) * size_t(B));
-    w.q_ctr = off;       off = align256(off + sizeof(int32_t) * 8);
+    w.q_ctr = off;       off = align256(off + sizeof(int32_t) * 16);
     w.rowrec = off;      off = align256(off + 16 * rows * size_t(w.nc));
     w.blkrec = off;      off = align256(off + 8 * size_t(B) * w.nblk * warps);
     w.zrec = off;        off = align256(off + 8 * size_t(B) * w.nblk * warps);
@@ -351,6 +352,10 @@ struct VerifyArgs {
     int32_t *qb_job, *qb_ready;
     int32_t *req_cnt, *r1_cnt, *status;
     int32_t *bon_cnt, *join, *rejflag;
+    // Cap-accept audit (all NULL on the plain verify): the window W_b that is
+    // committed, the full-block acceptance a_b, and the batch totals.
+    const int32_t *commit_len;
+    int32_t *accept_full, *audit_totals;
 };
 
 cudaError_t launch_score_budget(const ScoreArgs &a, int grid, cudaStream_t s);

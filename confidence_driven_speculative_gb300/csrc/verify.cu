@@ -61,9 +61,9 @@ constexpr size_t kSmemBytes = size_t(kStages) * kStageBytes;
 enum : int { T_EXIT = 0, T_STREAM = 1, T_RESID = 2 };
 enum : int { D_BONUS = 0, D_RESID = 1, D_FALLBACK = 2 };
 // q_ctr words: residual-tile queue head / tail, finished requests, exited CTAs,
-// launch epoch, stream-chunk counter, decide queue head / tail.
+// launch epoch, stream-chunk counter, decide queue head / tail, audit sums.
 enum : int { QA_HEAD = 0, QA_TAIL = 1, Q_FINISHED = 2, Q_EXITED = 3, Q_EPOCH = 4, Q_CHUNK = 5,
-             QB_HEAD = 6, QB_TAIL = 7 };
+             QB_HEAD = 6, QB_TAIL = 7, Q_AFULL = 8, Q_ACOMMIT = 9 };
 
 struct TaskInfo {
     int type;   // T_*
@@ -930,11 +930,17 @@ __device__ void decide_request(const VerifyArgs &a, const StreamShape &sh, int b
                                int epoch, int lane) {
     // Round 1: lengths, offsets and draft tokens.
     const int Lb = verify_len(a, b), r0 = a.row_off[b], d0 = a.draft_off[b];
+    // Committed window: L_b, or in the cap-accept audit the scheduled W_b
+    // clamped to [0, L_b] (the full block is verified, the window committed).
+    const int W = a.commit_len ? min(max(__ldcg(a.commit_len + b), 0), Lb) : Lb;
     const Drafts dr = load_drafts(a, b, lane);
     const float scale = a.scale;
     int ab = Lb;                                   // first rejected draft (L_b: none)
-    float Mp = 0.f, Sp = 0.f, Mq = 0.f, Sq = 0.f;  // normalisers of row a_b (sampling)
-    float ub = 0.f, ut = 0.f;                      // block / token uniforms of row a_b
+    // Normalisers and uniforms of the row the emitted token is drawn from:
+    // min(a_b, W) -- row a_b after a rejection inside the window, row W when
+    // the window ends inside the accepted run.
+    float Mp = 0.f, Sp = 0.f, Mq = 0.f, Sq = 0.f;
+    float ub = 0.f, ut = 0.f;
     int g_tok = 0;
     // Round 2, one lane per row k (two rounds when gamma > 32): the row's
     // chunk records and its gathered z values.
@@ -997,7 +1003,7 @@ __device__ void decide_request(const VerifyArgs &a, const StreamShape &sh, int b
         const unsigned rows = __ballot_sync(0xffffffffu, live);
         const unsigned rej = rows & ~acc;
         if (ab == Lb && rej) ab = base + __ffs(rej) - 1;
-        const int src = ab - base;
+        const int src = min(ab, W) - base;
         const int sl_ = src >= 0 && src < 32 ? src : 0;
         const float m1 = __shfl_sync(0xffffffffu, rr.x, sl_), s1 = __shfl_sync(0xffffffffu, rr.y, sl_);
         const float m2 = __shfl_sync(0xffffffffu, rr.z, sl_), s2 = __shfl_sync(0xffffffffu, rr.w, sl_);
@@ -1012,15 +1018,24 @@ __device__ void decide_request(const VerifyArgs &a, const StreamShape &sh, int b
             g_tok = __float_as_int(s1);  // greedy: the row's argmax
         }
     }
-    if (ab < Lb) {
+    const int acc = min(ab, W);  // committed drafts
+    if (lane == 0 && a.accept_full) a.accept_full[b] = ab;
+    if (lane == 0 && a.audit_totals) {
+        atomicAdd(&a.q_ctr[Q_AFULL], ab);
+        atomicAdd(&a.q_ctr[Q_ACOMMIT], acc);
+    }
+    if (acc < Lb) {
+        // A rejection inside the window (residual draw at row a_b), or a
+        // window that ends inside the accepted run (draw from p at row W,
+        // what compact's bonus draw would be).  The bonus row is not needed.
         if (lane == 0) st_relaxed(&a.rejflag[b], epoch);  // phase Q skips the bonus row
         if (a.greedy) {
-            finish_request(a, b, ab, g_tok, dr, lane);
+            finish_request(a, b, acc, g_tok, dr, lane);
             return;
         }
         DecideState st;
-        st.a = ab;
-        st.mode = D_RESID;
+        st.a = acc;
+        st.mode = ab < W ? D_RESID : D_FALLBACK;
         st.Mp = Mp;
         st.Sp = Sp;
         st.Mq = Mq;
@@ -1085,9 +1100,10 @@ __device__ void finish_residual(const VerifyArgs &a, int b, int wpb, int lane) {
         const int i = t0 + lane;
         total = total + warp_sum_f2(i < a.nblk ? mass(i, true) : f2(0.f));
     }
-    const bool residual = total.hi > 0.f;
+    const bool residual = st.mode == D_RESID && total.hi > 0.f;
     if (!residual) {
-        // No residual mass: draw from p of the same row instead.
+        // A draw from p (window cut inside the accepted run), or no residual
+        // mass: draw from p of the same row.
         st.mode = D_FALLBACK;
         st.Sp = 1.f;
     }
@@ -1350,6 +1366,10 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(const VerifyA
             a.q_ctr[Q_CHUNK] = 0;
             a.q_ctr[Q_EXITED] = 0;
             a.q_ctr[Q_EPOCH] = epoch;
+            if (a.audit_totals) {
+                a.audit_totals[0] = atomicExch(&a.q_ctr[Q_AFULL], 0);
+                a.audit_totals[1] = atomicExch(&a.q_ctr[Q_ACOMMIT], 0);
+            }
         }
         __threadfence();
     }

@@ -212,6 +212,40 @@ dspark_status dspark_compact(const dspark_step *step, dspark_stream_t stream);
 dspark_status dspark_verify(const dspark_step *step, dspark_stream_t stream);
 
 /*
+ * The cap-accept audit arm of steps a5-a6.  [DS] "The confidence scheduler
+ * and verify modes": cap-accept verifies the full block like static, so it
+ * costs what static costs, but commits only the scheduled window, so its
+ * output is compact's; it records what the trim gave up.  [DS] "Scheduling
+ * results" quotes utilization against the ceiling from such runs.
+ *
+ * The step's L, draft_off, row_off and target_logits describe the block
+ * that is verified (for the static audit: fixed_budget = gamma in
+ * dspark_score_budget, then dspark_compact).  commit_len[b] (device, [B],
+ * read only) is the window W_b the scheduler chose (the L of a
+ * confidence-driven dspark_score_budget); it is clamped to [0, L_b].
+ * Every draft k < L_b is verified as in dspark_verify; with a_b the first
+ * rejected k (L_b if none), the committed drafts are min(a_b, W_b):
+ *   - a_b < W_b: the residual draw at row a_b, as in dspark_verify;
+ *   - a_b >= W_b, W_b < L_b: the window ends inside the accepted run; the
+ *     token is drawn from p at row W_b with the uniforms (u', u'') of
+ *     position W_b -- the bonus draw compact would make with L_b = W_b
+ *     (greedy: the argmax of row W_b);
+ *   - a_b = W_b = L_b: the bonus draw at row L_b.
+ * accept_len, num_emitted, out_tokens and seq_lens_commit hold the
+ * committed result; p_tok and q_tok cover every draft k < L_b of the block.
+ *
+ * accept_full:  device int32 [B] or NULL; receives a_b, the acceptance of
+ *               the full verify (the ceiling).
+ * audit_totals: device int32 [2] or NULL; receives (sum of a_b, sum of
+ *               accept_len) over the batch.  Their ratio is the utilization
+ *               against the ceiling.
+ * Errors as dspark_verify; commit_len NULL with B > 0 is DSPARK_EINVAL.
+ */
+dspark_status dspark_verify_cap_accept(const dspark_step *step, const int32_t *commit_len,
+                                       int32_t *accept_full, int32_t *audit_totals,
+                                       dspark_stream_t stream);
+
+/*
  * Blocking read of the workspace's device status word (0 = healthy).  A
  * nonzero value means a kernel gave up on a bounded wait; the workspace must
  * then be re-initialised.  Synchronises `stream`.

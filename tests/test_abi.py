@@ -170,3 +170,10 @@ def test_verify_validation(lib):
 
 def test_version(lib):
     assert "sm_103a" in binding.version()
+
+
+def test_cap_accept_needs_a_window(lib):
+    s = valid_step()
+    assert lib.dspark_verify_cap_accept(ctypes.byref(s), None, None, None, None) == binding.DSPARK_EINVAL
+    assert "commit_len" in binding.last_error()
+    assert lib.dspark_verify_cap_accept(None, None, None, None, None) == binding.DSPARK_EINVAL
