@@ -513,11 +513,16 @@ def run_ours(args, rank, world, local):
         same_req = sum(int((st["bufs"].out_tokens == st["window"]["bufs"].out_tokens)
                            .all(dim=1).sum().item()) for st in audit)
         ams = statistics.mean(e0.elapsed_time(e2) for e0, _, e2 in eva)
+        avm = statistics.mean(e1.elapsed_time(e2) for _, e1, e2 in eva)
+        avb = verify_bytes(B, B * g, V, ls, sampling, g)
         audit_arm = {
             "mode": "cap-accept: static block (L_b = gamma) verified, confidence-driven "
                     "window committed",
             "ms_per_step": ams, "steps_per_s": 1000.0 / ams,
-            "verify_ms": statistics.mean(e1.elapsed_time(e2) for _, e1, e2 in eva),
+            "verify_ms": avm,
+            "verify_bytes_per_launch": avb,
+            "verify_gbs": avb / (avm * 1e-3) / 1e9,
+            "verify_frac": avb / (avm * 1e-3) / 1e9 / peak,
             "utilization": sum(t[1] for t in tot) / max(1, sum(t[0] for t in tot)),
             "accepted_full_per_step": statistics.mean(t[0] for t in tot),
             "accepted_committed_per_step": statistics.mean(t[1] for t in tot),
