@@ -18,6 +18,9 @@ Function-to-source map (page titles and sections):
 * :func:`philox4x64_10`, :func:`uniforms` -- Salmon et al., SC'11, Philox4x64-10.
 * :func:`score` -- "DFlash to DSpark in SGLang", section "DSpark: a sequential
   head and a verify budget" (confidence head, STS, survival, budget rule).
+* :func:`score_entropy` -- "SGLang Integrates DSpark ...", section "DSpark's
+  Core Idea: Only Verify the Parts You're Confident About" (confidence from
+  the entropy of the drafter's distribution); survival and budget as above.
 * :func:`cap` -- same page, section "Zero-overhead scheduling and kernels"
   (verify-length top-k schedule under a batch-wide cap).
 * :func:`fixed_budget` -- same page, "The confidence scheduler and verify modes".
@@ -75,6 +78,7 @@ def _load():
             lib.orc_uniforms.argtypes = [u64, i64, i64, P, P, P]
             lib.orc_uniforms.restype = None
             lib.orc_score.argtypes = [i32, i32, i32, i32, P, P, P, P, f64, f64, P, P, P, P]
+            lib.orc_score_entropy.argtypes = [i32, i32, i32, i32, P, f64, f64, f64, P, P, P, P]
             lib.orc_fixed_budget.argtypes = [i32, i32, i32, P]
             lib.orc_cap.argtypes = [i32, i32, P, P, i32, f64, P, P]
             lib.orc_compact.argtypes = [i32, i32, P, P, P, P, P, P, P, P, P, P]
@@ -82,8 +86,8 @@ def _load():
                                                f64, P, P, P, P, P]
             lib.orc_verify.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, f64, u64, f64, f64,
                                        f64, P, P, P, P, P, P, P]
-            for name in ("orc_score", "orc_fixed_budget", "orc_cap", "orc_compact",
-                         "orc_verify_request", "orc_verify"):
+            for name in ("orc_score", "orc_score_entropy", "orc_fixed_budget", "orc_cap",
+                         "orc_compact", "orc_verify_request", "orc_verify"):
                 getattr(lib, name).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -152,6 +156,27 @@ def score(hidden, w, bias, tau, c: float, eps: float = 1e-5):
                        _ptr(tau), float(np.float32(c)), eps, _ptr(conf), _ptr(surv), _ptr(L0),
                        _ptr(tie))
     _check(rc, "score")
+    return conf, surv, L0, tie
+
+
+def score_entropy(draft_logits, theta: float, c: float, eps: float = 1e-5):
+    """Entropy confidence + survival + pre-cap budget.
+
+    ``draft_logits`` [B, gamma, V]; ``theta`` the temperature of the
+    drafter's distribution q = softmax(z_q / theta).  conf = exp(-H(q)).
+    Returns ``(conf, surv, L0, tie)`` as :func:`score`.
+    """
+    lib = _load()
+    z = np.ascontiguousarray(draft_logits)
+    B, gamma, V = z.shape
+    conf = np.zeros((B, gamma), np.float64)
+    surv = np.zeros((B, gamma), np.float64)
+    L0 = np.zeros(B, np.int32)
+    tie = np.zeros(B, np.int32)
+    rc = lib.orc_score_entropy(B, gamma, V, _logit_dtype(z), _ptr(z), float(np.float32(theta)),
+                               float(np.float32(c)), eps, _ptr(conf), _ptr(surv), _ptr(L0),
+                               _ptr(tie))
+    _check(rc, "score_entropy")
     return conf, surv, L0, tie
 
 

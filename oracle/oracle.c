@@ -111,6 +111,64 @@ static double elem(const void *base, int dtype, int64_t i)
 }
 
 /* ------------------------------------------------------------------------ */
+/* a1 + a2, entropy-confidence variant.                                     */
+/*   [KC] "DSpark's Core Idea: Only Verify the Parts You're Confident        */
+/*   About": the lower the entropy of the drafter's output distribution at  */
+/*   a position, the more certain the drafter and the likelier the draft is */
+/*   accepted; verification goes to low-entropy positions.  Reading taken:   */
+/*   q = softmax(z_q / theta) over the vocabulary, H = -sum_y q(y) ln q(y)    */
+/*   (nats), conf = exp(-H) -- the q-weighted geometric mean of q, in        */
+/*   (1/V, 1], 1 for a one-hot q and 1/V for a uniform one.  The survival    */
+/*   curve and the budget then follow orc_score's definitions.               */
+/* H is taken from its definition with a shifted exponent: with m the row   */
+/* maximum of x = z / theta, e_y = exp(x_y - m), s = sum e_y,                */
+/*   H = ln s - sum_y (e_y / s) (x_y - m).                                   */
+/* Inputs: draft_logits [B, gamma, V] (dtype 0 fp32 / 1 bf16), theta > 0.    */
+/* Outputs as orc_score.                                                     */
+/* ------------------------------------------------------------------------ */
+int orc_score_entropy(int B, int gamma, int V, int dtype, const void *draft_logits,
+                      double theta, double c, double eps, double *conf, double *surv,
+                      int32_t *L0, int32_t *tie)
+{
+    if (B < 0 || gamma < 1 || V < 1 || !(theta > 0.0)) return -1;
+    double *x = (double *)malloc(sizeof(double) * (size_t)V);
+    if (!x) return -2;
+    for (int b = 0; b < B; ++b) {
+        for (int i = 0; i < gamma; ++i) {
+            const int64_t row = ((int64_t)b * gamma + i) * V;
+            double m = -INFINITY;
+            for (int y = 0; y < V; ++y) {
+                x[y] = elem(draft_logits, dtype, row + y) / theta;
+                if (x[y] > m) m = x[y];
+            }
+            double s = 0.0;
+            for (int y = 0; y < V; ++y) s += exp(x[y] - m);
+            double mean = 0.0; /* sum_y q(y) (x_y - m) */
+            for (int y = 0; y < V; ++y) {
+                const double e = exp(x[y] - m);
+                if (e > 0.0) mean += (e / s) * (x[y] - m);
+            }
+            const double H = log(s) - mean;
+            conf[b * gamma + i] = exp(-H);
+        }
+        double S = 1.0; /* S_0 */
+        int32_t L = (1.0 >= c) ? 0 : -1;
+        int32_t ties = 0;
+        for (int k = 1; k <= gamma; ++k) {
+            S = S * conf[b * gamma + (k - 1)];
+            surv[b * gamma + (k - 1)] = S;
+            if (S >= c) L = k;
+            if (fabs(S - c) < eps) ties++;
+        }
+        if (fabs(1.0 - c) < eps) ties++;
+        L0[b] = (L < 0) ? 0 : L;
+        tie[b] = ties;
+    }
+    free(x);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* a1 + a2.  Confidence head with Sequential Temperature Scaling, survival,  */
 /* pre-cap verify length.                                                    */
 /*   [DS] "DSpark: a sequential head and a verify budget": the head is a     */
