@@ -21,6 +21,9 @@ gamma=16, V=129280, d=7168, bf16, c=0.35, cap T=768, sampling at Tm=1.
   verified, the confidence-driven window committed -- with its step time and
   the utilization against the ceiling (accepted drafts kept / accepted drafts
   the full verify finds).
+* entropy_arm: the step with the entropy-confidence variant of the score
+  (conf = exp(-H) of each draft row at theta = 0.3): step time, the score
+  kernel's time and bandwidth over the B*gamma*V draft logits it streams.
 * latency_b1: the B=1 DeepSeek-class greedy step, microseconds per step with
   plain launches and replayed as one CUDA graph.
 * --impl reference: the CPU oracle as the reference arm (bounded samples).
@@ -66,6 +69,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-latency", action="store_true")
     ap.add_argument("--no-audit-arm", action="store_true")
+    ap.add_argument("--no-entropy-arm", action="store_true")
     ap.add_argument("--no-fixed-arm", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -243,7 +247,7 @@ def profiled_traffic():
 # --------------------------------------------------------------------------- #
 # our arm
 # --------------------------------------------------------------------------- #
-def prepare_set(W, binding, w, step: int, fixed_budget: int = -1):
+def prepare_set(W, binding, w, step: int, fixed_budget: int = -1, entropy_theta=None):
     import torch
     kw = {"fixed_budget": fixed_budget}
     if fixed_budget >= 0:
@@ -252,7 +256,10 @@ def prepare_set(W, binding, w, step: int, fixed_budget: int = -1):
     bufs = binding.StepBuffers(inp["B"], inp["gamma"], inp["V"], inp["d"])
     commit = inp["seq_lens"].clone()
     bufs.bind(inp, seq_lens_commit=commit)
-    binding.dspark_score_budget(bufs.step)
+    if entropy_theta is None:
+        binding.dspark_score_budget(bufs.step)
+    else:
+        binding.dspark_score_entropy(bufs.step, entropy_theta)
     binding.dspark_compact(bufs.step)
     torch.cuda.synchronize()
     n_rows = int(bufs.row_off[inp["B"]].item())
@@ -303,6 +310,34 @@ def audit_loop(binding, audit, K, W_, flush, stream):
         if e:
             e[1].record()
         binding.dspark_verify_cap_accept(s, win.L, st["accept_full"], st["totals"], stream)
+        if e:
+            e[2].record()
+    torch.cuda.synchronize()
+    return ev
+
+
+ENTROPY_THETA = 0.3
+
+
+def entropy_loop(binding, sets, K, W_, flush, stream, theta):
+    """Warm-up, then K timed steps of the entropy-confidence variant:
+    score_entropy, compact, verify (events around the score kernel and the
+    whole step)."""
+    import torch
+    P = len(sets)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for i in range(W_ + K):
+        s = sets[i % P]["bufs"].step
+        flush.zero_()
+        e = ev[i - W_] if i >= W_ else None
+        if e:
+            e[0].record()
+        binding.dspark_score_entropy(s, theta, stream)
+        if e:
+            e[1].record()
+        binding.dspark_compact(s, stream)
+        binding.dspark_verify(s, stream)
         if e:
             e[2].record()
     torch.cuda.synchronize()
@@ -531,6 +566,25 @@ def run_ours(args, rank, world, local):
             "commit_equals_compact_sets": f"{same}/{len(audit)}",
             "commit_equals_compact_requests": f"{same_req}/{len(audit) * B}"}
 
+    entropy_arm = None
+    if not args.no_entropy_arm:
+        ent = [prepare_set(W, binding, w, s, entropy_theta=ENTROPY_THETA) for s in range(len(sets))]
+        eve = entropy_loop(binding, ent, args.steps, args.warmup, flush, stream, ENTROPY_THETA)
+        for st in ent:
+            assert torch.equal(st["bufs"].L, st["L_ref"]), "entropy verify lengths changed"
+            assert st["bufs"].device_status() == 0
+        ems = statistics.mean(e0.elapsed_time(e2) for e0, _, e2 in eve)
+        sms = statistics.mean(e0.elapsed_time(e1) for e0, e1, _ in eve)
+        sbytes = B * g * V * ls + 4 * (2 * B * g + 4 * B + 2)
+        entropy_arm = {
+            "theta": ENTROPY_THETA, "ms_per_step": ems, "steps_per_s": 1000.0 / ems,
+            "score_entropy_us": sms * 1000.0, "score_entropy_bytes_per_launch": sbytes,
+            "score_entropy_gbs": sbytes / (sms * 1e-3) / 1e9,
+            "score_entropy_frac": sbytes / (sms * 1e-3) / 1e9 / peak,
+            "mean_L": mean_L_of(ent, B),
+            "committed_tokens_per_step": statistics.mean(
+                float(st["bufs"].num_emitted.sum().item()) for st in ent)}
+
     latency = None
     if not args.no_latency:
         latency = run_latency(binding, W, flush)
@@ -577,6 +631,7 @@ def run_ours(args, rank, world, local):
             float(st["bufs"].num_emitted.sum().item()) for st in sets),
         "fixed_budget_arm": fixed_arm,
         "cap_accept_arm": audit_arm,
+        "entropy_arm": entropy_arm,
         "latency_b1": latency,
     }
 

@@ -69,6 +69,8 @@ def load():
             fn = getattr(lib, name)
             fn.argtypes = [SP, _P]
             fn.restype = ctypes.c_int
+        lib.dspark_score_entropy.argtypes = [SP, ctypes.c_float, _P]
+        lib.dspark_score_entropy.restype = ctypes.c_int
         lib.dspark_verify_cap_accept.argtypes = [SP, _P, _P, _P, _P]
         lib.dspark_verify_cap_accept.restype = ctypes.c_int
         lib.dspark_verify_noalloc.argtypes = [SP, ctypes.c_int32, _P, _P]
@@ -109,6 +111,14 @@ def _call(name: str, step: DsparkStep, stream, check: bool) -> int:
 
 def dspark_score_budget(step: DsparkStep, stream=None, check: bool = True) -> int:
     return _call("dspark_score_budget", step, stream, check)
+
+
+def dspark_score_entropy(step: DsparkStep, theta: float, stream=None, check: bool = True) -> int:
+    """Steps a1-a3 with conf = exp(-entropy of softmax(draft logits / theta))."""
+    rc = load().dspark_score_entropy(ctypes.byref(step), float(theta), _stream(stream))
+    if check and rc != DSPARK_OK:
+        raise DsparkError(rc, "dspark_score_entropy")
+    return rc
 
 
 def dspark_compact(step: DsparkStep, stream=None, check: bool = True) -> int:

@@ -35,6 +35,7 @@ struct DeviceInfo {
     int sms = 0;
     int verify_blocks[2] = {0, 0};  // per logit dtype (0 = fp32, 1 = bf16)
     int score_blocks[2] = {0, 0};   // per hidden dtype
+    int entropy_blocks[2] = {0, 0}; // per logit dtype
 };
 constexpr int kMaxDevices = 64;
 DeviceInfo g_dev[kMaxDevices];
@@ -64,6 +65,9 @@ dspark_status device_info(DeviceInfo **out) {
             d.score_blocks[bf] = dspark::score_blocks_per_sm(bf);
             if (d.score_blocks[bf] <= 0)
                 return fail(DSPARK_ECUDA, "score kernel cannot be resident");
+            d.entropy_blocks[bf] = dspark::entropy_blocks_per_sm(bf);
+            if (d.entropy_blocks[bf] <= 0)
+                return fail(DSPARK_ECUDA, "entropy score kernel cannot be resident");
         }
         d.ready = true;
     }
@@ -182,6 +186,52 @@ dspark_status dspark_score_budget(const dspark_step *s, dspark_stream_t stream) 
     a.status = ws_at<int32_t>(s, lay.status);
     cudaError_t e = dspark::launch_score_budget(a, grid, cs);
     if (e != cudaSuccess) return cuda_fail(e, "score_budget_kernel launch");
+    return DSPARK_OK;
+}
+
+dspark_status dspark_score_entropy(const dspark_step *s, float theta, dspark_stream_t stream) {
+    const char *fn = "dspark_score_entropy";
+    dspark_status st = check_shape(s);
+    if (st) return st;
+    if (!(theta > 0.0f) || std::isinf(theta))
+        return fail(DSPARK_EINVAL, "%s: theta must be finite and > 0", fn);
+    if (s->fixed_budget >= 0)
+        return fail(DSPARK_EINVAL, "%s: a fixed budget has no confidences (use dspark_score_budget)",
+                    fn);
+    if (std::isnan(s->cost_c)) return fail(DSPARK_EINVAL, "%s: cost_c is NaN", fn);
+    if (s->B == 0) return DSPARK_OK;
+    REQUIRE(s->draft_logits);
+    REQUIRE(s->conf);
+    REQUIRE(s->survival);
+    REQUIRE(s->L0);
+    REQUIRE(s->L);
+    REQUIRE(s->draft_off);
+    REQUIRE(s->row_off);
+    const size_t ls = dtype_size(s->logit_dtype);
+    REQUIRE_ALIGNED(s->draft_logits, 16);
+    if ((size_t(s->V) * ls) % 16 != 0)
+        return fail(DSPARK_EALIGN, "%s: a logit row (V=%d) is not a multiple of 16 bytes", fn, s->V);
+    dspark::WorkspaceLayout lay;
+    if ((st = check_workspace(s, &lay))) return st;
+    DeviceInfo *dev;
+    if ((st = device_info(&dev))) return st;
+
+    const long long rows = (long long)s->B * s->gamma;
+    const int bf = s->logit_dtype == DSPARK_BF16;
+    const int grid = int(std::min<long long>(rows, (long long)dev->sms * dev->entropy_blocks[bf]));
+    dspark::ScoreArgs a{};
+    a.B = s->B; a.gamma = s->gamma; a.d = s->V;
+    a.hidden_bf16 = bf;
+    a.hidden = s->draft_logits;
+    a.ent_scale = float(1.4426950408889634 / double(theta));
+    a.cost_c = s->cost_c; a.cap_T = s->cap_T;
+    a.conf = s->conf; a.survival = s->survival; a.L0 = s->L0; a.L = s->L;
+    a.draft_off = s->draft_off; a.row_off = s->row_off;
+    a.done_cnt = ws_at<int32_t>(s, lay.score_done);
+    a.row_ctr = ws_at<int32_t>(s, lay.score_rows);
+    a.status = ws_at<int32_t>(s, lay.status);
+    cudaError_t e = dspark::launch_score_entropy(a, grid, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "score_budget_kernel (entropy) launch");
     return DSPARK_OK;
 }
 

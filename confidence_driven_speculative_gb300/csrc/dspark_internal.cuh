@@ -312,6 +312,9 @@ struct ScoreArgs {
     float *conf, *survival;
     int32_t *L0, *L, *draft_off, *row_off;
     int32_t *done_cnt, *row_ctr, *status;
+    // Entropy-confidence variant: hidden points at the draft logits, d = V,
+    // and ent_scale = log2(e) / theta.
+    float ent_scale;
 };
 
 struct FixedArgs {
@@ -360,6 +363,8 @@ struct VerifyArgs {
 
 cudaError_t launch_score_budget(const ScoreArgs &a, int grid, cudaStream_t s);
 int score_blocks_per_sm(int hidden_bf16);
+cudaError_t launch_score_entropy(const ScoreArgs &a, int grid, cudaStream_t s);
+int entropy_blocks_per_sm(int logit_bf16);
 cudaError_t launch_fixed_budget(const FixedArgs &a, cudaStream_t s);
 cudaError_t launch_compact(const CompactArgs &a, cudaStream_t s);
 cudaError_t launch_verify(const VerifyArgs &a, int logit_bf16, int grid, cudaStream_t s);

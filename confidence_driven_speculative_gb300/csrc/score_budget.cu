@@ -258,6 +258,153 @@ __device__ int score_consumer(const ScoreArgs &a, ScoreSmem &sm, const uint8_t *
 }
 
 // ---------------------------------------------------------------------------
+// Entropy-confidence variant ("SGLang Integrates DSpark ...", "DSpark's Core
+// Idea: Only Verify the Parts You're Confident About": a low-entropy draft
+// distribution is a confident one).  conf = exp(-H(q)), q = softmax(z / theta),
+// over the draft logit row of each draft.  The rows stream through the same
+// ring; each thread keeps, in log2 units y = z log2(e) / theta,
+//   m = max y,  s = sum 2^(y - m),  t = sum 2^(y - m) (y - m),
+// so that H = ln 2 (log2 s - t / s) and conf = 2^(t / s) / s.
+// ---------------------------------------------------------------------------
+struct Ent {
+    float m, s, t;
+};
+
+// Bring both onto the larger maximum and add.  An empty side (s = 0, no
+// finite logit seen, m = -inf) is skipped.
+__device__ __forceinline__ Ent ent_join(Ent a, Ent b) {
+    if (!(a.s > 0.f)) return b;
+    if (!(b.s > 0.f)) return a;
+    const float M = fmaxf(a.m, b.m);
+    const float da = a.m - M, db = b.m - M;
+    const float fa = exp2_approx(da), fb = exp2_approx(db);
+    Ent r;
+    r.m = M;
+    r.s = a.s * fa + b.s * fb;
+    r.t = fa * fmaf(da, a.s, a.t) + fb * fmaf(db, b.s, b.t);
+    return r;
+}
+
+__device__ __forceinline__ Ent ent_warp_reduce(Ent e) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        Ent x;
+        x.m = __shfl_xor_sync(0xffffffffu, e.m, o);
+        x.s = __shfl_xor_sync(0xffffffffu, e.s, o);
+        x.t = __shfl_xor_sync(0xffffffffu, e.t, o);
+        e = ent_join(e, x);
+    }
+    return e;
+}
+
+// Warps 0-7 of the entropy kernel.  Returns the number of rows published.
+template <typename T>
+__device__ int entropy_consumer(const ScoreArgs &a, ScoreSmem &sm, const uint8_t *ring,
+                                const RowShape &rs, int warp, int lane) {
+    constexpr int VE = Vec<T>::kElems;
+    constexpr int NV = kScoreVecPerThread;
+    __shared__ float4 part[kScoreStages][kWarps];
+    const int tid = warp * 32 + lane;
+    const float scale = a.ent_scale;
+    int nrows = 0;
+    Ent acc{-INFINITY, 0.f, 0.f};
+    for (int fill = 0;; ++fill) {
+        const int s = fill % kScoreStages, n = fill / kScoreStages;
+        if (!mbar_wait_bounded(&sm.full[s], n & 1)) {
+            if (lane == 0) atomicOr(a.status, kStatusWaitTimeout);
+            return nrows;
+        }
+        const int r = sm.row[s], q = sm.tile[s];
+        if (r < 0) return nrows;
+        if (q == 0) acc = Ent{-INFINITY, 0.f, 0.f};
+        const int nvec = min(kScoreTile, rs.row_bytes - q * kScoreTile) / 16;
+        const uint4 *tv = reinterpret_cast<const uint4 *>(ring + size_t(s) * kScoreTile);
+        uint4 x[NV];
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            const int v = tid + kThreads * i;
+            x[i] = v < nvec ? tv[v] : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            if (tid + kThreads * i >= nvec) continue;
+            float y[VE];
+            Vec<T>::unpack(x[i], y);
+            float mv = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < VE; ++j) {
+                y[j] *= scale;
+                mv = fmaxf(mv, y[j]);
+            }
+            if (mv > acc.m) {
+                if (acc.s > 0.f) {  // acc.m is finite once anything was added
+                    const float dm = acc.m - mv;
+                    const float f = exp2_approx(dm);
+                    acc.t = f * fmaf(dm, acc.s, acc.t);
+                    acc.s *= f;
+                }
+                acc.m = mv;
+            }
+            // -inf logits (masked ids) have weight 0.  The vector's terms are
+            // summed pairwise before joining the running sums (shorter
+            // rounding chains).
+            float p[VE], pd[VE];
+#pragma unroll
+            for (int j = 0; j < VE; ++j) {
+                const bool live = y[j] > -INFINITY;
+                const float dy = live ? y[j] - acc.m : 0.f;
+                p[j] = live ? exp2_approx(dy) : 0.f;
+                pd[j] = p[j] * dy;
+            }
+#pragma unroll
+            for (int st = 1; st < VE; st <<= 1)
+#pragma unroll
+                for (int j = 0; j + st < VE; j += 2 * st) {
+                    p[j] += p[j + st];
+                    pd[j] += pd[j + st];
+                }
+            acc.s += p[0];
+            acc.t += pd[0];
+        }
+        if (q + 1 < rs.ntr) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.empty[s]);
+            continue;
+        }
+        // Last tile of row r: the last warp here joins the eight partials.
+        ++nrows;
+        const Ent w = ent_warp_reduce(acc);
+        int last = 0;
+        if (lane == 0) {
+            part[s][warp] = make_float4(w.m, w.s, w.t, 0.f);
+            __threadfence_block();
+            last = atomicAdd(&sm.done[s], 1) == kWarps - 1;
+        }
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (!last) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.empty[s]);
+            continue;
+        }
+        __threadfence_block();
+        Ent tot{-INFINITY, 0.f, 0.f};
+#pragma unroll
+        for (int k = 0; k < kWarps; ++k) {
+            const float4 pk = part[s][k];
+            tot = ent_join(tot, Ent{pk.x, pk.y, pk.z});
+        }
+        __syncwarp();
+        if (lane == 0) {
+            sm.done[s] = 0;
+            mbar_arrive(&sm.empty[s]);
+            // conf = exp(-H) = 2^(t / s) / s
+            a.conf[r] = exp2f(tot.t / tot.s) / tot.s;
+        }
+        __syncwarp();
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Request curves and the cap, run by the CTA that publishes the batch's last
 // row (warps 0-7).  Its 64 KB ring is free by then.  When B * pitch <=
 // kOnChip (pitch = gamma rounded up to odd, so a thread per request reads
@@ -521,9 +668,10 @@ __device__ void finish_and_budget(const ScoreArgs &a, uint8_t *ring) {
     write_offsets(B, a.L, a.draft_off, a.row_off, fs.sh);
 }
 
-// Steps a1-a3: streaming confidence head, survival curve, pre-cap lengths,
-// then (in the CTA that finishes the batch) the cap and the scans.
-template <typename T>
+// Steps a1-a3: streaming confidence head (or, with kEntropy, the entropy of
+// each draft row), survival curve, pre-cap lengths, then (in the CTA that
+// finishes the batch) the cap and the scans.
+template <typename T, bool kEntropy>
 __global__ void __launch_bounds__(kScoreThreads, 3) score_budget_kernel(const ScoreArgs a) {
     extern __shared__ __align__(1024) uint8_t ring[];
     __shared__ ScoreSmem sm;
@@ -541,14 +689,15 @@ __global__ void __launch_bounds__(kScoreThreads, 3) score_budget_kernel(const Sc
         sm.run_cap = 0;
         fence_barrier_init();
     }
-    if (tid < a.gamma) sm.tau[tid] = a.sts_tau[tid];
+    if (!kEntropy && tid < a.gamma) sm.tau[tid] = a.sts_tau[tid];
     __syncthreads();
     const RowShape rs = row_shape(a, int(sizeof(T)));
     if (warp == kWarps) {
         if (lane == 0) score_producer(a, sm, ring, rs);
         return;
     }
-    const int nrows = score_consumer<T>(a, sm, ring, rs, warp, lane);
+    const int nrows = kEntropy ? entropy_consumer<T>(a, sm, ring, rs, warp, lane)
+                               : score_consumer<T>(a, sm, ring, rs, warp, lane);
     // Publish this CTA's confidences; the CTA that adds the batch's last
     // rows finishes every request and runs the cap.
     __threadfence();
@@ -574,27 +723,34 @@ __global__ void __launch_bounds__(kThreads) fixed_budget_kernel(const FixedArgs 
 
 }  // namespace
 
-int score_blocks_per_sm(int hidden_bf16) {
+template <bool kEntropy>
+static int blocks_per_sm(int bf16) {
     const int bytes = int(kScoreSmemBytes);
-    cudaError_t e =
-        hidden_bf16 ? cudaFuncSetAttribute(score_budget_kernel<uint16_t>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)
-                    : cudaFuncSetAttribute(score_budget_kernel<float>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    auto kern = bf16 ? score_budget_kernel<uint16_t, kEntropy> : score_budget_kernel<float, kEntropy>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return -1;
     int n = 0;
-    e = hidden_bf16 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, score_budget_kernel<uint16_t>,
-                                                                    kScoreThreads, kScoreSmemBytes)
-                    : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, score_budget_kernel<float>,
-                                                                    kScoreThreads, kScoreSmemBytes);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kScoreThreads, kScoreSmemBytes);
     return e == cudaSuccess ? n : -1;
 }
 
+int score_blocks_per_sm(int hidden_bf16) { return blocks_per_sm<false>(hidden_bf16); }
+
+int entropy_blocks_per_sm(int logit_bf16) { return blocks_per_sm<true>(logit_bf16); }
+
 cudaError_t launch_score_budget(const ScoreArgs &a, int grid, cudaStream_t s) {
     if (a.hidden_bf16)
-        score_budget_kernel<uint16_t><<<grid, kScoreThreads, kScoreSmemBytes, s>>>(a);
+        score_budget_kernel<uint16_t, false><<<grid, kScoreThreads, kScoreSmemBytes, s>>>(a);
     else
-        score_budget_kernel<float><<<grid, kScoreThreads, kScoreSmemBytes, s>>>(a);
+        score_budget_kernel<float, false><<<grid, kScoreThreads, kScoreSmemBytes, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_score_entropy(const ScoreArgs &a, int grid, cudaStream_t s) {
+    if (a.hidden_bf16)
+        score_budget_kernel<uint16_t, true><<<grid, kScoreThreads, kScoreSmemBytes, s>>>(a);
+    else
+        score_budget_kernel<float, true><<<grid, kScoreThreads, kScoreSmemBytes, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -13,6 +13,11 @@
  *   dspark_verify        vocab-wide softmax of target and draft rows,
  *                        accept / resample / bonus, commit.
  *
+ * Variants: dspark_score_entropy scores drafts by the entropy of their
+ * distribution instead of the head; dspark_verify_cap_accept is the audit arm
+ * that verifies the full block and commits the scheduled window;
+ * dspark_verify_noalloc runs dspark_verify on the library's own scratch.
+ *
  * Sources (page title and section):
  *   [DS] "DFlash to DSpark in SGLang: 4.3x faster decode, and DeepSeek-V4
  *        support": "Background"; "DSpark: a sequential head and a verify
@@ -21,7 +26,8 @@
  *   [KC] "SGLang Integrates DSpark: How Confidence-Driven Speculative
  *        Decoding Cracks the High-Concurrency Failure Problem": "The Old
  *        Problem with Speculative Decoding: It Breaks Down at Scale" (the
- *        speculative-sampling rule of Chen et al. 2023).
+ *        speculative-sampling rule of Chen et al. 2023); "DSpark's Core Idea:
+ *        Only Verify the Parts You're Confident About" (entropy confidence).
  *   [SC11] Salmon et al., "Parallel Random Numbers: As Easy as 1, 2, 3"
  *        (Philox4x64-10).
  *
@@ -40,6 +46,8 @@
  *     thread-local message for the last failing call on this thread.
  *   - Layout: row-major, contiguous.  Index b is the request (0..B-1), i or
  *     k the 0-based draft position (0..gamma-1), y a token id (0..V-1).
+ *   - Values: logits and hidden states are finite (dspark_score_entropy
+ *     also takes -inf logits as masked ids).
  *   - Alignment: hidden, draft_logits and target_logits start on 16-byte
  *     boundaries and their rows are multiples of 16 bytes (d and V multiples
  *     of 8 for bf16, of 4 for fp32); otherwise DSPARK_EALIGN.
@@ -175,6 +183,23 @@ dspark_status dspark_workspace_init(void *workspace, size_t workspace_bytes,
  * draft_off, row_off.
  */
 dspark_status dspark_score_budget(const dspark_step *step, dspark_stream_t stream);
+
+/*
+ * Steps a1-a3 with the entropy-confidence variant of step a1.  [KC] "DSpark's
+ * Core Idea: Only Verify the Parts You're Confident About": the lower the
+ * entropy of the drafter's output distribution at a position, the more
+ * certain the draft and the more a verify of it is worth.  Read here as
+ *   q_{b,i} = softmax(z_q[b,i] / theta),  H_{b,i} = -sum_y q ln q  (nats),
+ *   conf_{b,i} = exp(-H_{b,i})   (in (1/V, 1]: 1 for a one-hot q, 1/V for a
+ *                                 uniform one),
+ * computed from the draft logits [B, gamma, V] (logit_dtype; each row needs
+ * a finite maximum, -inf entries are masked ids).  The survival curve, L0,
+ * the cap and the scans are those of dspark_score_budget.
+ * theta: host value, finite and > 0.  Reads draft_logits.  Writes conf,
+ * survival, L0, L, draft_off, row_off.  hidden, head_w, head_bias and
+ * sts_tau are not read.  fixed_budget >= 0 is DSPARK_EINVAL.
+ */
+dspark_status dspark_score_entropy(const dspark_step *step, float theta, dspark_stream_t stream);
 
 /*
  * Step a4, ragged packing.  [DS] "Ragged verify under full CUDA graphs": the

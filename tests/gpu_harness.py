@@ -21,20 +21,32 @@ EPS_S = 2 * TOL_S      # oracle near-tie window for S_k vs c
 EPS_CAP = 4 * TOL_S    # oracle near-tie window between the T-th and (T+1)-th gains
 EPS_U = 1e-5           # |u - min(1, p/q)| window named by the method's tolerance
 RTOL_P = 1e-3
+# Entropy confidence (conf = exp(-H)): the fp32 sums of 2^(y-m) and of
+# 2^(y-m)(y-m) carry ~5e-6 relative error at worst after pairwise vector sums,
+# which enters conf scaled by (1 + H) and S by the sum over k of (1 + H_k).
+TOL_S_ENT = 5e-5
+EPS_S_ENT = 2 * TOL_S_ENT
+EPS_CAP_ENT = 4 * TOL_S_ENT
+RTOL_CONF_ENT = 2e-4
 
 
 def to_device(inp: dict, device="cuda") -> dict:
     return {k: (v.to(device) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
 
 
-def gpu_step(inp_dev: dict, seq_lens_commit: bool = True, bufs=None, stream=None):
-    """score_budget -> compact -> (target-forward stand-in) -> verify."""
+def gpu_step(inp_dev: dict, seq_lens_commit: bool = True, bufs=None, stream=None,
+             entropy_theta=None):
+    """score_budget (or score_entropy) -> compact -> (target-forward
+    stand-in) -> verify."""
     B, g, V, d = inp_dev["B"], inp_dev["gamma"], inp_dev["V"], inp_dev["d"]
     if bufs is None:
         bufs = binding.StepBuffers(B, g, V, d, stream=stream)
     commit = inp_dev["seq_lens"].clone() if seq_lens_commit else None
     bufs.bind(inp_dev, seq_lens_commit=commit)
-    binding.dspark_score_budget(bufs.step, stream)
+    if entropy_theta is None:
+        binding.dspark_score_budget(bufs.step, stream)
+    else:
+        binding.dspark_score_entropy(bufs.step, entropy_theta, stream)
     binding.dspark_compact(bufs.step, stream)
     torch.cuda.synchronize()
     n_rows = int(bufs.row_off[B].item()) if B > 0 else 0
@@ -78,30 +90,40 @@ def check_L_valid(S, c, L0, L, T, tol=TOL_S):
         assert min(kept) >= max(dropped) - 2 * tol
 
 
-def compare_with_oracle(inp_np: dict, gpu: dict, max_flag_frac: float = 0.05) -> dict:
-    """Check every GPU output of one step against the oracle.  Returns counts."""
+def compare_with_oracle(inp_np: dict, gpu: dict, max_flag_frac: float = 0.05,
+                        entropy_theta=None) -> dict:
+    """Check every GPU output of one step against the oracle.  Returns counts.
+    With ``entropy_theta`` the confidences are the entropy variant's."""
     B, g = inp_np["draft_tokens"].shape
     stats = {"score_ties": 0, "cap_tie": 0, "verify_ties": 0}
     fixed = inp_np.get("fixed_budget", -1)
+    tol, eps_cap = (TOL_S, EPS_CAP) if entropy_theta is None else (TOL_S_ENT, EPS_CAP_ENT)
     if fixed is not None and fixed >= 0:
         L = oracle.fixed_budget(B, g, fixed)
         assert np.array_equal(gpu["L"], L)
     else:
-        conf, surv, L0, tie = oracle.score(inp_np["hidden"], inp_np["head_w"],
-                                           inp_np["head_bias"], inp_np["sts_tau"],
-                                           inp_np["cost_c"], EPS_S)
-        np.testing.assert_allclose(gpu["conf"], conf, rtol=0, atol=TOL_S)
-        np.testing.assert_allclose(gpu["survival"], surv, rtol=0, atol=TOL_S)
+        if entropy_theta is None:
+            conf, surv, L0, tie = oracle.score(inp_np["hidden"], inp_np["head_w"],
+                                               inp_np["head_bias"], inp_np["sts_tau"],
+                                               inp_np["cost_c"], EPS_S)
+        else:
+            conf, surv, L0, tie = oracle.score_entropy(inp_np["draft_logits"], entropy_theta,
+                                                       inp_np["cost_c"], EPS_S_ENT)
+        np.testing.assert_allclose(gpu["conf"], conf, rtol=0, atol=tol)
+        np.testing.assert_allclose(gpu["survival"], surv, rtol=0, atol=tol)
+        if entropy_theta is not None:
+            # relative error of exp(-H): (1 + H) times the sums' ~5e-6, H <= ln V
+            np.testing.assert_allclose(gpu["conf"], conf, rtol=RTOL_CONF_ENT, atol=1e-12)
         assert np.all(np.diff(gpu["survival"], axis=1) <= 0)
         c = float(np.float32(inp_np["cost_c"]))
         untied = tie == 0
         assert np.array_equal(gpu["L0"][untied], L0[untied]), "pre-cap lengths differ"
         stats["score_ties"] = int((~untied).sum())
-        Lcap, cap_tie = oracle.cap(surv, gpu["L0"], inp_np["cap_T"], EPS_CAP)
+        Lcap, cap_tie = oracle.cap(surv, gpu["L0"], inp_np["cap_T"], eps_cap)
         stats["cap_tie"] = cap_tie
         if cap_tie == 0:
             assert np.array_equal(gpu["L"], Lcap), "capped lengths differ"
-        check_L_valid(surv, c, gpu["L0"], gpu["L"], inp_np["cap_T"])
+        check_L_valid(surv, c, gpu["L0"], gpu["L"], inp_np["cap_T"], tol)
         L = gpu["L"]
     cpt = oracle.compact(L, inp_np["draft_tokens"], inp_np["last_tokens"], inp_np["seq_lens"])
     for k in ("draft_off", "row_off", "packed_ids", "packed_pos", "row_req", "row_k"):

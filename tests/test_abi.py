@@ -177,3 +177,22 @@ def test_cap_accept_needs_a_window(lib):
     assert lib.dspark_verify_cap_accept(ctypes.byref(s), None, None, None, None) == binding.DSPARK_EINVAL
     assert "commit_len" in binding.last_error()
     assert lib.dspark_verify_cap_accept(None, None, None, None, None) == binding.DSPARK_EINVAL
+
+
+def test_score_entropy_host_checks(lib):
+    f = lib.dspark_score_entropy
+    f.argtypes = [ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p]
+    assert f(None, 1.0, None) == binding.DSPARK_EINVAL
+    s = valid_step()
+    for theta in (0.0, -1.0, float("inf"), float("nan")):
+        assert f(ctypes.byref(s), theta, None) == binding.DSPARK_EINVAL, theta
+        assert "theta" in binding.last_error()
+    s.fixed_budget = 3
+    assert f(ctypes.byref(s), 1.0, None) == binding.DSPARK_EINVAL
+    s = valid_step()
+    s.draft_logits = None
+    assert f(ctypes.byref(s), 1.0, None) == binding.DSPARK_EINVAL
+    assert "draft_logits" in binding.last_error()
+    s = valid_step()
+    s.draft_logits = FAKE + 8
+    assert f(ctypes.byref(s), 1.0, None) == binding.DSPARK_EALIGN
