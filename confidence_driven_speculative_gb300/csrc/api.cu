@@ -231,7 +231,7 @@ dspark_status dspark_score_entropy(const dspark_step *s, float theta, dspark_str
     a.row_ctr = ws_at<int32_t>(s, lay.score_rows);
     a.status = ws_at<int32_t>(s, lay.status);
     cudaError_t e = dspark::launch_score_entropy(a, grid, reinterpret_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_fail(e, "score_budget_kernel (entropy) launch");
+    if (e != cudaSuccess) return cuda_fail(e, "score_entropy_kernel launch");
     return DSPARK_OK;
 }
 

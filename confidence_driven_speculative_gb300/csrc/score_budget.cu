@@ -328,14 +328,12 @@ __device__ int entropy_consumer(const ScoreArgs &a, ScoreSmem &sm, const uint8_t
 #pragma unroll
         for (int i = 0; i < NV; ++i) {
             if (tid + kThreads * i >= nvec) continue;
-            float y[VE];
-            Vec<T>::unpack(x[i], y);
-            float mv = -INFINITY;
+            float z[VE];
+            Vec<T>::unpack(x[i], z);
+            float zv = z[0];
 #pragma unroll
-            for (int j = 0; j < VE; ++j) {
-                y[j] *= scale;
-                mv = fmaxf(mv, y[j]);
-            }
+            for (int j = 1; j < VE; ++j) zv = fmaxf(zv, z[j]);
+            const float mv = zv * scale;
             if (mv > acc.m) {
                 if (acc.s > 0.f) {  // acc.m is finite once anything was added
                     const float dm = acc.m - mv;
@@ -345,26 +343,25 @@ __device__ int entropy_consumer(const ScoreArgs &a, ScoreSmem &sm, const uint8_t
                 }
                 acc.m = mv;
             }
-            // -inf logits (masked ids) have weight 0.  The vector's terms are
-            // summed pairwise before joining the running sums (shorter
-            // rounding chains).
-            float p[VE], pd[VE];
+            // dy = y - m, floored at -200: 2^dy is then 0 in fp32 (as it is for
+            // any dy below -150), so -inf logits (masked ids), and -inf - -inf
+            // while nothing finite has been seen (fmaxf drops the NaN), add
+            // nothing.  Per vector, the weights are summed pairwise and the
+            // weighted offsets in one fused chain, then both join the running
+            // sums (short rounding chains, one FFMA per term for t).
+            float p[VE], tv = 0.f;
 #pragma unroll
             for (int j = 0; j < VE; ++j) {
-                const bool live = y[j] > -INFINITY;
-                const float dy = live ? y[j] - acc.m : 0.f;
-                p[j] = live ? exp2_approx(dy) : 0.f;
-                pd[j] = p[j] * dy;
+                const float dy = fmaxf(fmaf(z[j], scale, -acc.m), -200.f);
+                p[j] = exp2_approx(dy);
+                tv = fmaf(p[j], dy, tv);
             }
 #pragma unroll
             for (int st = 1; st < VE; st <<= 1)
 #pragma unroll
-                for (int j = 0; j + st < VE; j += 2 * st) {
-                    p[j] += p[j + st];
-                    pd[j] += pd[j + st];
-                }
+                for (int j = 0; j + st < VE; j += 2 * st) p[j] += p[j + st];
             acc.s += p[0];
-            acc.t += pd[0];
+            acc.t += tv;
         }
         if (q + 1 < rs.ntr) {
             __syncwarp();
@@ -397,8 +394,9 @@ __device__ int entropy_consumer(const ScoreArgs &a, ScoreSmem &sm, const uint8_t
         if (lane == 0) {
             sm.done[s] = 0;
             mbar_arrive(&sm.empty[s]);
-            // conf = exp(-H) = 2^(t / s) / s
-            a.conf[r] = exp2f(tot.t / tot.s) / tot.s;
+            // conf = exp(-H) = 2^(t / s) / s, at most 1 (a one-hot row's
+            // rounding may leave t a hair above 0)
+            a.conf[r] = fminf(1.f, exp2f(tot.t / tot.s) / tot.s);
         }
         __syncwarp();
     }
@@ -672,7 +670,7 @@ __device__ void finish_and_budget(const ScoreArgs &a, uint8_t *ring) {
 // each draft row), survival curve, pre-cap lengths, then (in the CTA that
 // finishes the batch) the cap and the scans.
 template <typename T, bool kEntropy>
-__global__ void __launch_bounds__(kScoreThreads, 3) score_budget_kernel(const ScoreArgs a) {
+__device__ __forceinline__ void score_main(const ScoreArgs &a) {
     extern __shared__ __align__(1024) uint8_t ring[];
     __shared__ ScoreSmem sm;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -713,6 +711,16 @@ __global__ void __launch_bounds__(kScoreThreads, 3) score_budget_kernel(const Sc
     }
 }
 
+template <typename T>
+__global__ void __launch_bounds__(kScoreThreads, 3) score_budget_kernel(const ScoreArgs a) {
+    score_main<T, false>(a);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kScoreThreads, 3) score_entropy_kernel(const ScoreArgs a) {
+    score_main<T, true>(a);
+}
+
 __global__ void __launch_bounds__(kThreads) fixed_budget_kernel(const FixedArgs a) {
     __shared__ int sh[kWarps + 1];
     const int l = a.F < a.gamma ? a.F : a.gamma;
@@ -726,7 +734,9 @@ __global__ void __launch_bounds__(kThreads) fixed_budget_kernel(const FixedArgs 
 template <bool kEntropy>
 static int blocks_per_sm(int bf16) {
     const int bytes = int(kScoreSmemBytes);
-    auto kern = bf16 ? score_budget_kernel<uint16_t, kEntropy> : score_budget_kernel<float, kEntropy>;
+    void (*kern)(const ScoreArgs) =
+        kEntropy ? (bf16 ? score_entropy_kernel<uint16_t> : score_entropy_kernel<float>)
+                 : (bf16 ? score_budget_kernel<uint16_t> : score_budget_kernel<float>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return -1;
     int n = 0;
@@ -740,17 +750,17 @@ int entropy_blocks_per_sm(int logit_bf16) { return blocks_per_sm<true>(logit_bf1
 
 cudaError_t launch_score_budget(const ScoreArgs &a, int grid, cudaStream_t s) {
     if (a.hidden_bf16)
-        score_budget_kernel<uint16_t, false><<<grid, kScoreThreads, kScoreSmemBytes, s>>>(a);
+        score_budget_kernel<uint16_t><<<grid, kScoreThreads, kScoreSmemBytes, s>>>(a);
     else
-        score_budget_kernel<float, false><<<grid, kScoreThreads, kScoreSmemBytes, s>>>(a);
+        score_budget_kernel<float><<<grid, kScoreThreads, kScoreSmemBytes, s>>>(a);
     return cudaGetLastError();
 }
 
 cudaError_t launch_score_entropy(const ScoreArgs &a, int grid, cudaStream_t s) {
     if (a.hidden_bf16)
-        score_budget_kernel<uint16_t, true><<<grid, kScoreThreads, kScoreSmemBytes, s>>>(a);
+        score_entropy_kernel<uint16_t><<<grid, kScoreThreads, kScoreSmemBytes, s>>>(a);
     else
-        score_budget_kernel<float, true><<<grid, kScoreThreads, kScoreSmemBytes, s>>>(a);
+        score_entropy_kernel<float><<<grid, kScoreThreads, kScoreSmemBytes, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -178,6 +178,66 @@ def test_graph_replay_matches_direct_calls(cuda_lib, Tm):
         assert np.array_equal(commit.cpu().numpy(), ref["seq_lens_commit"])
 
 
+def test_one_graph_serves_every_packed_total(cuda_lib):
+    """One capture of the step -- score, compact, a fixed-shape target
+    stand-in over the batch's capacity of rows, verify -- replayed on
+    several batches whose packed totals differ.  Each replay equals direct
+    calls on that batch: the kernels take the total from device memory, so
+    no per-total graph tier is needed."""
+    from confidence_driven_speculative_gb300 import binding
+    B, V, d = 24, 20000, 128
+    sets = [to_device(W.make_inputs(W.MIXED_B256, 40 + i, B=B, V=V, d=d, cap_T=-1,
+                                    temperature=1.0)) for i in range(4)]
+    for st in sets:
+        st["seed"] = 5                      # a host scalar fixed at capture
+    keys = ("hidden", "head_w", "head_bias", "sts_tau", "draft_tokens", "draft_logits",
+            "target_dense", "last_tokens", "seq_lens")
+    live = {k: (v.clone() if k in keys else v) for k, v in sets[0].items()}
+    g1 = live["gamma"] + 1
+    bufs = binding.StepBuffers(B, live["gamma"], V, d)
+    commit = live["seq_lens"].clone()
+    bufs.bind(live, seq_lens_commit=commit)
+    tgt = torch.empty((B * g1, V), dtype=live["target_dense"].dtype, device="cuda")
+    bufs.bind_target(tgt)
+    flat = live["target_dense"].view(B * g1, V)
+
+    def step():
+        binding.dspark_score_budget(bufs.step)
+        binding.dspark_compact(bufs.step)
+        idx = (bufs.row_req.clamp(min=0) * g1 + bufs.row_k.clamp(min=0)).long()
+        torch.index_select(flat, 0, idx, out=tgt)
+        binding.dspark_verify(bufs.step)
+
+    step()                                  # warm-up outside the capture
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            step()
+    torch.cuda.current_stream().wait_stream(side)
+    totals = []
+    for st in sets:
+        ref, _ = gpu_step(st)
+        for k in keys:
+            live[k].copy_(st[k])
+        commit.copy_(st["seq_lens"])
+        for k in ("accept_len", "num_emitted", "out_tokens"):
+            getattr(bufs, k).fill_(-7)
+        g.replay()
+        torch.cuda.synchronize()
+        assert bufs.device_status() == 0
+        n = int(ref["draft_off"][B])
+        for k in ("L", "row_off", "packed_ids", "accept_len", "num_emitted", "out_tokens"):
+            assert np.array_equal(getattr(bufs, k).cpu().numpy(), ref[k]), k
+        for k in ("p_tok", "q_tok"):
+            assert np.array_equal(getattr(bufs, k).cpu().numpy()[:n], ref[k][:n]), k
+        assert np.array_equal(commit.cpu().numpy(), ref["seq_lens_commit"])
+        totals.append(int(ref["row_off"][B]))
+    assert len(set(totals)) > 1, totals
+
+
 def test_empty_batch(cuda_lib):
     from confidence_driven_speculative_gb300 import binding
     step = binding.DsparkStep()
