@@ -21,6 +21,8 @@ Function-to-source map (page titles and sections):
 * :func:`score_entropy` -- "SGLang Integrates DSpark ...", section "DSpark's
   Core Idea: Only Verify the Parts You're Confident About" (confidence from
   the entropy of the drafter's distribution); survival and budget as above.
+* :func:`fit_sts_tau` -- "DFlash to DSpark in SGLang", "DSpark: a sequential
+  head and a verify budget" (STS calibrates the survival to acceptance).
 * :func:`cap` -- same page, section "Zero-overhead scheduling and kernels"
   (verify-length top-k schedule under a batch-wide cap).
 * :func:`fixed_budget` -- same page, "The confidence scheduler and verify modes".
@@ -79,6 +81,7 @@ def _load():
             lib.orc_uniforms.restype = None
             lib.orc_score.argtypes = [i32, i32, i32, i32, P, P, P, P, f64, f64, P, P, P, P]
             lib.orc_score_entropy.argtypes = [i32, i32, i32, i32, P, f64, f64, f64, P, P, P, P]
+            lib.orc_fit_sts_tau.argtypes = [i32, i32, P, P, P, P, f64, f64, P, P, P]
             lib.orc_fixed_budget.argtypes = [i32, i32, i32, P]
             lib.orc_cap.argtypes = [i32, i32, P, P, i32, f64, P, P]
             lib.orc_compact.argtypes = [i32, i32, P, P, P, P, P, P, P, P, P, P]
@@ -86,7 +89,8 @@ def _load():
                                                f64, P, P, P, P, P]
             lib.orc_verify.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, f64, u64, f64, f64,
                                        f64, P, P, P, P, P, P, P]
-            for name in ("orc_score", "orc_score_entropy", "orc_fixed_budget", "orc_cap",
+            for name in ("orc_score", "orc_score_entropy", "orc_fit_sts_tau",
+                         "orc_fixed_budget", "orc_cap",
                          "orc_compact", "orc_verify_request", "orc_verify"):
                 getattr(lib, name).restype = ctypes.c_int
             _lib = lib
@@ -178,6 +182,30 @@ def score_entropy(draft_logits, theta: float, c: float, eps: float = 1e-5):
                                _ptr(tie))
     _check(rc, "score_entropy")
     return conf, surv, L0, tie
+
+
+def fit_sts_tau(conf, tau_used, L, accept_len, tau_min: float = 0.05,
+                tau_max: float = 20.0):
+    """Per-position STS temperatures by maximum likelihood on logged steps.
+
+    ``conf`` [N, gamma] confidences a step produced with temperatures
+    ``tau_used`` [gamma]; ``L`` [N] verify lengths; ``accept_len`` [N].
+    Returns ``(tau [gamma], nll [gamma], n_obs [gamma])``.
+    """
+    lib = _load()
+    conf = _c(conf, np.float32)
+    N, gamma = conf.shape
+    tau_used = _c(tau_used, np.float32)
+    L = _c(L, np.int32)
+    a = _c(accept_len, np.int32)
+    tau = np.zeros(gamma, np.float64)
+    nll = np.zeros(gamma, np.float64)
+    nobs = np.zeros(gamma, np.int32)
+    rc = lib.orc_fit_sts_tau(N, gamma, _ptr(conf), _ptr(tau_used), _ptr(L), _ptr(a),
+                             float(np.float32(tau_min)), float(np.float32(tau_max)), _ptr(tau),
+                             _ptr(nll), _ptr(nobs))
+    _check(rc, "fit_sts_tau")
+    return tau, nll, nobs
 
 
 def fixed_budget(B: int, gamma: int, F: int) -> np.ndarray:

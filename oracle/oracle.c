@@ -169,6 +169,90 @@ int orc_score_entropy(int B, int gamma, int V, int dtype, const void *draft_logi
 }
 
 /* ------------------------------------------------------------------------ */
+/* STS temperature fitting (offline calibration of a1).                      */
+/*   [DS] "DSpark: a sequential head and a verify budget": Sequential        */
+/*   Temperature Scaling calibrates the head's survival product to match     */
+/*   true acceptance rates.  Reading taken: the temperature tau_i of         */
+/*   position i in conf = sigmoid(x / tau_i) is the maximum-likelihood fit   */
+/*   to logged accept outcomes.  A logged request-step n (verify length L_n, */
+/*   accepted drafts a_n) observes position i when i < L_n and i <= a_n      */
+/*   (verified, every earlier draft accepted); the outcome is accept         */
+/*   (i < a_n) or reject (i = a_n).  Positions past the first rejection are  */
+/*   not observed.  The head logit is recovered from the logged confidence   */
+/*   and the temperature that produced it: x = tau_used_i * logit(conf),     */
+/*   conf clamped to [2^-126, 1 - 2^-24] (the fp32 confidences' range).       */
+/*   With beta = 1 / tau,                                                    */
+/*     NLL_i(beta) = sum_obs [ log(1 + e^{beta x}) - y beta x ],             */
+/*   convex in beta; minimised over [1/tau_max, 1/tau_min] by golden-section */
+/*   search in fp64.  No observation: tau_out = tau_used, nll = 0.           */
+/* ------------------------------------------------------------------------ */
+static double softplus(double z)
+{
+    return z > 0.0 ? z + log1p(exp(-z)) : log1p(exp(z));
+}
+
+static double sts_nll(const double *x, const int32_t *y, int n, double beta)
+{
+    double s = 0.0;
+    for (int j = 0; j < n; ++j) s += softplus(beta * x[j]) - (y[j] ? beta * x[j] : 0.0);
+    return s;
+}
+
+int orc_fit_sts_tau(int N, int gamma, const float *conf, const float *tau_used,
+                    const int32_t *L, const int32_t *accept_len, double tau_min,
+                    double tau_max, double *tau_out, double *nll_out, int32_t *n_obs)
+{
+    if (N < 0 || gamma < 1 || !(tau_min > 0.0) || !(tau_max >= tau_min)) return -1;
+    double *x = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+    int32_t *y = (int32_t *)malloc(sizeof(int32_t) * (size_t)(N > 0 ? N : 1));
+    if (!x || !y) { free(x); free(y); return -2; }
+    const double cmin = ldexp(1.0, -126), cmax = 1.0 - ldexp(1.0, -24);
+    for (int i = 0; i < gamma; ++i) {
+        int n = 0;
+        for (int b = 0; b < N; ++b) {
+            if (!(i < L[b] && i <= accept_len[b])) continue;
+            double c = (double)conf[(int64_t)b * gamma + i];
+            if (c < cmin) c = cmin;
+            if (c > cmax) c = cmax;
+            x[n] = (double)tau_used[i] * (log(c) - log1p(-c));
+            y[n] = i < accept_len[b];
+            ++n;
+        }
+        n_obs[i] = n;
+        if (n == 0) {
+            tau_out[i] = (double)tau_used[i];
+            nll_out[i] = 0.0;
+            continue;
+        }
+        const double g = (sqrt(5.0) - 1.0) / 2.0;
+        double lo = 1.0 / tau_max, hi = 1.0 / tau_min;
+        double c1 = hi - g * (hi - lo), c2 = lo + g * (hi - lo);
+        double f1 = sts_nll(x, y, n, c1), f2 = sts_nll(x, y, n, c2);
+        for (int it = 0; it < 300 && hi - lo > 1e-15 * hi; ++it) {
+            if (f1 <= f2) {
+                hi = c2; c2 = c1; f2 = f1;
+                c1 = hi - g * (hi - lo); f1 = sts_nll(x, y, n, c1);
+            } else {
+                lo = c1; c1 = c2; f1 = f2;
+                c2 = lo + g * (hi - lo); f2 = sts_nll(x, y, n, c2);
+            }
+        }
+        /* the interval's ends are candidates too (a minimum on a bound) */
+        double best = 0.5 * (lo + hi), fb = sts_nll(x, y, n, best);
+        const double ends[2] = {1.0 / tau_max, 1.0 / tau_min};
+        for (int e = 0; e < 2; ++e) {
+            const double fe = sts_nll(x, y, n, ends[e]);
+            if (fe < fb) { fb = fe; best = ends[e]; }
+        }
+        tau_out[i] = 1.0 / best;
+        nll_out[i] = fb;
+    }
+    free(x);
+    free(y);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* a1 + a2.  Confidence head with Sequential Temperature Scaling, survival,  */
 /* pre-cap verify length.                                                    */
 /*   [DS] "DSpark: a sequential head and a verify budget": the head is a     */
