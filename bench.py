@@ -24,6 +24,8 @@ gamma=16, V=129280, d=7168, bf16, c=0.35, cap T=768, sampling at Tm=1.
 * entropy_arm: the step with the entropy-confidence variant of the score
   (conf = exp(-H) of each draft row at theta = 0.3): step time, the score
   kernel's time and bandwidth over the B*gamma*V draft logits it streams.
+* sts_fit: the STS temperatures fitted to the logged confidences, lengths
+  and accept lengths of the timed step's input sets, with the fit's time.
 * latency_b1: the B=1 DeepSeek-class greedy step, microseconds per step with
   plain launches and replayed as one CUDA graph.
 * --impl reference: the CPU oracle as the reference arm (bounded samples).
@@ -70,6 +72,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-latency", action="store_true")
     ap.add_argument("--no-audit-arm", action="store_true")
     ap.add_argument("--no-entropy-arm", action="store_true")
+    ap.add_argument("--no-sts-fit", action="store_true")
     ap.add_argument("--no-fixed-arm", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -585,6 +588,31 @@ def run_ours(args, rank, world, local):
             "committed_tokens_per_step": statistics.mean(
                 float(st["bufs"].num_emitted.sum().item()) for st in ent)}
 
+    sts_fit = None
+    if not args.no_sts_fit:
+        # STS temperatures fitted to the logs of the timed step (conf, L and
+        # accept lengths of every input set), timed with events.
+        conf = torch.cat([st["bufs"].conf for st in sets])
+        Lg = torch.cat([st["bufs"].L for st in sets])
+        ag = torch.cat([st["bufs"].accept_len for st in sets])
+        tu = sets[0]["inp"]["sts_tau"]
+        tau = torch.empty(g, dtype=torch.float32, device="cuda")
+        nobs = torch.empty(g, dtype=torch.int32, device="cuda")
+        for _ in range(3):
+            binding.dspark_fit_sts_tau(conf, tu, Lg, ag, tau, n_obs=nobs)
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 20
+        f0.record()
+        for _ in range(reps):
+            binding.dspark_fit_sts_tau(conf, tu, Lg, ag, tau, n_obs=nobs)
+        f1.record()
+        torch.cuda.synchronize()
+        sts_fit = {"logged_request_steps": int(conf.shape[0]),
+                   "us_per_fit": f0.elapsed_time(f1) * 1000.0 / reps,
+                   "tau_used": [round(float(v), 4) for v in tu.tolist()],
+                   "tau_fit": [round(float(v), 4) for v in tau.tolist()],
+                   "observations": nobs.tolist()}
+
     latency = None
     if not args.no_latency:
         latency = run_latency(binding, W, flush)
@@ -632,6 +660,7 @@ def run_ours(args, rank, world, local):
         "fixed_budget_arm": fixed_arm,
         "cap_accept_arm": audit_arm,
         "entropy_arm": entropy_arm,
+        "sts_fit": sts_fit,
         "latency_b1": latency,
     }
 

@@ -69,6 +69,9 @@ def load():
             fn = getattr(lib, name)
             fn.argtypes = [SP, _P]
             fn.restype = ctypes.c_int
+        lib.dspark_fit_sts_tau.argtypes = [ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P,
+                                           ctypes.c_float, ctypes.c_float, _P, _P, _P, _P]
+        lib.dspark_fit_sts_tau.restype = ctypes.c_int
         lib.dspark_score_entropy.argtypes = [SP, ctypes.c_float, _P]
         lib.dspark_score_entropy.restype = ctypes.c_int
         lib.dspark_verify_cap_accept.argtypes = [SP, _P, _P, _P, _P]
@@ -138,6 +141,21 @@ def dspark_verify_cap_accept(step: DsparkStep, commit_len, accept_full=None, aud
                                          _ptr(audit_totals), _stream(stream))
     if check and rc != DSPARK_OK:
         raise DsparkError(rc, "dspark_verify_cap_accept")
+    return rc
+
+
+def dspark_fit_sts_tau(conf, tau_used, L, accept_len, tau_out, tau_min: float = 0.05,
+                       tau_max: float = 20.0, nll_out=None, n_obs=None, stream=None,
+                       check: bool = True) -> int:
+    """STS temperatures fitted to logged steps (device tensors: conf [N, gamma]
+    float32, tau_used [gamma] float32, L / accept_len [N] int32; writes
+    tau_out [gamma], and nll_out / n_obs when given)."""
+    N, gamma = int(conf.shape[0]), int(conf.shape[1])
+    rc = load().dspark_fit_sts_tau(N, gamma, _ptr(conf), _ptr(tau_used), _ptr(L),
+                                   _ptr(accept_len), float(tau_min), float(tau_max),
+                                   _ptr(tau_out), _ptr(nll_out), _ptr(n_obs), _stream(stream))
+    if check and rc != DSPARK_OK:
+        raise DsparkError(rc, "dspark_fit_sts_tau")
     return rc
 
 

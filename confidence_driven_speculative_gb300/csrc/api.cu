@@ -8,6 +8,7 @@
 #include <mutex>
 
 #include "dspark_internal.cuh"
+#include "sts_fit.cuh"
 
 namespace {
 
@@ -232,6 +233,34 @@ dspark_status dspark_score_entropy(const dspark_step *s, float theta, dspark_str
     a.status = ws_at<int32_t>(s, lay.status);
     cudaError_t e = dspark::launch_score_entropy(a, grid, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "score_entropy_kernel launch");
+    return DSPARK_OK;
+}
+
+dspark_status dspark_fit_sts_tau(int32_t N, int32_t gamma, const float *conf,
+                                 const float *tau_used, const int32_t *L,
+                                 const int32_t *accept_len, float tau_min, float tau_max,
+                                 float *tau_out, float *nll_out, int32_t *n_obs,
+                                 dspark_stream_t stream) {
+    const char *fn = "dspark_fit_sts_tau";
+    if (N < 0) return fail(DSPARK_EINVAL, "%s: N=%d < 0", fn, N);
+    if (gamma < 1 || gamma > DSPARK_MAX_GAMMA)
+        return fail(DSPARK_EINVAL, "%s: gamma=%d outside [1, %d]", fn, gamma, DSPARK_MAX_GAMMA);
+    if (!(tau_min > 0.0f) || !(tau_max >= tau_min) || std::isinf(tau_max))
+        return fail(DSPARK_EINVAL, "%s: need 0 < tau_min <= tau_max < inf", fn);
+    REQUIRE(tau_used);
+    REQUIRE(tau_out);
+    if (N > 0) {
+        REQUIRE(conf);
+        REQUIRE(L);
+        REQUIRE(accept_len);
+    }
+    DeviceInfo *dev;
+    dspark_status st;
+    if ((st = device_info(&dev))) return st;
+    dspark::FitArgs a{N, gamma, conf, tau_used, L, accept_len, tau_min, tau_max,
+                      tau_out, nll_out, n_obs};
+    cudaError_t e = dspark::launch_sts_fit(a, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "sts_fit_kernel launch");
     return DSPARK_OK;
 }
 

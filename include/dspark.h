@@ -16,7 +16,8 @@
  * Variants: dspark_score_entropy scores drafts by the entropy of their
  * distribution instead of the head; dspark_verify_cap_accept is the audit arm
  * that verifies the full block and commits the scheduled window;
- * dspark_verify_noalloc runs dspark_verify on the library's own scratch.
+ * dspark_verify_noalloc runs dspark_verify on the library's own scratch;
+ * dspark_fit_sts_tau calibrates sts_tau offline from logged steps.
  *
  * Sources (page title and section):
  *   [DS] "DFlash to DSpark in SGLang: 4.3x faster decode, and DeepSeek-V4
@@ -269,6 +270,35 @@ dspark_status dspark_verify(const dspark_step *step, dspark_stream_t stream);
 dspark_status dspark_verify_cap_accept(const dspark_step *step, const int32_t *commit_len,
                                        int32_t *accept_full, int32_t *audit_totals,
                                        dspark_stream_t stream);
+
+/*
+ * Offline calibration of the STS temperatures sts_tau from logged steps.
+ * [DS] "DSpark: a sequential head and a verify budget": Sequential
+ * Temperature Scaling calibrates the survival product to match true
+ * acceptance rates.  Read here as: for each position i, tau_i is the
+ * maximum-likelihood temperature of conf = sigmoid(x / tau_i) on the logged
+ * outcomes.  Logged request-step n (the conf, L and accept_len a step wrote)
+ * observes position i when i < L_n and i <= a_n; the outcome is accept
+ * (i < a_n) or reject (i = a_n).  The head logit is recovered as
+ * x = tau_used_i * logit(conf_{n,i}), conf clamped to [2^-126, 1 - 2^-24].
+ * The likelihood is convex in 1/tau; the fit bisects its derivative over
+ * [1/tau_max, 1/tau_min] (a bound when the data are separable).  Not a step
+ * of the per-step path: run it now and then over accumulated logs.
+ *
+ * All pointers are device memory.  conf [N, gamma] (the step's conf rows,
+ * stacked over logged steps), tau_used [gamma] (the sts_tau that produced
+ * them), L [N], accept_len [N]: read only.  tau_out [gamma]: the fitted
+ * temperatures (tau_used where a position has no observation).  nll_out
+ * [gamma] (the minimised negative log-likelihood, nats) and n_obs [gamma]
+ * (observations per position) may be NULL.  N may be 0.
+ * Errors: DSPARK_EINVAL for N < 0, gamma outside [1, DSPARK_MAX_GAMMA],
+ * bounds not 0 < tau_min <= tau_max < inf, or a NULL required pointer.
+ */
+dspark_status dspark_fit_sts_tau(int32_t N, int32_t gamma, const float *conf,
+                                 const float *tau_used, const int32_t *L,
+                                 const int32_t *accept_len, float tau_min, float tau_max,
+                                 float *tau_out, float *nll_out, int32_t *n_obs,
+                                 dspark_stream_t stream);
 
 /*
  * Blocking read of the workspace's device status word (0 = healthy).  A

@@ -196,3 +196,21 @@ def test_score_entropy_host_checks(lib):
     s = valid_step()
     s.draft_logits = FAKE + 8
     assert f(ctypes.byref(s), 1.0, None) == binding.DSPARK_EALIGN
+
+
+def test_fit_sts_tau_host_checks(lib):
+    f = lib.dspark_fit_sts_tau
+    P = ctypes.c_void_p
+    f.argtypes = [ctypes.c_int32, ctypes.c_int32, P, P, P, P, ctypes.c_float, ctypes.c_float,
+                  P, P, P, P]
+    ok = dict(N=4, gamma=3, conf=FAKE, tu=FAKE, L=FAKE, a=FAKE, lo=0.05, hi=20.0, out=FAKE)
+
+    def call(**kw):
+        k = dict(ok, **kw)
+        return f(k["N"], k["gamma"], k["conf"], k["tu"], k["L"], k["a"], k["lo"], k["hi"],
+                 k["out"], None, None, None)
+
+    for bad in (dict(N=-1), dict(gamma=0), dict(gamma=65), dict(lo=0.0), dict(lo=2.0, hi=1.0),
+                dict(hi=float("inf")), dict(lo=float("nan")), dict(tu=None), dict(out=None),
+                dict(conf=None), dict(L=None), dict(a=None)):
+        assert call(**bad) == binding.DSPARK_EINVAL, bad
