@@ -635,9 +635,10 @@ def run_ours(args, rank, world, local):
     return {
         "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
         "config": {"workload": w.name, "B": B, "gamma": g, "V": V, "d": d,
+                   "storage": w.dtype + " logits and hidden states; fp32 arithmetic",
                    "temperature": w.temperature, "cost_c": w.cost_c, "cap_T": w.cap_T,
                    "input_sets": P, "parallelism": "replicas" if world > 1 else "single",
                    "l2": "256 MiB flush before every timed step (outside the events); "
@@ -647,7 +648,9 @@ def run_ours(args, rank, world, local):
         "hbm_gbs_step": step_bytes / (ms_per_step * 1e-3) / 1e9,
         "hbm_frac_step": step_bytes / (ms_per_step * 1e-3) / 1e9 / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": profiled_traffic(),
+                     "frac": achieved / peak,
+                     # the committed capture is of the default workload only
+                     "traffic": profiled_traffic() if w.name == DEFAULT_WORKLOAD else None,
                      "kernel": "verify_kernel", "peak_kind": peak_kind,
                      "bytes_per_launch": statistics.mean(vb), "launch_us": ver_mean * 1000.0,
                      "early_exit_logit_bytes_per_launch": statistics.mean(
