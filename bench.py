@@ -474,6 +474,13 @@ def cpu_baseline_oracle(W, st, seconds: float):
             "sample": f"{n} full steps of input set 0 ({npi['workload']}), {dt:.1f} s"}
 
 
+def workload_config(w) -> dict:
+    """The keys naming the workload, the same in both arms' lines."""
+    return {"workload": w.name, "B": w.B, "gamma": w.gamma, "V": w.V, "d": w.d,
+            "storage": w.dtype + " logits and hidden states",
+            "temperature": w.temperature, "cost_c": w.cost_c, "cap_T": w.cap_T}
+
+
 def mean_L_of(sets, B):
     return statistics.mean(st["sum_L"] / B for st in sets)
 
@@ -637,9 +644,7 @@ def run_ours(args, rank, world, local):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": w.name, "B": B, "gamma": g, "V": V, "d": d,
-                   "storage": w.dtype + " logits and hidden states; fp32 arithmetic",
-                   "temperature": w.temperature, "cost_c": w.cost_c, "cap_T": w.cap_T,
+        "config": {**workload_config(w),
                    "input_sets": P, "parallelism": "replicas" if world > 1 else "single",
                    "l2": "256 MiB flush before every timed step (outside the events); "
                          "each step's inputs (~0.5 GB) exceed L2",
@@ -696,7 +701,7 @@ def run_reference(args, rank, world):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": full_s * 1000.0, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "B": w.B, "gamma": w.gamma, "V": w.V, "d": w.d},
+            "config": workload_config(w),
             "cpu_baseline": {"value": value, "unit": "steps/s", "cores": 1, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0,
