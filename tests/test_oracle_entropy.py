@@ -105,3 +105,13 @@ def test_survival_and_budget_definition(c):
     # a near tie is any S_k (k = 0..gamma) within eps of c
     expect = (np.abs(Sx - cf) < 1e-5).sum(axis=1)
     np.testing.assert_array_equal(tie, expect)
+
+
+def test_budget_counts_a_gain_equal_to_the_cost():
+    # a uniform row over V = 2 ids has conf = 1/2 exactly, so S_k = 2^-k is
+    # exact; L0 = max{k : S_k >= c} includes S_k == c
+    z = np.zeros((1, 3, 2), np.float32)
+    for c, L0_expect in [(0.5, 1), (0.25, 2), (0.125, 3), (0.2, 2)]:
+        conf, surv, L0, tie = oracle.score_entropy(z, 1.0, c)
+        np.testing.assert_array_equal(surv[0], [0.5, 0.25, 0.125])
+        assert L0[0] == L0_expect, c
