@@ -7,6 +7,8 @@
 #include <cstring>
 #include <mutex>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "dspark_internal.cuh"
 #include "sts_fit.cuh"
 
@@ -104,6 +106,16 @@ T *ws_at(const dspark_step *s, size_t off) {
     return reinterpret_cast<T *>(static_cast<char *>(s->workspace) + off);
 }
 
+// One NVTX range per ABI call, named after the call: profilers (nsys, ncu's
+// NVTX filters) see the step's structure.  Without a tool attached the
+// push / pop are no-ops.
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
+
 #define REQUIRE(ptr)                                                             \
     do {                                                                         \
         if (!(ptr)) return fail(DSPARK_EINVAL, "%s: " #ptr " is NULL", fn);     \
@@ -134,6 +146,7 @@ dspark_status dspark_workspace_init(void *workspace, size_t workspace_bytes, dsp
 }
 
 dspark_status dspark_score_budget(const dspark_step *s, dspark_stream_t stream) {
+    NvtxRange range("dspark_score_budget");
     const char *fn = "dspark_score_budget";
     dspark_status st = check_shape(s);
     if (st) return st;
@@ -191,6 +204,7 @@ dspark_status dspark_score_budget(const dspark_step *s, dspark_stream_t stream) 
 }
 
 dspark_status dspark_score_entropy(const dspark_step *s, float theta, dspark_stream_t stream) {
+    NvtxRange range("dspark_score_entropy");
     const char *fn = "dspark_score_entropy";
     dspark_status st = check_shape(s);
     if (st) return st;
@@ -241,6 +255,7 @@ dspark_status dspark_fit_sts_tau(int32_t N, int32_t gamma, const float *conf,
                                  const int32_t *accept_len, float tau_min, float tau_max,
                                  float *tau_out, float *nll_out, int32_t *n_obs,
                                  dspark_stream_t stream) {
+    NvtxRange range("dspark_fit_sts_tau");
     const char *fn = "dspark_fit_sts_tau";
     if (N < 0) return fail(DSPARK_EINVAL, "%s: N=%d < 0", fn, N);
     if (gamma < 1 || gamma > DSPARK_MAX_GAMMA)
@@ -265,6 +280,7 @@ dspark_status dspark_fit_sts_tau(int32_t N, int32_t gamma, const float *conf,
 }
 
 dspark_status dspark_compact(const dspark_step *s, dspark_stream_t stream) {
+    NvtxRange range("dspark_compact");
     const char *fn = "dspark_compact";
     dspark_status st = check_shape(s);
     if (st) return st;
@@ -374,12 +390,14 @@ static dspark_status verify_impl(const dspark_step *s, const int32_t *commit_len
 extern "C" {
 
 dspark_status dspark_verify(const dspark_step *s, dspark_stream_t stream) {
+    NvtxRange range("dspark_verify");
     return verify_impl(s, nullptr, nullptr, nullptr, stream, "dspark_verify");
 }
 
 dspark_status dspark_verify_cap_accept(const dspark_step *s, const int32_t *commit_len,
                                        int32_t *accept_full, int32_t *audit_totals,
                                        dspark_stream_t stream) {
+    NvtxRange range("dspark_verify_cap_accept");
     const char *fn = "dspark_verify_cap_accept";
     if (s && s->B > 0 && !commit_len) return fail(DSPARK_EINVAL, "%s: commit_len is NULL", fn);
     return verify_impl(s, commit_len, accept_full, audit_totals, stream, fn);
