@@ -379,6 +379,13 @@ static dspark_status verify_impl(const dspark_step *s, const int32_t *commit_len
     a.commit_len = commit_len;
     a.accept_full = accept_full;
     a.audit_totals = audit_totals;
+    if (accept_full) {
+        // A request with L_b = 0 has no decision rows: only its bonus draw
+        // runs, so its a_b = 0 is written here.
+        cudaError_t e = cudaMemsetAsync(accept_full, 0, sizeof(int32_t) * size_t(s->B),
+                                        reinterpret_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(accept_full)");
+    }
     // One CTA per resident slot: the cooperative launch requires it, and the
     // work is spread over the grid inside the kernel.
     const int grid = dev->sms * dev->verify_blocks[bf];

@@ -31,14 +31,23 @@ def scheduler_window(inp_np):
     return L.astype(np.int32)
 
 
-def gpu_cap_accept(inp_dev, window):
+def gpu_cap_accept(inp_dev, window, L=None):
+    """The audited block is static (every L_b = gamma) unless ``L`` gives
+    the layout explicitly (offsets by torch cumsum, packing by the library)."""
     B, g, V, d = inp_dev["B"], inp_dev["gamma"], inp_dev["V"], inp_dev["d"]
     bufs = binding.StepBuffers(B, g, V, d)
     commit = inp_dev["seq_lens"].clone()
     bufs.bind(inp_dev, seq_lens_commit=commit)
-    bufs.step.cap_T = binding.DSPARK_NO_CAP
-    bufs.step.fixed_budget = g                      # the audited block: static
-    binding.dspark_score_budget(bufs.step)
+    if L is None:
+        bufs.step.cap_T = binding.DSPARK_NO_CAP
+        bufs.step.fixed_budget = g                  # the audited block: static
+        binding.dspark_score_budget(bufs.step)
+    else:
+        Lt = torch.as_tensor(np.asarray(L, np.int32)).cuda()
+        z = torch.zeros(1, dtype=torch.int32, device="cuda")
+        bufs.L.copy_(Lt)
+        bufs.draft_off.copy_(torch.cat([z, torch.cumsum(Lt, 0).to(torch.int32)]))
+        bufs.row_off.copy_(torch.cat([z, torch.cumsum(Lt + 1, 0).to(torch.int32)]))
     binding.dspark_compact(bufs.step)
     torch.cuda.synchronize()
     n_rows = int(bufs.row_off[B].item())
@@ -59,12 +68,12 @@ def gpu_cap_accept(inp_dev, window):
     return out, bufs
 
 
-def run_and_compare(inp_cpu, window, max_flag_frac=0.05):
+def run_and_compare(inp_cpu, window, max_flag_frac=0.05, L=None):
     inp = W.to_numpy(inp_cpu)
     B, g = inp["draft_tokens"].shape
-    gpu, bufs = gpu_cap_accept(to_device(inp_cpu), window)
-    assert np.all(gpu["L"] == g)
-    L = np.full(B, g, np.int32)
+    gpu, bufs = gpu_cap_accept(to_device(inp_cpu), window, L)
+    L = np.full(B, g, np.int32) if L is None else np.asarray(L, np.int32)
+    assert np.array_equal(gpu["L"], L)
     ora = oracle.verify_cap_accept(inp["draft_tokens"], inp["draft_logits"], inp["target_dense"],
                                    L, window, inp["temperature"], inp["seed"], EPS_U,
                                    inp["seq_lens"])
@@ -81,7 +90,7 @@ def run_and_compare(inp_cpu, window, max_flag_frac=0.05):
     if not flagged.any():
         assert gpu["audit_totals"].tolist() == ora["audit_totals"].tolist()
     if inp["temperature"] > 0:
-        n = B * g
+        n = int(L.sum())
         np.testing.assert_allclose(gpu["p_tok"][:n].astype(np.float64), ora["p_tok"],
                                    rtol=RTOL_P, atol=1e-30)
         np.testing.assert_allclose(gpu["q_tok"][:n].astype(np.float64), ora["q_tok"],
@@ -162,3 +171,19 @@ def test_mixed_b256_scheduler_window(cuda_lib):
     gpu, ora, _ = run_and_compare(inp, scheduler_window(W.to_numpy(inp)))
     tot = gpu["audit_totals"]
     assert 0 < tot[1] <= tot[0]
+
+
+@pytest.mark.parametrize("Tm", [0.0, 1.0])
+def test_layout_with_empty_requests(cuda_lib, Tm):
+    """A verified block with L_b = 0 for some requests (only their bonus row
+    is read): a_b = 0 there, and every other output as the oracle's."""
+    B, g, V, d = 24, 6, 8200, 40
+    inp = W.make_inputs(W.MIXED_B256, 21, B=B, gamma=g, V=V, d=d, temperature=Tm,
+                        cap_T=-1, cost_c=0.0)
+    rng = np.random.default_rng(77)
+    L = rng.integers(0, g + 1, B).astype(np.int32)
+    L[:4] = 0
+    window = rng.integers(-1, g + 2, B).astype(np.int32)
+    gpu, ora, _ = run_and_compare(inp, window, L=L)
+    assert np.all(gpu["accept_full"][:4] == 0)
+    assert np.all(gpu["accept_full"] <= L)
