@@ -261,7 +261,9 @@ dspark_status dspark_verify(const dspark_step *step, dspark_stream_t stream);
  * committed result; p_tok and q_tok cover every draft k < L_b of the block.
  *
  * accept_full:  device int32 [B] or NULL; receives a_b, the acceptance of
- *               the full verify (the ceiling).
+ *               the full verify (the ceiling).  The call zeroes it on
+ *               `stream` before the launch (cudaMemsetAsync), which gives
+ *               a_b = 0 to requests with L_b = 0.
  * audit_totals: device int32 [2] or NULL; receives (sum of a_b, sum of
  *               accept_len) over the batch.  Their ratio is the utilization
  *               against the ceiling.
