@@ -25,6 +25,11 @@
 // S_{b,k} (non-negative floats order like their bit patterns), ties resolved
 // by request then position, followed by the exclusive scans.  Counters reset
 // themselves, so no CTA waits on another and the kernel is safe to replay.
+//
+// score_entropy_kernel is the same kernel with the draft logit rows as its
+// rows and an entropy consumer in place of the dot product: the confidence of
+// a draft is exp(-H) of its distribution ("SGLang Integrates DSpark ...",
+// "DSpark's Core Idea: Only Verify the Parts You're Confident About").
 #include "dspark_internal.cuh"
 
 namespace dspark {
