@@ -47,6 +47,12 @@
 //    two-float (TwoSum) arithmetic, as exact as fp64 on the fast fp32 pipe.
 //  * Every wait is bounded (2 s) and sets a status bit when it gives up;
 //    counters reset themselves at the end of the launch.
+//  * The cap-accept audit arm ("DFlash to DSpark in SGLang", "The
+//    confidence scheduler and verify modes") is the same launch with a
+//    committed window W_b: every draft of the block is tested, the commit is
+//    min(a_b, W_b), and a window that ends inside the accepted run draws
+//    from p at row W_b through the residual-tile path (what compact's bonus
+//    draw would be).
 #include <climits>
 
 #include "dspark_internal.cuh"
