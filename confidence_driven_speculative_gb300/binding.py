@@ -137,6 +137,10 @@ def dspark_verify_cap_accept(step: DsparkStep, commit_len, accept_full=None, aud
     """The cap-accept audit arm: verify the step's full block, commit the
     window ``commit_len`` (device int32 [B]).  ``accept_full`` (device int32
     [B]) and ``audit_totals`` (device int32 [2]) are optional outputs."""
+    B = int(step.B)
+    _device_array(commit_len, "commit_len", "int32", B)
+    _device_array(accept_full, "accept_full", "int32", B, optional=True)
+    _device_array(audit_totals, "audit_totals", "int32", 2, optional=True)
     rc = load().dspark_verify_cap_accept(ctypes.byref(step), _ptr(commit_len), _ptr(accept_full),
                                          _ptr(audit_totals), _stream(stream))
     if check and rc != DSPARK_OK:
@@ -150,7 +154,17 @@ def dspark_fit_sts_tau(conf, tau_used, L, accept_len, tau_out, tau_min: float = 
     """STS temperatures fitted to logged steps (device tensors: conf [N, gamma]
     float32, tau_used [gamma] float32, L / accept_len [N] int32; writes
     tau_out [gamma], and nll_out / n_obs when given)."""
+    if conf is None or conf.dim() != 2:
+        raise ValueError("conf must be a [N, gamma] tensor")
     N, gamma = int(conf.shape[0]), int(conf.shape[1])
+    if N > 0:
+        _device_array(conf, "conf", "float32")
+        _device_array(L, "L", "int32", N)
+        _device_array(accept_len, "accept_len", "int32", N)
+    _device_array(tau_used, "tau_used", "float32", gamma)
+    _device_array(tau_out, "tau_out", "float32", gamma)
+    _device_array(nll_out, "nll_out", "float32", gamma, optional=True)
+    _device_array(n_obs, "n_obs", "int32", gamma, optional=True)
     rc = load().dspark_fit_sts_tau(N, gamma, _ptr(conf), _ptr(tau_used), _ptr(L),
                                    _ptr(accept_len), float(tau_min), float(tau_max),
                                    _ptr(tau_out), _ptr(nll_out), _ptr(n_obs), _stream(stream))
@@ -212,6 +226,28 @@ def _dtype_code(t) -> int:
 
 def _ptr(t) -> Optional[int]:
     return None if t is None else t.data_ptr()
+
+
+def _device_array(t, name: str, dtype: str, numel: Optional[int] = None, optional=False):
+    """Check that ``t`` is a contiguous CUDA tensor of ``dtype`` ("int32" or
+    "float32") with ``numel`` elements (when given); raise ValueError
+    otherwise, before anything reaches the library."""
+    if t is None:
+        if optional:
+            return
+        raise ValueError(f"{name} is required")
+    import torch
+    want = {"int32": torch.int32, "float32": torch.float32}[dtype]
+    if not isinstance(t, torch.Tensor):
+        raise ValueError(f"{name} must be a torch tensor")
+    if t.dtype != want:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be CUDA device memory")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if numel is not None and t.numel() != numel:
+        raise ValueError(f"{name} must have {numel} elements, got {t.numel()}")
 
 
 class StepBuffers:

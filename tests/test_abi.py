@@ -214,3 +214,27 @@ def test_fit_sts_tau_host_checks(lib):
                 dict(hi=float("inf")), dict(lo=float("nan")), dict(tu=None), dict(out=None),
                 dict(conf=None), dict(L=None), dict(a=None)):
         assert call(**bad) == binding.DSPARK_EINVAL, bad
+
+
+def test_binding_checks_variant_arrays_before_the_call():
+    """The binding refuses host, mistyped or missized arrays for the variant
+    calls before anything reaches the library (no GPU needed)."""
+    import torch
+    s = binding.DsparkStep()
+    s.B = 4
+    with pytest.raises(ValueError, match="commit_len must be int32"):
+        binding.dspark_verify_cap_accept(s, torch.zeros(4, dtype=torch.int64))
+    with pytest.raises(ValueError, match="CUDA device memory"):
+        binding.dspark_verify_cap_accept(s, torch.zeros(4, dtype=torch.int32))
+    with pytest.raises(ValueError, match="required"):
+        binding.dspark_verify_cap_accept(s, None)
+    conf = torch.zeros((3, 5), dtype=torch.float32)
+    with pytest.raises(ValueError, match="CUDA device memory"):
+        binding.dspark_fit_sts_tau(conf, torch.ones(5), torch.zeros(3, dtype=torch.int32),
+                                   torch.zeros(3, dtype=torch.int32), torch.zeros(5))
+    empty = torch.zeros((0, 5), dtype=torch.float32)   # N = 0: only tau arrays matter
+    with pytest.raises(ValueError, match="tau_used must be float32"):
+        binding.dspark_fit_sts_tau(empty, torch.ones(5, dtype=torch.float64), None, None,
+                                   torch.zeros(5))
+    with pytest.raises(ValueError, match="conf must be a"):
+        binding.dspark_fit_sts_tau(torch.zeros(5), torch.ones(5), None, None, torch.zeros(5))
