@@ -119,12 +119,20 @@ def compare_with_oracle(inp_np: dict, gpu: dict, max_flag_frac: float = 0.05,
         untied = tie == 0
         assert np.array_equal(gpu["L0"][untied], L0[untied]), "pre-cap lengths differ"
         stats["score_ties"] = int((~untied).sum())
-        Lcap, cap_tie = oracle.cap(surv, gpu["L0"], inp_np["cap_T"], eps_cap)
+        # The GPU's lengths are a valid outcome of the budget and cap (this
+        # covers the flagged near ties too).
+        check_L_valid(surv, c, gpu["L0"], gpu["L"], inp_np["cap_T"], tol)
+        # The oracle goes on from its own L0.  Only where it flagged a near
+        # tie, where either choice is correct, does it take the GPU's (just
+        # checked valid), so that the later stages compare like with like.
+        L0_used = np.where(untied, L0, gpu["L0"]).astype(np.int32)
+        Lcap, cap_tie = oracle.cap(surv, L0_used, inp_np["cap_T"], eps_cap)
         stats["cap_tie"] = cap_tie
         if cap_tie == 0:
             assert np.array_equal(gpu["L"], Lcap), "capped lengths differ"
-        check_L_valid(surv, c, gpu["L0"], gpu["L"], inp_np["cap_T"], tol)
-        L = gpu["L"]
+            L = Lcap
+        else:
+            L = gpu["L"].astype(np.int32)  # a flagged cap boundary: the GPU's valid choice
     cpt = oracle.compact(L, inp_np["draft_tokens"], inp_np["last_tokens"], inp_np["seq_lens"])
     for k in ("draft_off", "row_off", "packed_ids", "packed_pos", "row_req", "row_k"):
         assert np.array_equal(gpu[k], cpt[k]), k
