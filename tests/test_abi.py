@@ -238,3 +238,39 @@ def test_binding_checks_variant_arrays_before_the_call():
                                    torch.zeros(5))
     with pytest.raises(ValueError, match="conf must be a"):
         binding.dspark_fit_sts_tau(torch.zeros(5), torch.ones(5), None, None, torch.zeros(5))
+
+
+def test_a_c_program_builds_against_the_header_and_library(lib):
+    """A plain C11 program (warnings as errors) includes dspark.h, links
+    libdspark.so and calls the host-side entry points: the ABI needs no C++
+    and no Python."""
+    src = r'''
+#include <stdio.h>
+#include "dspark.h"
+int main(void) {
+    dspark_step s = {0};
+    printf("%s\n", dspark_version());
+    printf("%zu\n", dspark_workspace_size(256, 16, 129280, 7168));
+    printf("%d\n", (int)dspark_verify(NULL, NULL));
+    printf("%d\n", (int)dspark_score_entropy(NULL, 1.0f, NULL));
+    printf("%d\n", (int)dspark_verify_cap_accept(&s, NULL, NULL, NULL, NULL));
+    printf("%d\n", (int)dspark_fit_sts_tau(-1, 4, NULL, NULL, NULL, NULL, 0.1f, 10.0f,
+                                           NULL, NULL, NULL, NULL));
+    printf("%s\n", dspark_last_error());
+    return 0;
+}
+'''
+    libdir = os.path.dirname(binding.lib_path())
+    with tempfile.TemporaryDirectory() as td:
+        c = os.path.join(td, "use.c")
+        exe = os.path.join(td, "use")
+        open(c, "w").write(src)
+        subprocess.run(["gcc", "-std=c11", "-Wall", "-Wextra", "-Werror", "-I",
+                        os.path.join(ROOT, "include"), c, "-o", exe, "-L", libdir, "-ldspark",
+                        f"-Wl,-rpath,{libdir}"], check=True)
+        out = subprocess.run([exe], capture_output=True, text=True, check=True).stdout.split("\n")
+    assert out[0] == binding.version()
+    assert int(out[1]) == binding.dspark_workspace_size(256, 16, 129280, 7168)
+    # B = 0 in a zeroed struct: check_shape rejects gamma = 0 first
+    assert [int(x) for x in out[2:6]] == [binding.DSPARK_EINVAL] * 4
+    assert "N=-1" in out[6]
