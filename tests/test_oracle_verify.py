@@ -299,3 +299,100 @@ def test_uniforms_are_wired_to_philox_words():
         assert out["accept_len"][b] == (1 if u < 0.5 else 0), b
         if u >= 0.5 and abs(u2 * 0.4 - 0.3) > 1e-6:
             assert out["out_tokens"][b, 0] == (0 if u2 * 0.4 < 0.3 else 2), b
+
+
+def _block_rows(V, spec, rest_mass):
+    """Probabilities over V ids: `spec` {id: p}, the rest of the mass spread
+    evenly over the other ids (rest_mass may be 0: those ids then get a
+    logit far enough below the others that their weight is exactly 0 in
+    fp64)."""
+    p = np.zeros(V)
+    for i, v in spec.items():
+        p[i] = v
+    others = np.ones(V, bool)
+    others[list(spec)] = False
+    if rest_mass > 0:
+        p[others] = rest_mass / others.sum()
+        return np.log(p).astype(np.float32)
+    z = np.full(V, -2000.0)
+    z[~others] = np.log(p[~others])
+    return z.astype(np.float32)
+
+
+def test_block_uniform_is_wired_to_philox_word_1():
+    """Rows of two 4096-id blocks.  Residual path: draft id 1 has
+    p/q = 1/2, so slot b rejects iff u_b >= 1/2; the residual's only positive
+    ids are 5 (mass 0.30, block 0) and 4103 (mass 0.10, block 1), so after a
+    rejection the token is 5 iff u'_b * 0.4 < 0.3, u' being word 1 of
+    Philox((b, 0, 0, 0), (seed, 0)).  Bonus path (draft = target, always
+    accepted): the bonus row has block masses 0.65 / 0.35, so the bonus token
+    lies in block 0 iff u' of position 1 is below 0.65.  Swapping words 1 and
+    2 fails both."""
+    from tests.test_oracle_philox import numpy_block
+    V, seed, n = 8192, 91, 300
+    zp = _block_rows(V, {1: 0.1, 5: 0.35, 4103: 0.15}, 0.4)
+    zq = _block_rows(V, {1: 0.2, 5: 0.05, 4103: 0.05}, 0.7)
+    out = _replicate(zp, zq, zp, np.ones(n, np.int32), n, seed)
+    checked = 0
+    for b in range(n):
+        w = numpy_block((b, 0, 0, 0), (seed, 0))
+        u = int(w[0] >> np.uint64(40)) / 2.0**24
+        u1 = int(w[1] >> np.uint64(40)) / 2.0**24
+        if abs(u - 0.5) < 1e-4:
+            continue
+        assert out["accept_len"][b] == (1 if u < 0.5 else 0), b
+        if u >= 0.5 and abs(u1 - 0.75) > 1e-4:
+            assert out["out_tokens"][b, 0] == (5 if u1 < 0.75 else 4103), b
+            checked += 1
+    assert checked > 100
+    z1 = _block_rows(V, {10: 0.6, 4116: 0.3}, 0.1)
+    out = _replicate(zp, zp, z1, np.ones(n, np.int32), n, seed)
+    assert np.all(out["accept_len"] == 1)
+    for b in range(n):
+        w = numpy_block((b, 1, 0, 0), (seed, 0))
+        u1 = int(w[1] >> np.uint64(40)) / 2.0**24
+        if abs(u1 - 0.65) > 1e-4:
+            assert (out["out_tokens"][b, 1] < 4096) == (u1 < 0.65), b
+
+
+def test_bonus_draw_across_three_blocks_follows_the_target():
+    """chi-square of L = 0 bonus draws from a row whose mass sits on two ids
+    in each of three 4096-id blocks (the other ids weigh exactly 0): both
+    levels of the draw -- the block by u', the id inside it by u'' -- must
+    reproduce p."""
+    V, n, seed = 3 * 4096, 20_000, 17
+    spec = {3: 0.10, 1000: 0.15, 4100: 0.20, 8000: 0.05, 8200: 0.25, 12000: 0.25}
+    z = _block_rows(V, spec, 0.0)
+    L = np.zeros(n, np.int32)
+    tgt = np.broadcast_to(z, (n, V)).astype(np.float32)
+    row_off = np.arange(n + 1, dtype=np.int32)
+    draft_off = np.zeros(n + 1, np.int32)
+    out = oracle.verify(np.zeros((n, 1), np.int32), np.zeros((n, 1, V), np.float32), tgt, L,
+                        row_off, draft_off, 1.0, seed)
+    toks = out["out_tokens"][:, 0]
+    ids = np.array(sorted(spec))
+    assert np.all(np.isin(toks, ids))
+    counts = np.array([np.sum(toks == i) for i in ids])
+    P = special.softmax(z.astype(np.float64))[ids]
+    assert stats.chisquare(counts, P / P.sum() * n).pvalue > ALPHA
+
+
+def test_residual_draw_across_two_blocks_follows_the_residual():
+    """chi-square of residual draws whose positive part max(0, p - q) sits on
+    two ids in each of two blocks (4096 ids and a ragged 8): the resampled
+    ids follow norm(max(0, p - q)) across the block boundary."""
+    V, n, seed = 4096 + 8, 20_000, 23
+    zp = _block_rows(V, {50: 0.05, 3: 0.25, 700: 0.20, 4097: 0.30, 4100: 0.15}, 0.05)
+    zq = _block_rows(V, {50: 0.60, 3: 0.05, 700: 0.05, 4097: 0.05, 4100: 0.05}, 0.20)
+    out = _replicate(zp, zq, zp, np.full(n, 50, np.int32), n, seed)
+    rej = out["accept_len"] == 0
+    assert rej.sum() > 0.85 * n
+    toks = out["out_tokens"][rej, 0]
+    P = special.softmax(zp.astype(np.float64))
+    Q = special.softmax(zq.astype(np.float64))
+    resid = np.maximum(0.0, P - Q)
+    ids = np.nonzero(resid > 0)[0]
+    assert set(ids.tolist()) == {3, 700, 4097, 4100}
+    assert np.all(np.isin(toks, ids))
+    counts = np.array([np.sum(toks == i) for i in ids])
+    assert stats.chisquare(counts, resid[ids] / resid[ids].sum() * counts.sum()).pvalue > ALPHA
