@@ -84,6 +84,10 @@ def load():
         lib.dspark_workspace_init.restype = ctypes.c_int
         lib.dspark_read_device_status.argtypes = [_P, ctypes.POINTER(ctypes.c_int32), _P]
         lib.dspark_read_device_status.restype = ctypes.c_int
+        lib.dspark_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
+        lib.dspark_set_wait_timeout_ns.restype = ctypes.c_int
+        lib.dspark_wait_timeout_ns.argtypes = []
+        lib.dspark_wait_timeout_ns.restype = ctypes.c_uint64
         lib.dspark_last_error.argtypes = []
         lib.dspark_last_error.restype = ctypes.c_char_p
         lib.dspark_version.argtypes = []
@@ -205,6 +209,15 @@ def dspark_read_device_status(ptr: int, stream=None) -> int:
     if rc != DSPARK_OK:
         raise DsparkError(rc, "dspark_read_device_status")
     return int(out.value)
+
+
+def dspark_set_wait_timeout_ns(ns: int) -> int:
+    """Bound of every device wait in later launches (0: the 2 s default)."""
+    return int(load().dspark_set_wait_timeout_ns(int(ns)))
+
+
+def dspark_wait_timeout_ns() -> int:
+    return int(load().dspark_wait_timeout_ns())
 
 
 def last_error() -> str:

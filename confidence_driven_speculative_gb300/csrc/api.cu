@@ -1,6 +1,7 @@
 // api.cu -- the C ABI of libdspark.so (declared in include/dspark.h):
 // argument validation, workspace carving, per-device launch configuration.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -15,6 +16,9 @@
 namespace {
 
 thread_local char g_err[512] = "";
+
+// Bound of every device wait, read at each launch (dspark_set_wait_timeout_ns).
+std::atomic<uint64_t> g_wait_ns{dspark::kWaitTimeoutNs};
 
 dspark_status fail(dspark_status s, const char *fmt, ...) {
     va_list ap;
@@ -198,6 +202,7 @@ dspark_status dspark_score_budget(const dspark_step *s, dspark_stream_t stream) 
     a.done_cnt = ws_at<int32_t>(s, lay.score_done);
     a.row_ctr = ws_at<int32_t>(s, lay.score_rows);
     a.status = ws_at<int32_t>(s, lay.status);
+    a.wait_ns = g_wait_ns.load();
     cudaError_t e = dspark::launch_score_budget(a, grid, cs);
     if (e != cudaSuccess) return cuda_fail(e, "score_budget_kernel launch");
     return DSPARK_OK;
@@ -245,6 +250,7 @@ dspark_status dspark_score_entropy(const dspark_step *s, float theta, dspark_str
     a.done_cnt = ws_at<int32_t>(s, lay.score_done);
     a.row_ctr = ws_at<int32_t>(s, lay.score_rows);
     a.status = ws_at<int32_t>(s, lay.status);
+    a.wait_ns = g_wait_ns.load();
     cudaError_t e = dspark::launch_score_entropy(a, grid, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "score_entropy_kernel launch");
     return DSPARK_OK;
@@ -334,6 +340,12 @@ static dspark_status verify_impl(const dspark_step *s, const int32_t *commit_len
         return fail(DSPARK_EALIGN, "%s: a logit row (V=%d) is not a multiple of 16 bytes", fn, s->V);
     if (size_t(s->V) * ls > size_t(INT32_MAX))
         return fail(DSPARK_EINVAL, "%s: a logit row is too large", fn);
+    // The stream work is counted in 32-bit chunk indices: at most 2^30 tiles
+    // (16 TB of logits, beyond any device's memory).
+    if (size_t(s->B) * size_t(s->gamma + 1) *
+            ((size_t(s->V) * ls + dspark::kChunkBytes - 1) / dspark::kChunkBytes) > (size_t(1) << 30))
+        return fail(DSPARK_EINVAL, "%s: B=%d gamma=%d V=%d is too large a batch", fn, s->B,
+                    s->gamma, s->V);
     dspark::WorkspaceLayout lay;
     if ((st = check_workspace(s, &lay))) return st;
     DeviceInfo *dev;
@@ -348,8 +360,6 @@ static dspark_status verify_impl(const dspark_step *s, const int32_t *commit_len
     a.chunk_elems = int(dspark::kChunkBytes / ls);
     a.nblk = lay.nblk;
     a.grp_stride = lay.nc;
-    a.qcap = lay.qcap;
-    a.qbcap = 2 * s->B;
     a.greedy = greedy;
     a.scale = greedy ? 0.f : float(1.4426950408889634 / double(s->temperature));
     a.seed = s->seed;
@@ -365,20 +375,22 @@ static dspark_status verify_impl(const dspark_step *s, const int32_t *commit_len
     a.zrec = ws_at<float2>(s, lay.zrec);
     a.gath = ws_at<float2>(s, lay.gath);
     a.dstate = ws_at<dspark::DecideState>(s, lay.dstate);
+    a.q_ctr = ws_at<int32_t>(s, lay.q_ctr);
+    a.req_cnt = ws_at<int32_t>(s, lay.verify_cnt);
+    a.bon_cnt = ws_at<int32_t>(s, lay.bon_cnt);
+    a.r1_cnt = ws_at<int32_t>(s, lay.r1_cnt);
+    a.join = ws_at<int32_t>(s, lay.join);
+    a.act = ws_at<int32_t>(s, lay.act);
+    a.rejflag = ws_at<int32_t>(s, lay.rejflag);
+    a.rej_list = ws_at<int32_t>(s, lay.rej_list);
     a.q_job = ws_at<int2>(s, lay.q_job);
     a.q_ready = ws_at<int32_t>(s, lay.q_ready);
-    a.q_ctr = ws_at<int32_t>(s, lay.q_ctr);
-    a.qb_job = ws_at<int32_t>(s, lay.qb_job);
-    a.qb_ready = ws_at<int32_t>(s, lay.qb_ready);
-    a.req_cnt = ws_at<int32_t>(s, lay.verify_cnt);
-    a.r1_cnt = ws_at<int32_t>(s, lay.r1_cnt);
-    a.bon_cnt = ws_at<int32_t>(s, lay.bon_cnt);
-    a.join = ws_at<int32_t>(s, lay.join);
-    a.rejflag = ws_at<int32_t>(s, lay.rejflag);
+    a.qcap = lay.qcap;
     a.status = ws_at<int32_t>(s, lay.status);
     a.commit_len = commit_len;
     a.accept_full = accept_full;
     a.audit_totals = audit_totals;
+    a.wait_ns = g_wait_ns.load();
     if (accept_full) {
         // A request with L_b = 0 has no decision rows: only its bonus draw
         // runs, so its a_b = 0 is written here.
@@ -386,8 +398,8 @@ static dspark_status verify_impl(const dspark_step *s, const int32_t *commit_len
                                         reinterpret_cast<cudaStream_t>(stream));
         if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(accept_full)");
     }
-    // One CTA per resident slot: the cooperative launch requires it, and the
-    // work is spread over the grid inside the kernel.
+    // One CTA per resident slot; the work is spread over the grid inside the
+    // kernel.
     const int grid = dev->sms * dev->verify_blocks[bf];
     cudaError_t e = dspark::launch_verify(a, bf, grid, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "verify_kernel launch");
@@ -420,6 +432,13 @@ dspark_status dspark_read_device_status(const void *workspace, int32_t *status_o
     if (e != cudaSuccess) return cuda_fail(e, "reading the device status");
     return DSPARK_OK;
 }
+
+dspark_status dspark_set_wait_timeout_ns(uint64_t ns) {
+    g_wait_ns.store(ns == 0 ? dspark::kWaitTimeoutNs : ns);
+    return DSPARK_OK;
+}
+
+uint64_t dspark_wait_timeout_ns(void) { return g_wait_ns.load(); }
 
 const char *dspark_last_error(void) { return g_err; }
 

@@ -17,13 +17,15 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kConsumerWarps = 8;        // verify: consumer warps per CTA
 constexpr int kVerifyThreads = (kConsumerWarps + 2) * 32;  // + producer and decider warps
 constexpr int kChunkBytes = 16384;       // one vocab tile of one row (verify)
-constexpr int kStages = 3;               // verify smem ring: kStages x (target + draft) tiles
 constexpr int kSampleBlock = 4096;       // token ids per block of the two-level draw
-constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // bounded waits: 2 s
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // bounded waits: 2 s (default)
+constexpr uint64_t kDrainTimeoutNs = 100000000ull;  // a CTA that gave up waits this long at
+                                                    // most for its own copies in flight
 
 // Device status bits (workspace word 0).
-constexpr int32_t kStatusWaitTimeout = 1;   // an mbarrier wait gave up
-constexpr int32_t kStatusQueueTimeout = 2;  // the verify job queue stalled
+constexpr int32_t kStatusWaitTimeout = 1;   // a wait on the shared-memory copy ring gave up
+constexpr int32_t kStatusQueueTimeout = 2;  // a wait on other warps or CTAs (events, grid
+                                            // barrier) gave up
 
 // Per-request draw state written by the verify kernel's decide step.
 struct DecideState {
@@ -40,22 +42,22 @@ struct WorkspaceLayout {
     size_t status;        // int32
     size_t score_done;    // int32 [1]   hidden rows published
     size_t score_rows;    // int32 [1]   hidden rows claimed
-    size_t verify_cnt;    // int32 [B]   per-request stream tiles done
+    size_t verify_cnt;    // int32 [B]   per-request decision chunks done
+    size_t bon_cnt;       // int32 [B]   per-request bonus-row chunks done
     size_t r1_cnt;        // int32 [B]   per-request residual tiles done
-    size_t bon_cnt;       // int32 [B]   per-request bonus-row tiles done
     size_t join;          // int32 [B]   drafts all accepted + bonus row streamed
+    size_t act;           // int32 [B]   per-request draw still to make (verify)
     size_t rejflag;       // int32 [B]   launch epoch of a found rejection
-    size_t q_ctr;         // int32 [16]  queue heads / tails, finished, exited, epoch, chunk,
-                          //             audit totals
+    size_t rej_list;      // int32 [B]   requests with a residual draw
+    size_t q_ctr;         // int32 [16]  chunk counter, grid barrier, epoch, exited CTAs,
+                          //             rejections, audit totals
     size_t rowrec;        // float4 [B*(gamma+1) * nc]      row partials per (row, chunk)
-    size_t blkrec;        // float2 [B * nblk * 8]          bonus-row block partials per warp
-    size_t zrec;          // float2 [B * nblk * 8]          residual / p block masses per warp
+    size_t blkrec;        // float2 [B * nblk * 8]          bonus-row (max, sum) per slot
+    size_t zrec;          // float2 [B * nblk * 8]          residual / p masses per slot
     size_t gath;          // float2 [B * (gamma+1)]         z_p[d], z_q[d]
     size_t dstate;        // DecideState [B]
     size_t q_job;         // int2 [qcap]    residual-tile jobs (request, tile)
-    size_t q_ready;       // int32 [qcap]
-    size_t qb_job;        // int32 [2B]     decider jobs (decide / finish residual)
-    size_t qb_ready;      // int32 [2B]
+    size_t q_ready;       // int32 [qcap]   launch epoch once the job is published
     size_t total;
     int nblk;             // sampling blocks per row
     int nc;               // 16 KB tiles per row (fp32, the larger count)
@@ -77,10 +79,12 @@ inline WorkspaceLayout workspace_layout(int B, int gamma, int V) {
     w.score_done = off;  off = align256(off + sizeof(int32_t));
     w.score_rows = off;  off = align256(off + sizeof(int32_t));
     w.verify_cnt = off;  off = align256(off + sizeof(int32_t) * size_t(B));
-    w.r1_cnt = off;      off = align256(off + sizeof(int32_t) * size_t(B));
     w.bon_cnt = off;     off = align256(off + sizeof(int32_t) * size_t(B));
+    w.r1_cnt = off;      off = align256(off + sizeof(int32_t) * size_t(B));
     w.join = off;        off = align256(off + sizeof(int32_t) * size_t(B));
+    w.act = off;         off = align256(off + sizeof(int32_t) * size_t(B));
     w.rejflag = off;     off = align256(off + sizeof(int32_t) * size_t(B));
+    w.rej_list = off;    off = align256(off + sizeof(int32_t) * size_t(B));
     w.q_ctr = off;       off = align256(off + sizeof(int32_t) * 16);
     w.rowrec = off;      off = align256(off + 16 * rows * size_t(w.nc));
     w.blkrec = off;      off = align256(off + 8 * size_t(B) * w.nblk * warps);
@@ -89,8 +93,6 @@ inline WorkspaceLayout workspace_layout(int B, int gamma, int V) {
     w.dstate = off;      off = align256(off + sizeof(DecideState) * size_t(B));
     w.q_job = off;       off = align256(off + 8 * size_t(w.qcap));
     w.q_ready = off;     off = align256(off + 4 * size_t(w.qcap));
-    w.qb_job = off;      off = align256(off + 8 * size_t(B));
-    w.qb_ready = off;    off = align256(off + 8 * size_t(B));
     w.total = off;
     return w;
 }
@@ -278,24 +280,26 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 // Wait for phase `parity` of `bar`, sleeping between polls once the wait
 // has lasted a while: a warp that idles this way (a consumer with no tile
 // coming) leaves its issue slots to the warps that still work.  Gives up
-// after kWaitTimeoutNs.
-__device__ __forceinline__ bool mbar_wait_backoff(uint64_t *bar, uint32_t parity) {
+// after `limit_ns`.
+__device__ __forceinline__ bool mbar_wait_backoff(uint64_t *bar, uint32_t parity,
+                                                  uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if (it >= 8) __nanosleep(it >= 64 ? 256u : 64u);
-        if ((it & 15u) == 0 && global_timer_ns() - t0 > kWaitTimeoutNs) return false;
+        if ((it & 15u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
     }
 }
 
-// Wait for phase `parity` of `bar`, giving up after kWaitTimeoutNs.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
+// Wait for phase `parity` of `bar`, giving up after `limit_ns`.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
+                                                  uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 255u) == 0 && global_timer_ns() - t0 > kWaitTimeoutNs) return false;
+        if ((it & 255u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
     }
 }
 
@@ -315,6 +319,7 @@ struct ScoreArgs {
     // Entropy-confidence variant: hidden points at the draft logits, d = V,
     // and ent_scale = log2(e) / theta.
     float ent_scale;
+    uint64_t wait_ns;  // bound of every wait
 };
 
 struct FixedArgs {
@@ -336,8 +341,6 @@ struct VerifyArgs {
     int row_bytes;     // V * elem_bytes
     int nblk;          // sampling blocks per row
     int grp_stride;    // chunk slots per row in rowrec
-    int qcap;          // residual-tile queue capacity
-    int qbcap;         // decider queue capacity
     int greedy;
     float scale;       // log2(e) / Tm (sampling only)
     uint64_t seed;
@@ -350,15 +353,15 @@ struct VerifyArgs {
     float4 *rowrec;
     float2 *blkrec, *zrec, *gath;
     DecideState *dstate;
-    int2 *q_job;
-    int32_t *q_ready, *q_ctr;
-    int32_t *qb_job, *qb_ready;
-    int32_t *req_cnt, *r1_cnt, *status;
-    int32_t *bon_cnt, *join, *rejflag;
+    int32_t *q_ctr, *req_cnt, *bon_cnt, *r1_cnt, *join, *act, *rejflag, *rej_list, *status;
+    int2 *q_job;       // residual-tile queue: jobs (request, tile) ...
+    int32_t *q_ready;  // ... and their ready words (launch epoch)
+    int qcap;          // its capacity
     // Cap-accept audit (all NULL on the plain verify): the window W_b that is
     // committed, the full-block acceptance a_b, and the batch totals.
     const int32_t *commit_len;
     int32_t *accept_full, *audit_totals;
+    uint64_t wait_ns;  // bound of every wait
 };
 
 cudaError_t launch_score_budget(const ScoreArgs &a, int grid, cudaStream_t s);
@@ -368,6 +371,9 @@ int entropy_blocks_per_sm(int logit_bf16);
 cudaError_t launch_fixed_budget(const FixedArgs &a, cudaStream_t s);
 cudaError_t launch_compact(const CompactArgs &a, cudaStream_t s);
 cudaError_t launch_verify(const VerifyArgs &a, int logit_bf16, int grid, cudaStream_t s);
+// The bound of every device wait in the next launches (0 restores kWaitTimeoutNs).
+void set_wait_timeout_ns(uint64_t ns);
+uint64_t wait_timeout_ns();
 int verify_blocks_per_sm(int logit_bf16);
 size_t verify_smem_bytes();
 

@@ -130,8 +130,12 @@ __device__ void score_producer(const ScoreArgs &a, ScoreSmem &sm, uint8_t *ring,
         if (r < rs.rows) next = int(gridDim.x) + atomicAdd(a.row_ctr, 1);
         for (int q = 0; q < (r < rs.rows ? rs.ntr : 1); ++q, ++fill) {
             const int s = fill % kScoreStages, n = fill / kScoreStages;
-            if (n > 0 && !mbar_wait_bounded(&sm.empty[s], (n - 1) & 1)) {
+            if (n > 0 && !mbar_wait_bounded(&sm.empty[s], (n - 1) & 1, a.wait_ns)) {
                 atomicOr(a.status, kStatusWaitTimeout);
+                // Leave only once every copy issued into the ring has landed.
+                for (int f = max(0, fill - kScoreStages); f < fill; ++f)
+                    mbar_wait_bounded(&sm.full[f % kScoreStages], (f / kScoreStages) & 1,
+                                      kDrainTimeoutNs);
                 return;
             }
             if (r >= rs.rows) {
@@ -180,7 +184,7 @@ __device__ int score_consumer(const ScoreArgs &a, ScoreSmem &sm, const uint8_t *
     float acc = 0.f;
     for (int fill = 0;; ++fill) {
         const int s = fill % kScoreStages, n = fill / kScoreStages;
-        if (!mbar_wait_bounded(&sm.full[s], n & 1)) {
+        if (!mbar_wait_bounded(&sm.full[s], n & 1, a.wait_ns)) {
             if (lane == 0) atomicOr(a.status, kStatusWaitTimeout);
             return nrows;
         }
@@ -315,7 +319,7 @@ __device__ int entropy_consumer(const ScoreArgs &a, ScoreSmem &sm, const uint8_t
     Ent acc{-INFINITY, 0.f, 0.f};
     for (int fill = 0;; ++fill) {
         const int s = fill % kScoreStages, n = fill / kScoreStages;
-        if (!mbar_wait_bounded(&sm.full[s], n & 1)) {
+        if (!mbar_wait_bounded(&sm.full[s], n & 1, a.wait_ns)) {
             if (lane == 0) atomicOr(a.status, kStatusWaitTimeout);
             return nrows;
         }

@@ -304,8 +304,10 @@ dspark_status dspark_fit_sts_tau(int32_t N, int32_t gamma, const float *conf,
 
 /*
  * Blocking read of the workspace's device status word (0 = healthy).  A
- * nonzero value means a kernel gave up on a bounded wait; the workspace must
- * then be re-initialised.  Synchronises `stream`.
+ * nonzero value means a kernel gave up on a bounded wait: bit 0 (1) an
+ * in-CTA wait on the copy ring, bit 1 (2) a wait on the verify's work
+ * (events, residual jobs, the end of the batch).  The workspace must then be
+ * re-initialised.  Synchronises `stream`.
  */
 dspark_status dspark_read_device_status(const void *workspace, int32_t *status_out,
                                         dspark_stream_t stream);
@@ -355,6 +357,20 @@ dspark_status dspark_read_device_status(const void *workspace, int32_t *status_o
  */
 dspark_status dspark_verify_noalloc(const dspark_step *step, int32_t reset,
                                     int32_t *status_out, dspark_stream_t stream);
+
+/*
+ * Bound, in nanoseconds, of every wait inside the kernels launched after this
+ * call (process-wide; 0 restores the default of 2 s).  A kernel whose wait
+ * runs out sets a nonzero device status (dspark_read_device_status), lets
+ * its own copies in flight land, and returns; its outputs are then not
+ * valid and the workspace must be re-initialised.  Meant for tests of that
+ * error path: a bound of a few microseconds makes ordinary waits give up.
+ * Always returns DSPARK_OK.
+ */
+dspark_status dspark_set_wait_timeout_ns(uint64_t ns);
+
+/* The current bound (see dspark_set_wait_timeout_ns). */
+uint64_t dspark_wait_timeout_ns(void);
 
 /* Thread-local message for the last failing call on this thread ("" if none). */
 const char *dspark_last_error(void);
