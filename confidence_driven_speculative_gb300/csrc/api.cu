@@ -360,6 +360,8 @@ static dspark_status verify_impl(const dspark_step *s, const int32_t *commit_len
     a.chunk_elems = int(dspark::kChunkBytes / ls);
     a.nblk = lay.nblk;
     a.grp_stride = lay.nc;
+    a.qcap = lay.qcap;
+    a.qbcap = 2 * s->B;
     a.greedy = greedy;
     a.scale = greedy ? 0.f : float(1.4426950408889634 / double(s->temperature));
     a.seed = s->seed;
@@ -380,12 +382,11 @@ static dspark_status verify_impl(const dspark_step *s, const int32_t *commit_len
     a.bon_cnt = ws_at<int32_t>(s, lay.bon_cnt);
     a.r1_cnt = ws_at<int32_t>(s, lay.r1_cnt);
     a.join = ws_at<int32_t>(s, lay.join);
-    a.act = ws_at<int32_t>(s, lay.act);
     a.rejflag = ws_at<int32_t>(s, lay.rejflag);
-    a.rej_list = ws_at<int32_t>(s, lay.rej_list);
     a.q_job = ws_at<int2>(s, lay.q_job);
     a.q_ready = ws_at<int32_t>(s, lay.q_ready);
-    a.qcap = lay.qcap;
+    a.qb_job = ws_at<int32_t>(s, lay.qb_job);
+    a.qb_ready = ws_at<int32_t>(s, lay.qb_ready);
     a.status = ws_at<int32_t>(s, lay.status);
     a.commit_len = commit_len;
     a.accept_full = accept_full;
@@ -398,8 +399,8 @@ static dspark_status verify_impl(const dspark_step *s, const int32_t *commit_len
                                         reinterpret_cast<cudaStream_t>(stream));
         if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(accept_full)");
     }
-    // One CTA per resident slot; the work is spread over the grid inside the
-    // kernel.
+    // One CTA per resident slot: the cooperative launch requires it, and the
+    // work is spread over the grid inside the kernel.
     const int grid = dev->sms * dev->verify_blocks[bf];
     cudaError_t e = dspark::launch_verify(a, bf, grid, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "verify_kernel launch");

@@ -17,6 +17,7 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kConsumerWarps = 8;        // verify: consumer warps per CTA
 constexpr int kVerifyThreads = (kConsumerWarps + 2) * 32;  // + producer and decider warps
 constexpr int kChunkBytes = 16384;       // one vocab tile of one row (verify)
+constexpr int kStages = 3;               // verify smem ring: kStages x (target + draft) tiles
 constexpr int kSampleBlock = 4096;       // token ids per block of the two-level draw
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // bounded waits: 2 s (default)
 constexpr uint64_t kDrainTimeoutNs = 100000000ull;  // a CTA that gave up waits this long at
@@ -35,6 +36,7 @@ struct DecideState {
     float u_blk, u_tok;      // the draw's two uniforms
 };
 
+
 // ---------------------------------------------------------------------------
 // Workspace layout (all offsets 256-byte aligned).
 // ---------------------------------------------------------------------------
@@ -42,22 +44,22 @@ struct WorkspaceLayout {
     size_t status;        // int32
     size_t score_done;    // int32 [1]   hidden rows published
     size_t score_rows;    // int32 [1]   hidden rows claimed
-    size_t verify_cnt;    // int32 [B]   per-request decision chunks done
-    size_t bon_cnt;       // int32 [B]   per-request bonus-row chunks done
+    size_t verify_cnt;    // int32 [B]   per-request stream tiles done
     size_t r1_cnt;        // int32 [B]   per-request residual tiles done
+    size_t bon_cnt;       // int32 [B]   per-request bonus-row tiles done
     size_t join;          // int32 [B]   drafts all accepted + bonus row streamed
-    size_t act;           // int32 [B]   per-request draw still to make (verify)
     size_t rejflag;       // int32 [B]   launch epoch of a found rejection
-    size_t rej_list;      // int32 [B]   requests with a residual draw
-    size_t q_ctr;         // int32 [16]  chunk counter, grid barrier, epoch, exited CTAs,
-                          //             rejections, audit totals
+    size_t q_ctr;         // int32 [16]  queue heads / tails, finished, exited, epoch, chunk,
+                          //             audit totals
     size_t rowrec;        // float4 [B*(gamma+1) * nc]      row partials per (row, chunk)
-    size_t blkrec;        // float2 [B * nblk * 8]          bonus-row (max, sum) per slot
-    size_t zrec;          // float2 [B * nblk * 8]          residual / p masses per slot
+    size_t blkrec;        // float2 [B * nblk * 8]          bonus-row block partials per warp
+    size_t zrec;          // float2 [B * nblk * 8]          residual / p block masses per warp
     size_t gath;          // float2 [B * (gamma+1)]         z_p[d], z_q[d]
     size_t dstate;        // DecideState [B]
     size_t q_job;         // int2 [qcap]    residual-tile jobs (request, tile)
-    size_t q_ready;       // int32 [qcap]   launch epoch once the job is published
+    size_t q_ready;       // int32 [qcap]
+    size_t qb_job;        // int32 [2B]     decider jobs (decide / finish residual)
+    size_t qb_ready;      // int32 [2B]
     size_t total;
     int nblk;             // sampling blocks per row
     int nc;               // 16 KB tiles per row (fp32, the larger count)
@@ -79,12 +81,10 @@ inline WorkspaceLayout workspace_layout(int B, int gamma, int V) {
     w.score_done = off;  off = align256(off + sizeof(int32_t));
     w.score_rows = off;  off = align256(off + sizeof(int32_t));
     w.verify_cnt = off;  off = align256(off + sizeof(int32_t) * size_t(B));
-    w.bon_cnt = off;     off = align256(off + sizeof(int32_t) * size_t(B));
     w.r1_cnt = off;      off = align256(off + sizeof(int32_t) * size_t(B));
+    w.bon_cnt = off;     off = align256(off + sizeof(int32_t) * size_t(B));
     w.join = off;        off = align256(off + sizeof(int32_t) * size_t(B));
-    w.act = off;         off = align256(off + sizeof(int32_t) * size_t(B));
     w.rejflag = off;     off = align256(off + sizeof(int32_t) * size_t(B));
-    w.rej_list = off;    off = align256(off + sizeof(int32_t) * size_t(B));
     w.q_ctr = off;       off = align256(off + sizeof(int32_t) * 16);
     w.rowrec = off;      off = align256(off + 16 * rows * size_t(w.nc));
     w.blkrec = off;      off = align256(off + 8 * size_t(B) * w.nblk * warps);
@@ -93,6 +93,8 @@ inline WorkspaceLayout workspace_layout(int B, int gamma, int V) {
     w.dstate = off;      off = align256(off + sizeof(DecideState) * size_t(B));
     w.q_job = off;       off = align256(off + 8 * size_t(w.qcap));
     w.q_ready = off;     off = align256(off + 4 * size_t(w.qcap));
+    w.qb_job = off;      off = align256(off + 8 * size_t(B));
+    w.qb_ready = off;    off = align256(off + 8 * size_t(B));
     w.total = off;
     return w;
 }
@@ -341,6 +343,8 @@ struct VerifyArgs {
     int row_bytes;     // V * elem_bytes
     int nblk;          // sampling blocks per row
     int grp_stride;    // chunk slots per row in rowrec
+    int qcap;          // residual-tile queue capacity
+    int qbcap;         // decider queue capacity
     int greedy;
     float scale;       // log2(e) / Tm (sampling only)
     uint64_t seed;
@@ -353,10 +357,11 @@ struct VerifyArgs {
     float4 *rowrec;
     float2 *blkrec, *zrec, *gath;
     DecideState *dstate;
-    int32_t *q_ctr, *req_cnt, *bon_cnt, *r1_cnt, *join, *act, *rejflag, *rej_list, *status;
-    int2 *q_job;       // residual-tile queue: jobs (request, tile) ...
-    int32_t *q_ready;  // ... and their ready words (launch epoch)
-    int qcap;          // its capacity
+    int2 *q_job;
+    int32_t *q_ready, *q_ctr;
+    int32_t *qb_job, *qb_ready;
+    int32_t *req_cnt, *r1_cnt, *status;
+    int32_t *bon_cnt, *join, *rejflag;
     // Cap-accept audit (all NULL on the plain verify): the window W_b that is
     // committed, the full-block acceptance a_b, and the batch totals.
     const int32_t *commit_len;

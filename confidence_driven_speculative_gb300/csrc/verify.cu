@@ -12,51 +12,47 @@
 // unchanged.
 //
 // Design (GB300).  The pass is HBM-bound: every packed target row (sum L + B)
-// and every kept draft row (sum L) is read at most once, V logits each; a
-// rejected request's row pair is read once more for its residual.
+// and every kept draft row (sum L) is read at most once, V logits each.
 //
-// One persistent cooperative grid, a few CTAs per SM, in three phases
-// separated by grid barriers:
-//
-//  1. Stream.  Each CTA is a producer warp, 8 consumer warps and a decider
-//     warp.  The producer fills a 3-stage shared-memory ring with 1-D bulk
-//     TMA copies (cp.async.bulk) completing on "full" mbarriers with byte
-//     counts; each consumer warp releases a stage on its "empty" mbarrier as
-//     soon as it has read it.  Work is a sequence of chunks handed out by an
-//     atomic counter: first the decision rows (target row k with draft row
-//     (b, k) in sampling, k < L_b) in draft order, a few 16 KB tiles per
-//     chunk, so a request's rows are spread over many CTAs; then each
-//     request's bonus row (k = L_b), skipping requests already known to
-//     reject (the method never reads past the first rejection).  A consumer
-//     warp owns one eighth of every tile: online (max, sum of
-//     2^(z log2(e)/Tm - max)) accumulators for p and q (greedy: max and
-//     lowest argmax), reduced once per chunk into a record slot of the row;
-//     a bonus row keeps one (max, sum) slot per tile and warp -- the block
-//     masses of its draw.  The warp that completes a chunk counts it per
-//     request with a device atomic; the CTA whose count completes a request
-//     decides it in its decider warp: accept tests, p(d), q(d), a_b, and a
-//     rejection marks the request so its bonus row is skipped.
-//  2. Residual.  The normalised residual max(0, p - q) of a rejected row
-//     pair needs that row's normalisers, known only now.  The tiles of every
-//     rejected row pair are spread over the grid and streamed again through
-//     the rings (partly still in L2); each warp writes the residual and p
-//     masses of its slot.
-//  3. Draw.  Every warp of the grid takes requests in turn and makes the
-//     draw: the bonus token from p at row L_b (every draft accepted), or the
-//     residual token at row a_b.  Draws are two-level: a 4096-id block by mass
-//     (u'), then an id inside it (u''); in-block running sums are fp32 over
-//     short lane runs combined in two-float (TwoSum) arithmetic, as exact as
-//     fp64 on the fast fp32 pipe.
-//
-// Every wait is bounded (VerifyArgs::wait_ns) and sets a status bit when it
-// gives up; a producer that gave up waits for its own copies in flight before
-// it leaves.  Counters reset themselves at the end of the launch.
-//
-// The cap-accept audit arm ("DFlash to DSpark in SGLang", "The confidence
-// scheduler and verify modes") is the same launch with a committed window
-// W_b: every draft of the block is tested, the commit is min(a_b, W_b), and a
-// window that ends inside the accepted run draws from p at row W_b through
-// the residual path (what compact's bonus draw would be).
+//  * One persistent cooperative grid, 2 CTAs per SM; each CTA is a producer
+//    warp, 8 consumer warps and a decider warp.  The producer's lane 0 fills
+//    a 3-stage shared-memory ring with 1-D bulk TMA copies (cp.async.bulk)
+//    completing on "full" mbarriers with byte counts; each consumer warp
+//    releases a stage on its "empty" mbarrier.  No block-wide barrier in the
+//    loop.
+//  * Stream work is a queue of chunks handed out by an atomic counter, in
+//    two phases.  Phase P streams the decision rows (k < L_b: target row k
+//    with draft row (b, k) in sampling) in packed-row order, whole rows and
+//    then quarter rows for the last wave (single 16 KB tiles for small
+//    batches).  Phase Q streams each request's bonus row (k = L_b), skipping
+//    requests already known to reject: the method never reads past the
+//    first rejection.
+//  * A consumer warp owns one eighth of every tile.  For a pair row its
+//    lanes keep online (max, sum of 2^(z log2(e)/Tm - max)) accumulators for
+//    p and q across the tiles of the chunk and reduce once, at the chunk's
+//    end, into a record slot of the row (plain stores: deterministic).  A
+//    bonus row stores one slot per tile and warp, which gives the per-block
+//    masses of the draw.  Greedy rows keep (max, lowest argmax).
+//  * The producer books the stages it gets back: tiles are counted per
+//    (request, decision / bonus) locally and published with one fenced
+//    atomic per change.  A request whose decision rows are in becomes a
+//    decide job; its bonus row being in, together with every draft accepted
+//    (a join counter), makes the bonus-draw job.  Decider warps serve these
+//    jobs from a device-wide queue.  A rejection queues residual-mass jobs
+//    (one tile of the rejecting row pair, read again while it is still in
+//    L2), which producers serve through their rings before their own chunks;
+//    the last of them queues the residual draw.
+//  * Draws are two-level: a 4096-id block by mass (u'), then an id inside it
+//    (u''); in-block running sums are fp32 over short lane runs combined in
+//    two-float (TwoSum) arithmetic, as exact as fp64 on the fast fp32 pipe.
+//  * Every wait is bounded (2 s) and sets a status bit when it gives up;
+//    counters reset themselves at the end of the launch.
+//  * The cap-accept audit arm ("DFlash to DSpark in SGLang", "The
+//    confidence scheduler and verify modes") is the same launch with a
+//    committed window W_b: every draft of the block is tested, the commit is
+//    min(a_b, W_b), and a window that ends inside the accepted run draws
+//    from p at row W_b through the residual-tile path (what compact's bonus
+//    draw would be).
 #include <climits>
 
 #include "dspark_internal.cuh"
@@ -65,30 +61,15 @@ namespace dspark {
 namespace {
 
 constexpr int kCW = kConsumerWarps;
-constexpr int kRing = 3;                      // stages of the shared-memory ring
-constexpr int kWarpsPerCta = kVerifyThreads / 32;
 constexpr int kStageBytes = 2 * kChunkBytes;  // target tile + draft tile
-constexpr size_t kSmemBytes = size_t(kRing) * kStageBytes;
-constexpr int kFifo = 64;                     // CTA event FIFO slots (power of two)
-constexpr int kJobs = 64;                     // CTA draw queue slots (power of two)
+constexpr size_t kSmemBytes = size_t(kStages) * kStageBytes;
 
-enum : int { T_END = 0, T_STREAM = 1, T_RESID = 2 };
+enum : int { T_EXIT = 0, T_STREAM = 1, T_RESID = 2 };
 enum : int { D_BONUS = 0, D_RESID = 1, D_FALLBACK = 2 };
-// Draw still to make for a request after phase 1 (act[b]).
-enum : int { A_NONE = 0, A_RESID = 1, A_BONUS = 2 };
-// q_ctr words: stream-chunk counter, grid barrier count and generation,
-// launch epoch, exited CTAs, rejected requests, audit sums.
-enum : int { Q_CHUNK = 0, Q_BAR = 1, Q_BARGEN = 2, Q_EPOCH = 3, Q_EXITED = 4, Q_NREJ = 5,
-             Q_AFULL = 8, Q_ACOMMIT = 9 };
-// Events the producer posts to its CTA's decider: request b's decision rows
-// (EV_P), its bonus row (EV_Q) or its residual tiles (EV_R) are all in.
-// Encoded as kEvMark | type << 24 | L_b << 16 | b (b < 2^16, L_b <= 64).
-enum : int { EV_P = 1, EV_Q = 2, EV_R = 3 };
-constexpr int kEvMark = 1 << 30;
-
-__device__ __forceinline__ int ev_make(int type, int Lb, int b) {
-    return kEvMark | (type << 24) | (Lb << 16) | b;
-}
+// q_ctr words: residual-tile queue head / tail, finished requests, exited CTAs,
+// launch epoch, stream-chunk counter, decide queue head / tail, audit sums.
+enum : int { QA_HEAD = 0, QA_TAIL = 1, Q_FINISHED = 2, Q_EXITED = 3, Q_EPOCH = 4, Q_CHUNK = 5,
+             QB_HEAD = 6, QB_TAIL = 7, Q_AFULL = 8, Q_ACOMMIT = 9 };
 
 struct TaskInfo {
     int type;   // T_*
@@ -104,44 +85,34 @@ struct TaskInfo {
     int bytes2; // target-only rows: the row's next tile in the second half (0: none)
     int d;      // stream pair: drafted id (its gather target)
     int flush;  // stream: last tile of the chunk
-    int mode;   // residual tile: D_RESID (residual weights) or D_FALLBACK (p)
-    float u_tok;           // bonus row / residual tile: the in-block uniform u'' of the draw
-    float Mp, Sp, Mq, Sq;  // residual tile: normalisers of the rejected row pair
 };
 
 struct VSmem {
-    uint64_t full[kRing], empty[kRing];
-    TaskInfo task[kRing];
-    // Chunk-end partials and the count of warps past a stage, one set per
-    // parity of the stage's use: a warp may reach the next use of the stage
-    // before the last warp of this one has counted itself.
-    float4 part[kRing][2][kCW];
-    int done[kRing][2];
-    int fifo[kFifo];       // consumer -> decider events (0: empty slot)
-    int fifo_tail;         // next slot a consumer claims
-    int fifo_head;         // next slot the decider reads
-    int prod_done;         // the producer has booked every unit of the phase
-    // Draws waiting for a warp (event codes): the decider queues them; any
-    // warp without other work -- the decider between events, the consumers
-    // and the producer once their phase's stream is done -- takes them.
-    int jobs[kJobs];
-    int job_tail;          // next slot the decider fills
-    int job_head;          // next slot a warp takes
-    int no_more;           // the decider has queued the phase's last draw
+    uint64_t full[kStages], empty[kStages];
+    TaskInfo task[kStages];
+    float4 part[kStages][kCW];  // per-warp row partials of a chunk's last tile
+    int done[kStages];          // warps finished with a chunk's last tile
 };
 
-// Grid-wide shape of the stream work, the same in every thread.  Packed row
-// i (0 <= i < sum L + B, request by request: decision rows, then the bonus
-// row) is cut into cpr chunks of CT tiles; chunk c is row c / cpr.
+// Grid-wide shape of the stream work, the same in every thread.  Two
+// phases.  Phase P walks the packed rows and streams the decision rows
+// (k < L_b; a bonus row's chunks are claimed and skipped): rows below nA are
+// one chunk each, rows [nA, nB) are cut into chunks of Cb tiles (gprb per
+// row), rows from nB on go out tile by tile.  Phase Q streams each
+// request's bonus row (k = L_b) in chunks of CbQ tiles, skipping requests
+// already known to reject.  So the accept tests -- and the residual draws
+// they start -- run while the bonus rows are still streaming.
 struct StreamShape {
     int n_rows;    // packed rows
-    int n_dec;     // decision rows (sum L)
-    int CT;        // tiles per decision chunk
-    int cpr;       // chunks per decision row
-    int CTQ;       // tiles per bonus chunk
-    int cprQ;      // chunks per bonus row
-    int nP;        // decision chunks
-    int n_chunks;  // decision and bonus chunks
+    int nA;        // rows handed out whole
+    int nB;        // first row handed out in single tiles
+    int Cb;        // tiles per chunk in rows [nA, nB)
+    int gprb;      // chunks per row in rows [nA, nB)
+    int nq;        // chunks of rows [nA, nB)
+    int nP;        // chunks of phase P
+    int CbQ;       // tiles per chunk of a bonus row
+    int gprbQ;     // chunks per bonus row
+    int n_chunks;  // phase P and phase Q
 };
 
 // ---------------------------------------------------------------------------
@@ -178,62 +149,36 @@ __device__ __forceinline__ DecideState load_state(const VerifyArgs &a, int b) {
     return st;
 }
 
-__device__ __forceinline__ int ld_vol(const int *p) { return *reinterpret_cast<const volatile int *>(p); }
-__device__ __forceinline__ void st_vol(int *p, int v) { *reinterpret_cast<volatile int *>(p) = v; }
-
-// The uniforms (u, u', u'') of draft position k of request b, out of line so
-// that decisions and draws share one copy of the generator's code.
-__device__ __noinline__ float3 uniforms_of(uint64_t seed, int b, int k) {
-    float3 r;
-    step_uniforms(seed, b, k, r.x, r.y, r.z);
-    return r;
-}
-
 __device__ __forceinline__ int verify_len(const VerifyArgs &a, int b) {
     return min(max(a.L[b], 0), a.gamma);
 }
 
 __device__ __forceinline__ StreamShape stream_shape(const VerifyArgs &a) {
     StreamShape sh;
-    const int cap = a.B * (a.gamma + 1);
-    // packed rows and drafts as written by the score and compaction kernels,
-    // never more than their capacities
-    sh.n_rows = min(max(a.row_off[a.B], 0), cap);
-    sh.n_dec = min(max(a.draft_off[a.B], 0), a.B * a.gamma);
-    if (sh.n_rows < a.B) sh.n_rows = sh.n_dec = 0;  // not the compaction's offsets: no work
-    const long long tiles = (long long)sh.n_rows * a.nc;
-    const long long g = gridDim.x;
-    // a few tiles per chunk when there is plenty of work (fewer chunk
-    // records and events); single tiles when there is little, so that every
-    // CTA gets some
-    sh.CT = tiles >= 16 * g ? 4 : tiles >= 4 * g ? 2 : 1;
-    sh.cpr = (a.nc + sh.CT - 1) / sh.CT;
-    sh.CTQ = sh.CT;
-    sh.cprQ = sh.cpr;
-    sh.nP = sh.n_rows * sh.cpr;
-    sh.n_chunks = sh.nP;
-    return sh;
-}
-
-// Largest b in [0, B) with off[b] <= i (off non-decreasing, off[0] = 0):
-// the request of decision i.  A 32-way search by the whole warp, two rounds
-// of loads for B <= 1024; off is read-only during the launch (__ldg).
-// off_b receives off[b].
-__device__ int find_request(const int32_t *off, int B, int i, int lane, int &off_b) {
-    int lo = 0, hi = B;
-    int val = __ldg(off);
-    while (hi - lo > 1) {
-        const int step = (hi - lo + 31) >> 5;
-        const int p = lo + lane * step;
-        const int x = p < hi ? __ldg(off + p) : INT_MAX;
-        const unsigned m = __ballot_sync(0xffffffffu, lane == 0 || x <= i);
-        const int l = 31 - __clz(m);
-        val = __shfl_sync(0xffffffffu, x, l);
-        lo += l * step;
-        hi = min(hi, lo + step);
+    // packed rows as written by the compaction, never more than its capacity
+    sh.n_rows = min(max(a.row_off[a.B], 0), a.B * (a.gamma + 1));
+    const long long n_tiles = (long long)sh.n_rows * a.nc;
+    if (n_tiles >= 32LL * gridDim.x) {
+        // many rows: whole rows, then the last gridDim.x rows in quarters
+        // (quarters everywhere, or single-tile chunks, cost more in chunk
+        // overhead than they gain in balance)
+        sh.nA = max(0, sh.n_rows - int(gridDim.x));
+        sh.nB = sh.n_rows;
+        sh.Cb = max(1, a.nc / 4);
+        sh.CbQ = sh.Cb;
+    } else {
+        // few rows: single tiles
+        sh.nA = 0;
+        sh.nB = 0;
+        sh.Cb = 1;
+        sh.CbQ = 1;
     }
-    off_b = val;
-    return lo;
+    sh.gprb = (a.nc + sh.Cb - 1) / sh.Cb;
+    sh.nq = (sh.nB - sh.nA) * sh.gprb;
+    sh.nP = sh.nA + sh.nq + (sh.n_rows - sh.nB) * a.nc;
+    sh.gprbQ = (a.nc + sh.CbQ - 1) / sh.CbQ;
+    sh.n_chunks = sh.nP + a.B * sh.gprbQ;
+    return sh;
 }
 
 // Fold one vector of logits into a running (max, sum of 2^((z - max) * s)).
@@ -324,234 +269,229 @@ __device__ __forceinline__ float warp_max(float v) {
 }
 
 // ---------------------------------------------------------------------------
-// producer: warp kCW.  Lane 0 issues the copies; the whole warp resolves the
-// next chunk, one step per fill, so that its loads overlap the copies of the
-// current chunk.
+// queues
 // ---------------------------------------------------------------------------
-struct Chunk {
-    // 0: claim an index, 1: locate it, 2: load its metadata, 3: keep or
-    // skip, 4: ready, 5: none left
+// Residual-tile jobs (request b, tile c), served by every producer through
+// its TMA ring.
+__device__ void push_resid_jobs(const VerifyArgs &a, int b, int epoch) {
+    const int pos = atomicAdd(&a.q_ctr[QA_TAIL], a.nc);
+    for (int i = 0; i < a.nc; ++i)
+        if (pos + i < a.qcap) a.q_job[pos + i] = make_int2(b, i);
+    __threadfence();  // every payload (and the caller's state) before any ready word
+    for (int i = 0; i < a.nc; ++i)
+        if (pos + i < a.qcap) st_relaxed(&a.q_ready[pos + i], epoch);
+}
+
+// Decider jobs, served by the decider warps: decide request b, or (with
+// kFinishResidual / kBonusDraw set) finish its residual draw / make its
+// bonus draw.
+__device__ void push_decide(const VerifyArgs &a, int job, int epoch) {
+    const int pos = atomicAdd(&a.q_ctr[QB_TAIL], 1);
+    if (pos < a.qbcap) {
+        a.qb_job[pos] = job;
+        __threadfence();
+        st_relaxed(&a.qb_ready[pos], epoch);
+    }
+}
+
+__device__ TaskInfo resid_task(const VerifyArgs &a, int2 jb) {
+    TaskInfo t;
+    t.type = T_RESID;
+    t.b = jb.x;
+    t.j = jb.y;
+    t.d = -1;
+    t.g = t.flush = 0;
+    t.Lb = verify_len(a, t.b);
+    const DecideState st = load_state(a, t.b);
+    t.k = st.a;
+    t.r = a.row_off[t.b] + st.a;
+    t.pair = 1;
+    t.y0 = t.j * a.chunk_elems;
+    t.bytes = min(kChunkBytes, a.row_bytes - t.j * kChunkBytes);
+    t.bytes2 = 0;
+    return t;
+}
+
+// ---------------------------------------------------------------------------
+// producer: lane 0 of warp kCW
+// ---------------------------------------------------------------------------
+// The next chunk, fetched over several fills so that its global loads
+// (counter, row ids, request metadata) never stall the issue of a tile.
+struct ChunkFetch {
+    // 0: claim an index, 1: row ids, 2: request data, 3: keep or skip,
+    // 4: ready, 5: none left
     int stage;
     int c, q, r, g, b, k, Lb, d, rej;
-    float u;  // bonus row: u'' of the bonus draw (position L_b)
 };
 
-__device__ void fetch_step(const VerifyArgs &a, const StreamShape &sh, Chunk &f, int epoch,
-                           int lane) {
+__device__ __forceinline__ void fetch_step(const VerifyArgs &a, const StreamShape &sh,
+                                           ChunkFetch &f, int epoch) {
     if (f.stage == 0) {
-        // the claim's round trip completes while the next fill is issued
-        if (lane == 0) f.c = atomicAdd(&a.q_ctr[Q_CHUNK], 1);
+        f.c = int(gridDim.x) + atomicAdd(&a.q_ctr[Q_CHUNK], 1);
         f.stage = 1;
     } else if (f.stage == 1) {
-        f.c = __shfl_sync(0xffffffffu, f.c, 0);
         if (f.c >= sh.n_chunks) {
             f.stage = 5;
             return;
         }
-        // packed row i of request b: index k = i - row_off[b] (k = L_b: the
-        // bonus row)
-        const int i = f.c / sh.cpr;
-        f.g = f.c - i * sh.cpr;
-        int off_b;
-        f.b = find_request(a.row_off, a.B, i, lane, off_b);
-        f.k = min(max(i - off_b, 0), a.gamma);
-        f.r = min(i, sh.n_rows - 1);
+        f.q = f.c >= sh.nP;
+        if (f.q) {
+            // phase Q: the bonus row of request b
+            const int cc = f.c - sh.nP;
+            f.b = cc / sh.gprbQ;
+            f.g = cc - f.b * sh.gprbQ;
+            f.r = a.row_off[f.b + 1] - 1;
+            f.rej = ld_relaxed(&a.rejflag[f.b]);
+        } else {
+            if (f.c < sh.nA) {
+                f.r = f.c;
+                f.g = 0;
+            } else if (f.c < sh.nA + sh.nq) {
+                const int cc = f.c - sh.nA;
+                f.r = sh.nA + cc / sh.gprb;
+                f.g = cc - (f.r - sh.nA) * sh.gprb;
+            } else {
+                const int cc = f.c - sh.nA - sh.nq;
+                f.r = sh.nB + cc / a.nc;
+                f.g = cc - (f.r - sh.nB) * a.nc;
+            }
+            f.b = a.row_req[f.r];
+            f.k = a.row_k[f.r];
+            f.rej = 0;
+        }
         f.stage = 2;
     } else if (f.stage == 2) {
-        // independent loads, one per lane; used a fill later
-        int v = 0;
-        if (lane == 0) v = a.L[f.b];
-        else if (lane == 1 && f.k < a.gamma) v = a.draft_tokens[size_t(f.b) * a.gamma + f.k];
-        f.d = v;  // parked in f.d per lane until the next step
+        f.Lb = verify_len(a, f.b);
+        if (f.q) {
+            f.k = f.Lb;
+            f.d = -1;
+        } else {
+            f.d = f.k < a.gamma ? a.draft_tokens[size_t(f.b) * a.gamma + f.k] : -1;
+        }
         f.stage = 3;
     } else if (f.stage == 3) {
-        const int v0 = __shfl_sync(0xffffffffu, f.d, 0);
-        const int v1 = __shfl_sync(0xffffffffu, f.d, 1);
-        f.Lb = min(max(v0, 0), a.gamma);
-        f.q = f.k >= f.Lb;  // the bonus row
-        f.d = f.q ? -1 : v1;
-        f.u = 0.f;
-        f.stage = 4;
+        // phase P skips bonus rows; phase Q skips requests already rejected
+        const bool skip = f.q ? f.rej == epoch : f.k >= f.Lb;
+        f.stage = skip ? 0 : 4;
     }
 }
 
-// A producer that gave up on a wait: let every copy it issued land before
-// the CTA can leave (each is the only outstanding use of its stage).
-__device__ void drain_copies(VSmem &sm, int fill, int lane) {
-    if (lane == 0)
-        for (int f = max(0, fill - kRing); f < fill; ++f)
-            mbar_wait_bounded(&sm.full[f % kRing], (f / kRing) & 1, kDrainTimeoutNs);
-    __syncwarp();
-}
+// Books of the stages the producer gets back: stream tiles are counted per
+// (request, kind) locally and published with one fenced atomic per change.
+// Decision-row tiles complete a request's decide job.  Bonus-row tiles
+// complete its bonus row; the bonus draw then runs once the decide has
+// accepted every draft (join counter), at once when there are no drafts.
+constexpr int kFinishResidual = 1 << 30;  // decider job: finish the residual draw
+constexpr int kBonusDraw = 1 << 29;       // decider job: the bonus draw
 
-// ---------------------------------------------------------------------------
-// consumer -> decider events
-// ---------------------------------------------------------------------------
-// Post an event (lane 0 of a consumer warp).  The caller has fenced its
-// global writes; the FIFO store is ordered after them.
-__device__ void post_event(const VerifyArgs &a, VSmem &sm, int ev) {
-    const int pos = atomicAdd(&sm.fifo_tail, 1);
-    if (pos - ld_vol(&sm.fifo_head) >= kFifo) {
-        const uint64_t t0 = global_timer_ns();
-        while (pos - ld_vol(&sm.fifo_head) >= kFifo) {
-            if (global_timer_ns() - t0 > a.wait_ns) {
-                atomicOr(a.status, kStatusQueueTimeout);
-                return;
-            }
-            __nanosleep(64);
-        }
-    }
-    __threadfence_block();
-    st_vol(&sm.fifo[pos & (kFifo - 1)], ev);
-}
-
-// The producer's books.  A stage it takes back from the consumers is done,
-// records included: the warp that writes a chunk's record releases the stage
-// after writing it.  A decision chunk is then counted towards its request with
-// a device atomic; the count comes back while the next fill is issued, and if
-// it completed the request's decision rows the request goes to the CTA's
-// decider (shared-memory FIFO).  Counting when the work completes, not when a
-// decider gets to it, keeps a busy decider from becoming the last arriver of
-// other requests.
+// The count an atomic returned is checked one flush (or one fill) later, so
+// the atomic's round trip overlaps the issue of copies instead of stalling it.
 struct Books {
-    int ev;      // event to post once the count is back (0: none)
-    int old;     // the counter's value before our increment
-    int target;  // chunks of the request
+    int acc_b, acc_kind, acc_n, acc_total, acc_Lb;
+    int chk_b, chk_kind, chk_end, chk_Lb, chk_old;  // a published count awaiting its check
 };
 
-__device__ __forceinline__ void check_books(const VerifyArgs &a, VSmem &sm, Books &bk) {
-    if (bk.ev != 0 && bk.old == bk.target - 1) post_event(a, sm, bk.ev);
-    bk.ev = 0;
+// Act on the count published last: a completed request's job.
+__device__ void check_books(const VerifyArgs &a, Books &bk, int epoch) {
+    if (bk.chk_b < 0) return;
+    const int b = bk.chk_b;
+    if (bk.chk_old == bk.chk_end) {
+        if (bk.chk_kind == 0) push_decide(a, b, epoch);
+        else if (bk.chk_Lb == 0 || atomicAdd(&a.join[b], 1) == 1) push_decide(a, b | kBonusDraw, epoch);
+    }
+    bk.chk_b = -1;
 }
 
-__device__ __forceinline__ void book_stage(const VerifyArgs &a, VSmem &sm, const TaskInfo &t,
-                                           Books &bk, const StreamShape &sh) {
-    check_books(a, sm, bk);
-    int *cnt;
-    if (t.type == T_RESID) {
-        // a residual tile of the request's rejected row pair
-        cnt = &a.r1_cnt[t.b];
-        bk.target = a.nc;
-        bk.ev = ev_make(EV_R, 0, t.b);
-    } else if (t.type == T_STREAM && t.flush) {
-        if (t.k < t.Lb) {
-            // a chunk of one of the request's decision rows
-            cnt = &a.req_cnt[t.b];
-            bk.target = t.Lb * sh.cpr;
-            bk.ev = ev_make(EV_P, t.Lb, t.b);
-        } else {
-            // a chunk of its bonus row
-            cnt = &a.bon_cnt[t.b];
-            bk.target = sh.cprQ;
-            bk.ev = ev_make(EV_Q, t.Lb, t.b);
-        }
-    } else {
-        return;
-    }
+__device__ void flush_books(const VerifyArgs &a, Books &bk, int epoch) {
+    if (bk.acc_n == 0) return;
+    check_books(a, bk, epoch);
     __threadfence();
-    bk.old = atomicAdd(cnt, 1);
+    const int b = bk.acc_b;
+    bk.chk_old = atomicAdd(bk.acc_kind == 0 ? &a.req_cnt[b] : &a.bon_cnt[b], bk.acc_n);
+    bk.chk_b = b;
+    bk.chk_kind = bk.acc_kind;
+    bk.chk_end = bk.acc_total - bk.acc_n;  // the count before ours when ours completes it
+    bk.chk_Lb = bk.acc_Lb;
+    bk.acc_n = 0;
 }
 
-// The end of a phase (the end marker is issued at `fill`): take back every
-// stage still out, the marker's included, book what they held, and tell the
-// decider that no more events will come.
-__device__ bool finish_books(const VerifyArgs &a, VSmem &sm, int fill, int lane, Books &bk,
-                             const StreamShape &sh) {
-    for (int f = max(0, fill - kRing + 1); f <= fill; ++f) {
-        int w = 1;
-        if (lane == 0) w = mbar_wait_bounded(&sm.empty[f % kRing], (f / kRing) & 1, a.wait_ns);
-        if (!__shfl_sync(0xffffffffu, w, 0)) {
-            if (lane == 0) atomicOr(a.status, kStatusWaitTimeout);
+__device__ __forceinline__ void account(const VerifyArgs &a, Books &bk, const TaskInfo &t,
+                                        int epoch) {
+    if (t.type != T_STREAM) return;
+    const int kind = t.k < t.Lb ? 0 : 1;
+    if (t.b != bk.acc_b || kind != bk.acc_kind) {
+        flush_books(a, bk, epoch);
+        bk.acc_b = t.b;
+        bk.acc_kind = kind;
+        bk.acc_Lb = t.Lb;
+        bk.acc_total = (kind == 0 ? t.Lb : 1) * a.nc;
+    }
+    bk.acc_n += t.bytes2 > 0 ? 2 : 1;
+}
+
+// Wait for every fill below `upto` to come back from the consumers and book it.
+__device__ bool reclaim(const VerifyArgs &a, VSmem &sm, Books &bk, int &booked, int upto,
+                        int epoch) {
+    for (; booked < upto; ++booked) {
+        const int s = booked % kStages;
+        if (!mbar_wait_bounded(&sm.empty[s], (booked / kStages) & 1, a.wait_ns)) {
+            atomicOr(a.status, kStatusWaitTimeout);
             return false;
         }
-        if (lane == 0) book_stage(a, sm, sm.task[f % kRing], bk, sh);
+        account(a, bk, sm.task[s], epoch);
     }
-    if (lane == 0) {
-        check_books(a, sm, bk);
-        // booked: the next phase's first fills take these stages back again
-        for (int q = 0; q < kRing; ++q) sm.task[q].type = T_END;
-        __threadfence_block();
-        st_vol(&sm.prod_done, 1);
-    }
-    __syncwarp();
     return true;
 }
 
-// Take stage fill % kRing back from the consumers and fill it with task t
-// (the whole producer warp; lane 0 issues).  A T_END task carries no copy:
-// it ends the consumers' phase.  On a wait that gives up, lets the copies in
-// flight land and returns false.
-__device__ bool issue_fill(const VerifyArgs &a, VSmem &sm, uint8_t *ring, const TaskInfo &t,
-                           int fill, int lane, Books &bk, const StreamShape &sh) {
-    const int s = fill % kRing;
-    if (fill >= kRing) {
-        int w = 1;
-        if (lane == 0) w = mbar_wait_bounded(&sm.empty[s], ((fill / kRing) - 1) & 1, a.wait_ns);
-        if (!__shfl_sync(0xffffffffu, w, 0)) {
-            if (lane == 0) atomicOr(a.status, kStatusWaitTimeout);
-            drain_copies(sm, fill, lane);
-            return false;
-        }
-        if (lane == 0) book_stage(a, sm, sm.task[s], bk, sh);
-    }
-    if (lane == 0) {
-        sm.task[s] = t;
-        uint64_t *bar = &sm.full[s];
-        if (t.type == T_END) {
-            mbar_arrive(bar);
-        } else {
-            uint8_t *dst = ring + s * kStageBytes;
-            const char *tsrc = static_cast<const char *>(a.target_logits) +
-                               size_t(t.r) * a.row_bytes + size_t(t.y0) * a.elem_bytes;
-            mbar_arrive_expect_tx(bar, uint32_t(t.bytes) * (t.pair ? 2u : 1u) + uint32_t(t.bytes2));
-            bulk_g2s(dst, tsrc, uint32_t(t.bytes), bar);
-            if (t.pair) {
-                const char *dsrc = static_cast<const char *>(a.draft_logits) +
-                                   (size_t(t.b) * a.gamma + t.k) * size_t(a.row_bytes) +
-                                   size_t(t.y0) * a.elem_bytes;
-                bulk_g2s(dst + kChunkBytes, dsrc, uint32_t(t.bytes), bar);
-            } else if (t.bytes2 > 0) {
-                bulk_g2s(dst + kChunkBytes, tsrc + kChunkBytes, uint32_t(t.bytes2), bar);
-            }
-        }
-    }
-    __syncwarp();
-    return true;
-}
-
-// Phase 1: decision and bonus chunks.  Returns the index of the next fill.
-__device__ int producer_stream(const VerifyArgs &a, VSmem &sm, uint8_t *ring,
-                               const StreamShape &sh, int epoch, int lane, bool &ok) {
-    Books bk{0, 0, 0};
-    Chunk nx;
-    nx.stage = 0;
-    nx.c = 0;
-    nx.d = 0;
-    int cr = 0, cg = 0, cb = 0, ck = 0, cLb = 0, cd = -1, cj = 0, cj_end = 0, cq = 0;
-    float cu = 0.f;
+__device__ void producer(const VerifyArgs &a, VSmem &sm, uint8_t *ring, const StreamShape &sh,
+                         int epoch) {
+    ChunkFetch nextc;
+    nextc.stage = 1;       // the first chunk is the CTA's own index; the counter
+    nextc.c = blockIdx.x;  // hands out the rest from gridDim.x on
+    int cr = 0, cg = 0, cb = 0, ck = 0, cLb = 0, cd = -1, cj = 0, cj_end = 0;
     bool in_chunk = false;
+    Books bk{-1, 0, 0, 0, 0, -1, 0, 0, 0, 0};
+    int booked = 0;
+    // Residual-tile queue, polled on every fourth fill: the values read at
+    // the end of a polling fill are used at the start of the next one, so a
+    // global load does not stall the issue of a copy while the stream runs
+    // (with free stages a fill is shorter than an L2 round trip).
+    int pending = -1;      // a claimed queue index
+    int pend_rdy = 0;      // its ready word, read four fills earlier
+    int2 pend_job = make_int2(0, 0);
+    int obs_head = 0, obs_tail = 0;
     for (int fill = 0;; ++fill) {
         TaskInfo t;
-        t.type = T_END;
-        if (!in_chunk && nx.stage != 5) {
-            while (nx.stage < 4) fetch_step(a, sh, nx, epoch, lane);
-            if (nx.stage == 4) {
-                cq = nx.q;
-                cr = nx.r;
-                cg = nx.g;
-                cb = nx.b;
-                ck = nx.k;
-                cLb = nx.Lb;
-                cd = nx.d;
-                cu = nx.u;
-                const int C = cq ? sh.CTQ : sh.CT;
+        t.type = T_EXIT;
+        bool have = false, ok = true;
+        const bool poll = (fill & 3) == 0;
+        // 1. residual tiles first
+        if (poll && pending >= 0 && pend_rdy == epoch) {
+            t = resid_task(a, pend_job);
+            pending = -1;
+            have = true;
+        } else if (poll && pending < 0 && obs_head < obs_tail) {
+            pending = atomicAdd(&a.q_ctr[QA_HEAD], 1);
+            pend_rdy = 0;
+        }
+        // 2. then the stream chunks
+        if (!have && !in_chunk) {
+            while (nextc.stage < 4) fetch_step(a, sh, nextc, epoch);
+            if (nextc.stage == 4) {
+                cr = nextc.r;
+                cg = nextc.g;
+                cb = nextc.b;
+                ck = nextc.k;
+                cLb = nextc.Lb;
+                cd = nextc.d;
+                const int C = nextc.q ? sh.CbQ : cr < sh.nA ? a.nc : cr < sh.nB ? sh.Cb : 1;
                 cj = cg * C;
                 cj_end = min(a.nc, cj + C);
                 in_chunk = true;
-                nx.stage = 0;
+                nextc.stage = 0;
             }
         }
-        if (in_chunk) {
+        if (!have && in_chunk) {
             t.type = T_STREAM;
             t.r = cr;
             t.g = cg;
@@ -559,10 +499,8 @@ __device__ int producer_stream(const VerifyArgs &a, VSmem &sm, uint8_t *ring,
             t.k = ck;
             t.Lb = cLb;
             t.d = cd;
-            t.u_tok = cu;
-            t.mode = 0;
             t.j = cj;
-            t.pair = !a.greedy && !cq;
+            t.pair = !a.greedy && ck < cLb;
             t.y0 = cj * a.chunk_elems;
             t.bytes = min(kChunkBytes, a.row_bytes - cj * kChunkBytes);
             // a target-only row (greedy, or a bonus row) carries its next tile
@@ -573,97 +511,89 @@ __device__ int producer_stream(const VerifyArgs &a, VSmem &sm, uint8_t *ring,
             t.flush = cj + ntile == cj_end;
             cj += ntile;
             if (cj == cj_end) in_chunk = false;
+            have = true;
         }
-        if (!issue_fill(a, sm, ring, t, fill, lane, bk, sh)) {
-            ok = false;
-            return fill;
+        // keep the next chunk coming; with many tiles of this chunk left, one
+        // fetch stage every fourth fill, so its loads are back before use
+        if (nextc.stage < 4 && (!in_chunk || cj_end - cj < 10 || (fill & 3) == 0))
+            fetch_step(a, sh, nextc, epoch);
+        // 3. nothing of our own left: book everything, then serve the
+        //    residual queue until every request has finished
+        if (!have) {
+            ok = reclaim(a, sm, bk, booked, fill, epoch);
+            flush_books(a, bk, epoch);
+            check_books(a, bk, epoch);
+            if (pending < 0) pending = atomicAdd(&a.q_ctr[QA_HEAD], 1);
+            const uint64_t t0 = global_timer_ns();
+            unsigned ns = 32;
+            while (ok) {
+                if (pending < a.qcap && ld_acquire(&a.q_ready[pending]) == epoch) {
+                    t = resid_task(a, __ldcg(a.q_job + pending));
+                    pending = -1;
+                    have = true;
+                    break;
+                }
+                if (ld_acquire(&a.q_ctr[Q_FINISHED]) >= a.B) break;
+                if (global_timer_ns() - t0 > a.wait_ns) {
+                    atomicOr(a.status, kStatusQueueTimeout);
+                    break;
+                }
+                __nanosleep(ns);
+                ns = min(ns * 2, 256u);
+            }
         }
-        if (t.type == T_END) {
-            ok = finish_books(a, sm, fill, lane, bk, sh);
-            return fill + 1;
+        // 4. take the stage back (booking what it held) and fill it
+        const int s = fill % kStages;
+        if (ok) ok = reclaim(a, sm, bk, booked, fill - kStages + 1, epoch);
+        if (!ok) {
+            // A wait gave up: let every copy still in flight land (each is
+            // the only outstanding use of its stage) before the CTA can
+            // leave.  The consumers give up on their own waits.
+            for (int f = booked; f < fill; ++f)
+                mbar_wait_bounded(&sm.full[f % kStages], (f / kStages) & 1, kDrainTimeoutNs);
+            return;
         }
-        // one step towards the next chunk
-        if (nx.stage < 4) fetch_step(a, sh, nx, epoch, lane);
-    }
-}
-
-// Phase 2: the tiles of every rejected row pair, tile t = blockIdx.x + i *
-// gridDim.x of n_rej * nc.  Up to 32 tiles are located at once, one per lane
-// (request, its draw state and row).  Returns the index of the next fill.
-__device__ int producer_resid(const VerifyArgs &a, VSmem &sm, uint8_t *ring,
-                              const StreamShape &sh, int fill, int lane, bool &ok) {
-    Books bk{0, 0, 0};
-    const int n_rej = min(max(ld_relaxed(&a.q_ctr[Q_NREJ]), 0), a.B);
-    const int total = n_rej * a.nc;
-    for (int base = blockIdx.x; base < total; base += 32 * int(gridDim.x)) {
-        const int tl = base + lane * int(gridDim.x);
-        TaskInfo mine;
-        mine.type = T_END;
-        if (tl < total) {
-            const int rj = tl / a.nc;
-            const int b = min(max(__ldcg(a.rej_list + rj), 0), a.B - 1);
-            const DecideState st = load_state(a, b);
-            const int r0 = __ldcg(a.row_off + b);
-            mine.type = T_RESID;
-            mine.b = b;
-            mine.j = tl - rj * a.nc;
-            mine.k = min(max(st.a, 0), a.gamma - 1);
-            mine.r = min(max(r0 + mine.k, 0), sh.n_rows - 1);
-            mine.Lb = 0;
-            mine.g = 0;
-            mine.d = -1;
-            mine.flush = 0;
-            mine.pair = 1;
-            mine.y0 = mine.j * a.chunk_elems;
-            mine.bytes = min(kChunkBytes, a.row_bytes - mine.j * kChunkBytes);
-            mine.bytes2 = 0;
-            mine.Mp = st.Mp;
-            mine.Sp = st.Sp;
-            mine.Mq = st.Mq;
-            mine.Sq = st.Sq;
-            mine.mode = st.mode;
-            mine.u_tok = st.u_tok;
+        if (!have) t.type = T_EXIT;
+        sm.task[s] = t;
+        if (t.type == T_EXIT) {
+            mbar_arrive(&sm.full[s]);
+            return;
         }
-        const int n = min(32, (total - base + int(gridDim.x) - 1) / int(gridDim.x));
-        for (int l = 0; l < n; ++l, ++fill) {
-            TaskInfo t;
-            t.type = __shfl_sync(0xffffffffu, mine.type, l);
-            t.b = __shfl_sync(0xffffffffu, mine.b, l);
-            t.j = __shfl_sync(0xffffffffu, mine.j, l);
-            t.k = __shfl_sync(0xffffffffu, mine.k, l);
-            t.r = __shfl_sync(0xffffffffu, mine.r, l);
-            t.Lb = 0;
-            t.g = 0;
-            t.d = -1;
-            t.flush = 0;
-            t.pair = 1;
-            t.y0 = __shfl_sync(0xffffffffu, mine.y0, l);
-            t.bytes = __shfl_sync(0xffffffffu, mine.bytes, l);
-            t.bytes2 = 0;
-            t.Mp = __shfl_sync(0xffffffffu, mine.Mp, l);
-            t.Sp = __shfl_sync(0xffffffffu, mine.Sp, l);
-            t.Mq = __shfl_sync(0xffffffffu, mine.Mq, l);
-            t.Sq = __shfl_sync(0xffffffffu, mine.Sq, l);
-            t.mode = __shfl_sync(0xffffffffu, mine.mode, l);
-            t.u_tok = __shfl_sync(0xffffffffu, mine.u_tok, l);
-            if (!issue_fill(a, sm, ring, t, fill, lane, bk, sh)) {
-                ok = false;
-                return fill;
+        uint8_t *dst = ring + s * kStageBytes;
+        uint64_t *bar = &sm.full[s];
+        const char *tsrc = static_cast<const char *>(a.target_logits) +
+                           size_t(t.r) * a.row_bytes + size_t(t.y0) * a.elem_bytes;
+        mbar_arrive_expect_tx(bar, uint32_t(t.bytes) * (t.pair ? 2u : 1u) + uint32_t(t.bytes2));
+        bulk_g2s(dst, tsrc, uint32_t(t.bytes), bar);
+        if (t.pair) {
+            const char *dsrc = static_cast<const char *>(a.draft_logits) +
+                               (size_t(t.b) * a.gamma + t.k) * size_t(a.row_bytes) +
+                               size_t(t.y0) * a.elem_bytes;
+            bulk_g2s(dst + kChunkBytes, dsrc, uint32_t(t.bytes), bar);
+        } else if (t.bytes2 > 0) {
+            bulk_g2s(dst + kChunkBytes, tsrc + kChunkBytes, uint32_t(t.bytes2), bar);
+        }
+        // 5. act on the count published last, then book whatever has already
+        //    come back, without waiting
+        check_books(a, bk, epoch);
+        while (booked < fill && mbar_test_wait(&sm.empty[booked % kStages], (booked / kStages) & 1)) {
+            account(a, bk, sm.task[booked % kStages], epoch);
+            ++booked;
+        }
+        // 6. look at the residual queue for the next polling fill
+        if (poll) {
+            obs_head = ld_relaxed(&a.q_ctr[QA_HEAD]);
+            obs_tail = ld_relaxed(&a.q_ctr[QA_TAIL]);
+            if (pending >= 0 && pending < a.qcap) {
+                pend_rdy = ld_acquire(&a.q_ready[pending]);
+                pend_job = __ldcg(a.q_job + pending);
             }
         }
     }
-    TaskInfo t;
-    t.type = T_END;
-    if (!issue_fill(a, sm, ring, t, fill, lane, bk, sh)) {
-        ok = false;
-        return fill;
-    }
-    ok = finish_books(a, sm, fill, lane, bk, sh);
-    return fill + 1;
 }
 
 // ---------------------------------------------------------------------------
-// decisions and draws (warp-level)
+// decisions (warp-level)
 // ---------------------------------------------------------------------------
 // Draft tokens d_{b, lane} and d_{b, lane + 32} of a request, loaded once per
 // decision (gamma <= 64).
@@ -697,65 +627,52 @@ __device__ void finish_request(const VerifyArgs &a, int b, int acc, int token, c
         a.accept_len[b] = acc;
         a.num_emitted[b] = acc + 1;
         if (a.seq_lens_commit) a.seq_lens_commit[b] += acc + 1;
+        a.req_cnt[b] = 0;
+        a.r1_cnt[b] = 0;
     }
+    __threadfence();
     __syncwarp();
+    if (lane == 0) atomicAdd(&a.q_ctr[Q_FINISHED], 1);
 }
 
-// ---------------------------------------------------------------------------
-// The two-level draw.  It runs once per request, latency-bound, on code that
-// is cold in every SM when phase 3 starts, so it is kept compact: each block's
-// mass is formed once by the lane that owns the block, one scan chooses the
-// block, one the slot, and one vector's weights are formed a second time.
-// ---------------------------------------------------------------------------
-// What a slot record holds for a draw: the (max, sum) pair of p over the slot
-// (a bonus row; the mass at the row's maximum M), the slot's residual mass,
-// or its mass of p at the rejected row's own maximum.
-enum : int { K_BONUS = 0, K_RESID = 1, K_P = 2 };
-
-__device__ __forceinline__ float slot_mass(float2 x, int kind, float M, float scale) {
-    if (kind == K_BONUS) return x.y > 0.f ? x.y * exp2_approx((x.x - M) * scale) : 0.f;
-    return kind == K_RESID ? x.x : x.y;
+// Choose a sampling block: the smallest i whose running mass exceeds
+// u * total; the last block with positive mass if rounding leaves no
+// crossing.  mass(i) is evaluated by the lane that owns i.
+template <typename F>
+__device__ int choose_block(int nblk, float u, F mass, int lane) {
+    F2 total = f2(0.f);
+    for (int t0 = 0; t0 < nblk; t0 += 32) {
+        const int i = t0 + lane;
+        total = total + warp_sum_f2(i < nblk ? mass(i) : f2(0.f));
+    }
+    const F2 target = f2_scale(total, u);
+    F2 run = f2(0.f);
+    int last_pos = 0;
+    for (int t0 = 0; t0 < nblk; t0 += 32) {
+        const int i = t0 + lane;
+        const F2 v = i < nblk ? mass(i) : f2(0.f);
+        const F2 incl = run + warp_scan_incl(v, lane);
+        const unsigned hit = __ballot_sync(0xffffffffu, i < nblk && f2_gt(incl, target));
+        if (hit) return t0 + __ffs(hit) - 1;
+        const unsigned pos = __ballot_sync(0xffffffffu, i < nblk && v.hi > 0.f);
+        if (pos) last_pos = t0 + 31 - __clz(pos);
+        run = f2_shfl(incl, 31);
+    }
+    return last_pos;
 }
 
-// Mass of sampling block i: the two-float sum of its wpb slots.
-__device__ __noinline__ F2 block_mass(const float2 *rec, int i, int wpb, int kind, float M,
-                                      float scale) {
-    float2 x[kCW];
-#pragma unroll
-    for (int w = 0; w < kCW; ++w)
-        x[w] = w < wpb ? __ldcg(rec + size_t(i) * kCW + w) : make_float2(0.f, 0.f);
-    F2 m = f2(0.f);
-#pragma unroll
-    for (int w = 0; w < kCW; ++w)
-        if (w < wpb) m = m + f2(slot_mass(x[w], kind, M, scale));
-    return m;
-}
-
-// The smallest index whose running mass exceeds `target` among the 32 lane
-// values v (running sum `run` before them); -1 if none.  *last becomes the
-// last index with positive mass seen so far, *run the running sum after them.
-__device__ __forceinline__ int scan_pick(F2 v, bool live, F2 target, F2 &run, int base,
-                                         int &last, int lane) {
-    const F2 incl = run + warp_scan_incl(v, lane);
-    const unsigned hit = __ballot_sync(0xffffffffu, live && f2_gt(incl, target));
-    const unsigned pos = __ballot_sync(0xffffffffu, live && v.hi > 0.f);
-    if (pos) last = base + 31 - __clz(pos);
-    run = f2_shfl(incl, 31);
-    return hit ? base + __ffs(hit) - 1 : -1;
-}
-
-// Draw weights of one 16-byte vector: p's unnormalised 2^((z - Mp) s) (a draw
-// from p), or the normalised residual max(0, p - q).
+// Draw weights of the VE elements of 16-byte vector v: 2^((z - Mp) s) for a
+// draw from p (bonus, fallback); max(0, p - q) for the residual.
 template <typename T>
-__device__ __forceinline__ void vec_weights(const uint4 &xv, const uint4 &yv, bool resid, float Mp,
-                                            float iSp, float Mq, float iSq, float scale,
-                                            float (&w)[Vec<T>::kElems]) {
+__device__ __forceinline__ void draw_weights(const uint4 *tv, const uint4 *dv, int v, int mode,
+                                             float Mp, float iSp, float Mq, float iSq,
+                                             float scale, float (&w)[Vec<T>::kElems]) {
     constexpr int VE = Vec<T>::kElems;
     float x[VE];
-    Vec<T>::unpack(xv, x);
-    if (resid) {
+    Vec<T>::unpack(__ldcg(tv + v), x);
+    if (mode == D_RESID) {
         float y[VE];
-        Vec<T>::unpack(yv, y);
+        Vec<T>::unpack(__ldcg(dv + v), y);
 #pragma unroll
         for (int e = 0; e < VE; ++e)
             w[e] = fmaxf(0.f, exp2_approx((x[e] - Mp) * scale) * iSp -
@@ -778,49 +695,57 @@ __device__ __forceinline__ float pair_sum(const float (&w)[VE]) {
     return t[0];
 }
 
-// The token of a draw inside one slot -- the ids [y0, y0 + 32 * kRunVec * VE)
-// that one consumer warp covers in a tile: the smallest id whose running
-// weight, counted from the slot's start, exceeds `target`.  Each lane owns a
-// contiguous run of kRunVec vectors (one batch of loads); per-vector weights
-// are summed pairwise and kept; runs are combined in two-float sums; the lane
-// holding the crossing finds its vector from the kept sums and forms only that
-// vector's weights again.  If rounding leaves no crossing, the last id with
-// positive weight.
-// What the draw needs of the launch, passed by value (a few registers): an
-// out-of-line function taking the whole argument block by reference would
-// copy it to the stack.
-struct DrawCtx {
-    const char *tgt, *dft;  // target and draft logits
-    int row_bytes, gamma, nblk, chunk_elems;
-    float scale;
-};
-
-__device__ __forceinline__ DrawCtx draw_ctx(const VerifyArgs &a) {
-    return DrawCtx{static_cast<const char *>(a.target_logits),
-                   static_cast<const char *>(a.draft_logits), a.row_bytes, a.gamma, a.nblk,
-                   a.chunk_elems, a.scale};
-}
-
+// The token of a draw inside one slot -- the ids [y0, y0 + n) that one
+// consumer warp covers in a tile: the smallest id whose running weight,
+// counted from the slot's start, exceeds `target`.  Each lane owns a
+// contiguous run of n/32 ids (kRunVec 16-byte vectors, one batch of loads);
+// per-vector weights are summed pairwise and kept in registers; runs are
+// combined in two-float sums; the lane holding the crossing finds its vector from the
+// kept sums and reloads only that vector.  If rounding leaves no crossing,
+// the last id with positive weight.  The rows were streamed moments
+// earlier, so the loads hit L2.
 template <typename T>
-__device__ int slot_pick(const DrawCtx &a, const uint4 *tv, const uint4 *dv, bool resid,
-                         int y0, F2 target, float Mp, float iSp, float Mq, float iSq, int lane) {
+__device__ int slot_pick(const VerifyArgs &a, const DecideState &st, int b, int r, int y0, int n,
+                         F2 target, int lane) {
     constexpr int VE = Vec<T>::kElems;
-    constexpr int kRunVec = 4;  // 32 lanes x 4 vectors: one warp's slot of a tile
-    const int v_end = a.row_bytes / 16;
+    constexpr int kRunVec = 4;  // n = 32 lanes x 4 vectors (1024 bf16 / 512 fp32 ids)
+    const uint4 *tv = reinterpret_cast<const uint4 *>(static_cast<const char *>(a.target_logits) +
+                                                      size_t(r) * a.row_bytes);
+    const uint4 *dv = reinterpret_cast<const uint4 *>(
+        static_cast<const char *>(a.draft_logits) + (size_t(b) * a.gamma + st.a) * a.row_bytes);
+    const int v_end = min(a.row_bytes / 16, (y0 + n) / VE);
+    const float scale = a.scale, iSp = 1.f / st.Sp, iSq = 1.f / st.Sq;
+    const bool resid = st.mode == D_RESID;
     const int v0 = y0 / VE + lane * kRunVec;
+    auto weights = [&](const uint4 &xv, const uint4 &yv, float (&w)[VE]) {
+        float x[VE];
+        Vec<T>::unpack(xv, x);
+        if (resid) {
+            float y[VE];
+            Vec<T>::unpack(yv, y);
+#pragma unroll
+            for (int e = 0; e < VE; ++e)
+                w[e] = fmaxf(0.f, exp2_approx((x[e] - st.Mp) * scale) * iSp -
+                                      exp2_approx((y[e] - st.Mq) * scale) * iSq);
+        } else {
+#pragma unroll
+            for (int e = 0; e < VE; ++e) w[e] = exp2_approx((x[e] - st.Mp) * scale);
+        }
+    };
     uint4 xv[kRunVec], yv[kRunVec];
 #pragma unroll
     for (int q = 0; q < kRunVec; ++q) {
-        const bool in = v0 + q < v_end;
-        xv[q] = in ? __ldcg(tv + v0 + q) : make_uint4(0, 0, 0, 0);
-        yv[q] = in && resid ? __ldcg(dv + v0 + q) : make_uint4(0, 0, 0, 0);
+        const int v = v0 + q;
+        const bool in = v < v_end;
+        xv[q] = in ? __ldcg(tv + v) : make_uint4(0, 0, 0, 0);
+        yv[q] = in && resid ? __ldcg(dv + v) : make_uint4(0, 0, 0, 0);
     }
     float vs[kRunVec];
     float ls = 0.f;
 #pragma unroll
     for (int q = 0; q < kRunVec; ++q) {
         float w[VE];
-        vec_weights<T>(xv[q], yv[q], resid, Mp, iSp, Mq, iSq, a.scale, w);
+        weights(xv[q], yv[q], w);
         vs[q] = v0 + q < v_end ? pair_sum<VE>(w) : 0.f;
         ls += vs[q];
     }
@@ -845,23 +770,20 @@ __device__ int slot_pick(const DrawCtx &a, const uint4 *tv, const uint4 *dv, boo
             run += vs[q];
         }
         if (qsel < 0) qsel = qlast;
-        uint4 xs = xv[0], ys = yv[0];
-#pragma unroll
-        for (int q = 1; q < kRunVec; ++q)
-            if (q == qsel) {
-                xs = xv[q];
-                ys = yv[q];
-            }
-        float w[VE];
-        vec_weights<T>(xs, ys, resid, Mp, iSp, Mq, iSq, a.scale, w);
-        float re = run_at;
         int lastpos = -1;
 #pragma unroll
-        for (int e = 0; e < VE; ++e) {
-            re += w[e];
-            if (pick < 0 && w[e] > 0.f) {
-                lastpos = (v0 + qsel) * VE + e;
-                if (f2_gt(excl + f2(re), target)) pick = (v0 + qsel) * VE + e;
+        for (int q = 0; q < kRunVec; ++q) {
+            if (q != qsel) continue;
+            float w[VE];
+            weights(xv[q], yv[q], w);
+            float re = run_at;
+#pragma unroll
+            for (int e = 0; e < VE; ++e) {
+                re += w[e];
+                if (pick < 0 && w[e] > 0.f) {
+                    lastpos = (v0 + q) * VE + e;
+                    if (f2_gt(excl + f2(re), target)) pick = (v0 + q) * VE + e;
+                }
             }
         }
         if (pick < 0) pick = lastpos >= 0 ? lastpos : v0 * VE;
@@ -869,121 +791,158 @@ __device__ int slot_pick(const DrawCtx &a, const uint4 *tv, const uint4 *dv, boo
     return __shfl_sync(0xffffffffu, pick, lsel);
 }
 
-// The two-level draw of request b from the slot records `rec` ([nblk][kCW]):
-// the smallest block whose running mass exceeds u_blk times the total, then
-// within it the smallest slot whose running mass exceeds u_tok times the
-// block's, then the id inside the slot (slot_pick).  Weights are p at target
-// row r (K_BONUS: its maximum is taken from the records; K_P: Mp), or the
-// residual of row r against draft row (b, dk) (K_RESID; a zero residual mass
-// falls back to p of the same row).  The rows were streamed moments earlier.
+// The token inside sampling block `blk` of packed target row r, given the
+// block's per-warp slot masses sm_w (w < wpb, in every lane): the slot whose
+// running mass crosses u_tok times the block mass, then the id inside it.
 template <typename T>
-__device__ __noinline__ int draw_token(const DrawCtx a, int b, int r, int dk, int kind,
-                                       const float2 *rec, float Mp, float Sp, float Mq, float Sq,
-                                       float u_blk, float u_tok, int lane) {
-    const int tpw = a.chunk_elems / kCW;
-    const int wpb = kSampleBlock / tpw;
-    const float scale = a.scale;
-    float M = Mp;
-    if (kind == K_BONUS) {
-        float mb = -INFINITY;
-#pragma unroll 1
-        for (int i = lane; i < a.nblk; i += 32) {
-            float2 x[kCW];
+__device__ int block_pick(const VerifyArgs &a, const DecideState &st, int b, int r, int blk,
+                          const float (&slot_mass)[kCW], int wpb, int tpw, int lane) {
+    F2 total = f2(0.f);
 #pragma unroll
-            for (int w = 0; w < kCW; ++w)
-                x[w] = w < wpb ? __ldcg(rec + size_t(i) * kCW + w) : make_float2(0.f, 0.f);
+    for (int w = 0; w < kCW; ++w)
+        if (w < wpb) total = total + f2(slot_mass[w]);
+    const F2 target = f2_scale(total, st.u_tok);
+    F2 cum = f2(0.f), before = f2(0.f);
+    int wsel = -1, wlast = 0;
 #pragma unroll
-            for (int w = 0; w < kCW; ++w)
-                if (w < wpb && x[w].y > 0.f) mb = fmaxf(mb, x[w].x);
+    for (int w = 0; w < kCW; ++w) {
+        if (w >= wpb || wsel >= 0) continue;
+        if (slot_mass[w] > 0.f) {
+            wlast = w;
+            if (f2_gt(cum + f2(slot_mass[w]), target)) {
+                wsel = w;
+                before = cum;
+            }
         }
-        M = warp_max(mb);
+        cum = cum + f2(slot_mass[w]);
     }
-    // Block masses (two blocks per lane kept for nblk <= 64) and their total.
-    F2 keep0 = f2(0.f), keep1 = f2(0.f), total = f2(0.f);
-#pragma unroll 1
-    for (int pass = 0; pass < 2; ++pass) {
-        total = f2(0.f);
-#pragma unroll 1
-        for (int t0 = 0; t0 < a.nblk; t0 += 32) {
-            const int i = t0 + lane;
-            const F2 m = i < a.nblk ? block_mass(rec, i, wpb, kind, M, scale) : f2(0.f);
-            if (t0 == 0) keep0 = m;
-            else if (t0 == 32) keep1 = m;
-            total = total + warp_sum_f2(m);
-        }
-        if (kind != K_RESID || total.hi > 0.f) break;
-        kind = K_P;  // no residual mass: draw from p of the same row
+    if (wsel < 0) {
+        wsel = wlast;
+        before = f2(0.f);
+#pragma unroll
+        for (int w = 0; w < kCW; ++w)
+            if (w < wsel) before = before + f2(slot_mass[w]);
     }
-    // The block.
-    F2 target = f2_scale(total, u_blk), run = f2(0.f);
-    int blk = -1, last = 0;
-#pragma unroll 1
-    for (int t0 = 0; t0 < a.nblk && blk < 0; t0 += 32) {
-        const int i = t0 + lane;
-        const F2 m = t0 == 0 ? keep0 : t0 == 32 ? keep1
-                   : (i < a.nblk ? block_mass(rec, i, wpb, kind, M, scale) : f2(0.f));
-        blk = scan_pick(m, i < a.nblk, target, run, t0, last, lane);
-    }
-    if (blk < 0) blk = last;
-    // The slot within it: lane w holds slot w's mass.
-    const float sm = lane < wpb ? slot_mass(__ldcg(rec + size_t(blk) * kCW + lane), kind, M, scale)
-                                : 0.f;
-    F2 bm = warp_sum_f2(f2(sm));
-    target = f2_scale(bm, u_tok);
-    run = f2(0.f);
-    int wl = 0;
-    int w = scan_pick(f2(sm), lane < wpb, target, run, 0, wl, lane);
-    if (w < 0) w = wl;
-    const F2 before = f2_shfl(f2_shfl_up(warp_scan_incl(f2(sm), lane), 1), w);
-    const F2 inside = w > 0 ? target - before : target;
-    // The token.
-    const bool resid = kind == K_RESID;
-    const uint4 *tv = reinterpret_cast<const uint4 *>(a.tgt + size_t(r) * a.row_bytes);
-    const uint4 *dv = reinterpret_cast<const uint4 *>(
-        resid ? a.dft + (size_t(b) * a.gamma + dk) * a.row_bytes : a.tgt);
-    return slot_pick<T>(a, tv, dv, resid, blk * kSampleBlock + w * tpw, inside, M,
-                        resid ? 1.f / Sp : 1.f, Mq, resid ? 1.f / Sq : 1.f, lane);
+    return slot_pick<T>(a, st, b, r, blk * kSampleBlock + wsel * tpw, tpw, target - before, lane);
+}
+
+// (max, sum) of p over sampling block i of request b's bonus row, from the
+// per-warp slots.
+__device__ __forceinline__ float2 bonus_block(const VerifyArgs &a, int b, int i, int wpb,
+                                              float scale) {
+    const float2 *sl = a.blkrec + (size_t(b) * a.nblk + i) * kCW;
+    float2 x[kCW];
+#pragma unroll
+    for (int w = 0; w < kCW; ++w) x[w] = w < wpb ? __ldcg(sl + w) : make_float2(-INFINITY, 0.f);
+    float m = -INFINITY, s = 0.f;
+#pragma unroll
+    for (int w = 0; w < kCW; ++w) ms_combine(m, s, x[w].x, x[w].y, scale);
+    return make_float2(m, s);
 }
 
 // The bonus draw of request b, every draft accepted: from p of row L_b
 // (sampling; block and slot masses from the row's per-warp slots), or the
 // argmax of row L_b (greedy; from its chunk records).
 template <typename T>
-__device__ void bonus_draw(const VerifyArgs &a, const StreamShape &sh, int b, int lane) {
+__device__ void bonus_draw(const VerifyArgs &a, const StreamShape &sh, int b, int wpb, int lane) {
     const int Lb = verify_len(a, b), r = a.row_off[b] + Lb;
     const Drafts dr = load_drafts(a, b, lane);
-    int token;
     if (a.greedy) {
         float v = -INFINITY;
         int id = INT_MAX;
         const float4 *rec = a.rowrec + size_t(r) * a.grp_stride;
-        for (int g = lane; g < sh.cprQ; g += 32) {
+        for (int g = lane; g < sh.gprbQ; g += 32) {
             const float4 x = __ldcg(rec + g);
             am_combine(v, id, x.x, __float_as_int(x.y));
         }
         warp_am_reduce(v, id);
-        token = id;
-    } else {
-        const float3 un = uniforms_of(a.seed, b, Lb);
-        token = draw_token<T>(draw_ctx(a), b, r, 0, K_BONUS, a.blkrec + size_t(b) * a.nblk * kCW,
-                              0.f, 1.f, 0.f, 1.f, un.y, un.z, lane);
+        finish_request(a, b, Lb, id, dr, lane);
+        return;
     }
+    const float scale = a.scale;
+    constexpr int kCache = 2;  // blocks per lane kept in registers (nblk <= 64)
+    float2 sl[kCache][kCW];
+#pragma unroll
+    for (int q = 0; q < kCache; ++q) {
+        const int i = q * 32 + lane;
+        const float2 *p = a.blkrec + (size_t(b) * a.nblk + (i < a.nblk ? i : 0)) * kCW;
+#pragma unroll
+        for (int w = 0; w < kCW; ++w)
+            sl[q][w] = i < a.nblk && w < wpb ? __ldcg(p + w) : make_float2(-INFINITY, 0.f);
+    }
+    float u, ub, ut;
+    step_uniforms(a.seed, b, Lb, u, ub, ut);
+    float mb = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < kCache; ++q)
+#pragma unroll
+        for (int w = 0; w < kCW; ++w)
+            if (sl[q][w].y > 0.f) mb = fmaxf(mb, sl[q][w].x);
+    for (int i = kCache * 32 + lane; i < a.nblk; i += 32) {
+        const float2 x = bonus_block(a, b, i, wpb, scale);
+        if (x.y > 0.f) mb = fmaxf(mb, x.x);
+    }
+    const float M = warp_max(mb);
+    // slot mass in the units of 2^((z - M) s)
+    auto smass = [&](float2 x) { return x.y > 0.f ? x.y * exp2_approx((x.x - M) * scale) : 0.f; };
+    auto mass = [&](int i) {
+        const int q = i >> 5;
+        F2 m = f2(0.f);
+        if (q < kCache) {
+#pragma unroll
+            for (int c = 0; c < kCache; ++c)
+                if (q == c)
+#pragma unroll
+                    for (int w = 0; w < kCW; ++w) m = m + f2(smass(sl[c][w]));
+        } else {
+            const float2 *p = a.blkrec + (size_t(b) * a.nblk + i) * kCW;
+            for (int w = 0; w < wpb; ++w) m = m + f2(smass(__ldcg(p + w)));
+        }
+        return m;
+    };
+    const int blk = choose_block(a.nblk, ub, mass, lane);
+    float slot_mass[kCW];
+    {
+        const int q = blk >> 5, owner = blk & 31;
+#pragma unroll
+        for (int w = 0; w < kCW; ++w) {
+            float m = 0.f;
+            if (q < kCache) {
+#pragma unroll
+                for (int c = 0; c < kCache; ++c)
+                    if (q == c) m = smass(sl[c][w]);
+                m = __shfl_sync(0xffffffffu, m, owner);
+            } else if (w < wpb) {
+                m = smass(__ldcg(a.blkrec + (size_t(b) * a.nblk + blk) * kCW + w));
+            }
+            slot_mass[w] = w < wpb ? m : 0.f;
+        }
+    }
+    DecideState st;
+    st.a = Lb;
+    st.mode = D_BONUS;
+    st.Mp = M;
+    st.Sp = 1.f;
+    st.Mq = 0.f;
+    st.Sq = 1.f;
+    st.u_blk = ub;
+    st.u_tok = ut;
+    const int token = block_pick<T>(a, st, b, r, blk, slot_mass, wpb, kSampleBlock / wpb, lane);
     finish_request(a, b, Lb, token, dr, lane);
 }
 
 // Request b's decision rows (k < L_b) are all in: accept tests and outputs
-// of the draft rows.  A rejection lists the request for the residual pass
-// (sampling) or emits the row's argmax (greedy); with every draft accepted
-// the bonus draw is due once the bonus row is in too: returns true when this
-// call completes that join.  Loads that do not depend on one another are issued together: a
-// decision runs while the streaming keeps L2 busy, and each dependent round
-// trip costs microseconds.
+// of the draft rows.  A rejection starts the residual draw (sampling) or
+// emits the row's argmax (greedy) and marks the request so its bonus row is
+// not streamed; with every draft accepted the bonus draw runs once the bonus
+// row is in too (join counter: whichever comes second runs it).  Loads that
+// do not depend on one another are issued together: a decision runs while
+// the streaming keeps L2 busy, and each dependent round trip costs
+// microseconds.
 template <typename T>
-__device__ bool decide_request(const VerifyArgs &a, const StreamShape &sh, int b, int wpb,
+__device__ void decide_request(const VerifyArgs &a, const StreamShape &sh, int b, int wpb,
                                int epoch, int lane) {
-    // Round 1: lengths, offsets and draft tokens.  The request's count is
-    // complete: reset it for the next launch.
-    if (lane == 0) a.req_cnt[b] = 0;
+    // Round 1: lengths, offsets and draft tokens.
     const int Lb = verify_len(a, b), r0 = a.row_off[b], d0 = a.draft_off[b];
     // Committed window: L_b, or in the cap-accept audit the scheduled W_b
     // clamped to [0, L_b] (the full block is verified, the window committed).
@@ -1003,32 +962,26 @@ __device__ bool decide_request(const VerifyArgs &a, const StreamShape &sh, int b
         const int k = base + lane;
         const bool live = k < Lb;
         const int r = r0 + k;
-        const int nrec = sh.cpr;
+        const int nrec = r < sh.nA ? 1 : r < sh.nB ? sh.gprb : a.nc;
         const float4 *rec = a.rowrec + size_t(live ? r : r0) * a.grp_stride;
-        constexpr int kRecBatch = 8;  // records per round of loads
-        float4 x[kRecBatch];
+        float4 x[4];
 #pragma unroll
-        for (int u = 0; u < kRecBatch; ++u)
+        for (int u = 0; u < 4; ++u)
             x[u] = live && u < nrec ? __ldcg(rec + u) : make_float4(0.f, 0.f, 0.f, 0.f);
         const float2 z = !a.greedy && live ? __ldcg(a.gath + r) : make_float2(0.f, 0.f);
         float u = 1.f, u1 = 0.f, u2 = 0.f;
-        if (!a.greedy && live) {
-            const float3 un = uniforms_of(a.seed, b, k);
-            u = un.x;
-            u1 = un.y;
-            u2 = un.z;
-        }
+        if (!a.greedy && live) step_uniforms(a.seed, b, k, u, u1, u2);
         float4 rr = a.greedy ? make_float4(-INFINITY, __int_as_float(INT_MAX), 0.f, 0.f)
                              : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
         if (live) {
-            for (int i0 = 0; i0 < nrec; i0 += kRecBatch) {
+            for (int i0 = 0; i0 < nrec; i0 += 4) {
                 if (i0 > 0) {
 #pragma unroll
-                    for (int v = 0; v < kRecBatch; ++v)
+                    for (int v = 0; v < 4; ++v)
                         if (i0 + v < nrec) x[v] = __ldcg(rec + i0 + v);
                 }
 #pragma unroll
-                for (int v = 0; v < kRecBatch; ++v) {
+                for (int v = 0; v < 4; ++v) {
                     if (i0 + v >= nrec) continue;
                     if (a.greedy) {
                         int bi = __float_as_int(rr.y);
@@ -1089,10 +1042,10 @@ __device__ bool decide_request(const VerifyArgs &a, const StreamShape &sh, int b
         // A rejection inside the window (residual draw at row a_b), or a
         // window that ends inside the accepted run (draw from p at row W,
         // what compact's bonus draw would be).  The bonus row is not needed.
+        if (lane == 0) st_relaxed(&a.rejflag[b], epoch);  // phase Q skips the bonus row
         if (a.greedy) {
-            if (lane == 0) a.act[b] = A_NONE;
             finish_request(a, b, acc, g_tok, dr, lane);
-            return false;
+            return;
         }
         DecideState st;
         st.a = acc;
@@ -1105,46 +1058,99 @@ __device__ bool decide_request(const VerifyArgs &a, const StreamShape &sh, int b
         st.u_tok = ut;
         if (lane == 0) {
             a.dstate[b] = st;
-            a.act[b] = A_RESID;
-            a.rej_list[atomicAdd(&a.q_ctr[Q_NREJ], 1)] = b;
+            push_resid_jobs(a, b, epoch);
         }
-        return false;
+        return;
     }
-    // Every draft accepted: the bonus draw is due once the bonus row is in
-    // too (join counter: whichever comes second queues it).
+    // Every draft accepted: the bonus draw, if the bonus row is in already.
     int go = 0;
     if (lane == 0) {
-        a.act[b] = A_BONUS;
         __threadfence();
         go = atomicAdd(&a.join[b], 1) == 1;
     }
-    return __shfl_sync(0xffffffffu, go, 0);
+    if (__shfl_sync(0xffffffffu, go, 0)) {
+        __threadfence();
+        bonus_draw<T>(a, sh, b, wpb, lane);
+    }
 }
 
-// The residual draw of a rejected request (or, for a cap-accept window cut
-// inside the accepted run, the draw from p at the window's row), from the
-// per-slot masses of the residual pass.
+// Every residual slot of request b is in: choose the block from the masses,
+// then the slot, then the token.
 template <typename T>
-__device__ void finish_residual(const VerifyArgs &a, int b, int lane) {
-    const DecideState st = load_state(a, b);
+__device__ void finish_residual(const VerifyArgs &a, int b, int wpb, int lane) {
+    // One round of independent loads: state, row offset, drafts, masses.
+    DecideState st = load_state(a, b);
     const int r0 = a.row_off[b];
     const Drafts dr = load_drafts(a, b, lane);
-    const int k = min(max(st.a, 0), a.gamma - 1);
-    if (lane == 0) a.r1_cnt[b] = 0;  // the count is complete: reset it for the next launch
-    const int token = draw_token<T>(draw_ctx(a), b, r0 + k, k, st.mode == D_RESID ? K_RESID : K_P,
-                                    a.zrec + size_t(b) * a.nblk * kCW, st.Mp, st.Sp, st.Mq, st.Sq,
-                                    st.u_blk, st.u_tok, lane);
+    const float2 *z = a.zrec + size_t(b) * a.nblk * kCW;
+    constexpr int kCache = 2;  // blocks per lane kept in registers (nblk <= 64)
+    float2 sl[kCache][kCW];
+#pragma unroll
+    for (int q = 0; q < kCache; ++q) {
+        const int i = q * 32 + lane;
+#pragma unroll
+        for (int w = 0; w < kCW; ++w)
+            sl[q][w] = i < a.nblk && w < wpb ? __ldcg(z + size_t(i) * kCW + w) : make_float2(0.f, 0.f);
+    }
+    auto mass = [&](int i, bool residual) {
+        const int q = i >> 5;
+        F2 m = f2(0.f);
+        if (q < kCache) {
+#pragma unroll
+            for (int c = 0; c < kCache; ++c)
+                if (q == c)
+#pragma unroll
+                    for (int w = 0; w < kCW; ++w) m = m + f2(residual ? sl[c][w].x : sl[c][w].y);
+        } else {
+            for (int w = 0; w < wpb; ++w) {
+                const float2 x = __ldcg(z + size_t(i) * kCW + w);
+                m = m + f2(residual ? x.x : x.y);
+            }
+        }
+        return m;
+    };
+    F2 total = f2(0.f);
+    for (int t0 = 0; t0 < a.nblk; t0 += 32) {
+        const int i = t0 + lane;
+        total = total + warp_sum_f2(i < a.nblk ? mass(i, true) : f2(0.f));
+    }
+    const bool residual = st.mode == D_RESID && total.hi > 0.f;
+    if (!residual) {
+        // A draw from p (window cut inside the accepted run), or no residual
+        // mass: draw from p of the same row.
+        st.mode = D_FALLBACK;
+        st.Sp = 1.f;
+    }
+    const int blk = choose_block(a.nblk, st.u_blk, [&](int i) { return mass(i, residual); }, lane);
+    float slot_mass[kCW];
+    {
+        const int q = blk >> 5, owner = blk & 31;
+#pragma unroll
+        for (int w = 0; w < kCW; ++w) {
+            float m = 0.f;
+            if (q < kCache) {
+#pragma unroll
+                for (int c = 0; c < kCache; ++c)
+                    if (q == c) m = residual ? sl[c][w].x : sl[c][w].y;
+                m = __shfl_sync(0xffffffffu, m, owner);
+            } else if (w < wpb) {
+                const float2 x = __ldcg(z + size_t(blk) * kCW + w);
+                m = residual ? x.x : x.y;
+            }
+            slot_mass[w] = w < wpb ? m : 0.f;
+        }
+    }
+    const int token =
+        block_pick<T>(a, st, b, r0 + st.a, blk, slot_mass, wpb, kSampleBlock / wpb, lane);
     finish_request(a, b, st.a, token, dr, lane);
 }
 
 // ---------------------------------------------------------------------------
-// consumers: warps 0 .. kCW-1
+// consumers
 // ---------------------------------------------------------------------------
-// Consumer warp of either streaming phase, from fill `fill`: returns the
-// index of the fill after the phase's end.
 template <typename T>
-__device__ int consumer(const VerifyArgs &a, VSmem &sm, const uint8_t *ring,
-                        const StreamShape &sh, int warp, int lane, int fill, int *fail) {
+__device__ void consumer(const VerifyArgs &a, VSmem &sm, const uint8_t *ring,
+                         const StreamShape &sh, int warp, int lane, int epoch) {
     constexpr int VE = Vec<T>::kElems;
     const float scale = a.scale;
     const int tpw = a.chunk_elems / kCW;  // tokens per warp in a tile
@@ -1154,27 +1160,18 @@ __device__ int consumer(const VerifyArgs &a, VSmem &sm, const uint8_t *ring,
     float mp = -INFINITY, sp = 0.f, mq = -INFINITY, sq = 0.f;
     float bv = -INFINITY;
     int bi = INT_MAX;
-    for (;; ++fill) {
-        const int s = fill % kRing, n = fill / kRing, par = n & 1;
+    for (int fill = 0;; ++fill) {
+        const int s = fill % kStages, n = fill / kStages;
         if (!mbar_wait_backoff(&sm.full[s], n & 1, a.wait_ns)) {
-            if (lane == 0) {
-                atomicOr(a.status, kStatusWaitTimeout);
-                atomicOr(fail, 1);
-            }
-            return fill;
+            if (lane == 0) atomicOr(a.status, kStatusWaitTimeout);
+            return;
         }
         const TaskInfo t = sm.task[s];
-        if (t.type == T_END) {
-            // the end of the phase: the stage goes back like any other
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.empty[s]);
-            return fill + 1;
-        }
+        if (t.type == T_EXIT) return;
         const uint4 *tv = reinterpret_cast<const uint4 *>(ring + s * kStageBytes);
         const uint4 *dv = tv + kChunkBytes / 16;
         const int nvec = t.bytes / 16;
         const int v0 = min(nvec, warp * vpw), v1 = min(nvec, v0 + vpw);
-        bool wrote = false;  // this warp wrote device memory another CTA will read
 
         if (t.type == T_STREAM) {
             if (a.greedy) {
@@ -1204,15 +1201,12 @@ __device__ int consumer(const VerifyArgs &a, VSmem &sm, const uint8_t *ring,
                 }
                 if (lane == 0) {
                     const int lo = t.y0 + v0 * VE, hi = t.y0 + v1 * VE;
-                    if (t.d >= lo && t.d < hi) {
+                    if (t.d >= lo && t.d < hi)
                         a.gath[t.r] = make_float2(Vec<T>::load1(tv, t.d - t.y0),
                                                   Vec<T>::load1(dv, t.d - t.y0));
-                        wrote = true;
-                    }
                 }
             } else {
-                // Bonus row: one (max, sum) slot per tile and warp -- the block
-                // and slot masses of its draw.
+                // Bonus row: one (max, sum) slot per tile and warp.
                 for (int h = 0; h < (t.bytes2 > 0 ? 2 : 1); ++h) {
                     const uint4 *xv = h ? dv : tv;
                     const int nv = (h ? t.bytes2 : t.bytes) / 16;
@@ -1226,72 +1220,54 @@ __device__ int consumer(const VerifyArgs &a, VSmem &sm, const uint8_t *ring,
                     warp_ms_reduce(bm, bs, scale);
                     const int y = t.y0 + h * a.chunk_elems + warp * tpw;
                     const int blk = y / kSampleBlock;
-                    if (lane == 0 && blk < a.nblk) {
+                    if (lane == 0 && blk < a.nblk)
                         a.blkrec[(size_t(t.b) * a.nblk + blk) * kCW + (y % kSampleBlock) / tpw] =
                             make_float2(bm, bs);
-                        wrote = true;
-                    }
                 }
             }
-            // The stage has been read: hand it back before the bookkeeping,
-            // except for the warp that writes a chunk's record (below).
-            __syncwarp();
-            if (!t.flush || !(a.greedy || t.pair)) {
-                if (lane == 0) {
-                    if (wrote) __threadfence();
-                    mbar_arrive(&sm.empty[s]);
-                }
-                continue;
-            }
-            // End of a chunk: the eight warp partials become one record of
-            // the row; the last warp writes it and only then releases the
-            // stage, so the producer books the chunk once the record is in.
-            {
-                // The eight warp partials become one record of the row.
-                float4 x;
+            if (t.flush && (a.greedy || t.pair)) {
+                // End of the chunk: the eight warp partials become one record.
                 if (a.greedy) {
                     warp_am_reduce(bv, bi);
-                    x = make_float4(bv, __int_as_float(bi), 0.f, 0.f);
+                    if (lane == 0) sm.part[s][warp] = make_float4(bv, __int_as_float(bi), 0.f, 0.f);
                 } else {
                     warp_ms_reduce(mp, sp, scale);
                     warp_ms_reduce(mq, sq, scale);
-                    x = make_float4(mp, sp, mq, sq);
+                    if (lane == 0) sm.part[s][warp] = make_float4(mp, sp, mq, sq);
                 }
                 mp = mq = bv = -INFINITY;
                 sp = sq = 0.f;
                 bi = INT_MAX;
                 int last = 0;
                 if (lane == 0) {
-                    sm.part[s][par][warp] = x;
-                    if (wrote) __threadfence();
-                    else __threadfence_block();
-                    last = atomicAdd(&sm.done[s][par], 1) == kCW - 1;
-                    if (!last) mbar_arrive(&sm.empty[s]);
+                    __threadfence_block();
+                    last = atomicAdd(&sm.done[s], 1) == kCW - 1;
                 }
                 if (__shfl_sync(0xffffffffu, last, 0)) {
                     __threadfence_block();
-                    float4 y = lane < kCW ? sm.part[s][par][lane]
+                    float4 x = lane < kCW ? sm.part[s][lane]
                                           : (a.greedy ? make_float4(-INFINITY, __int_as_float(INT_MAX), 0.f, 0.f)
                                                       : make_float4(-INFINITY, 0.f, -INFINITY, 0.f));
                     if (a.greedy) {
-                        int yi = __float_as_int(y.y);
-                        warp_am_reduce(y.x, yi);
-                        y.y = __int_as_float(yi);
+                        int xi = __float_as_int(x.y);
+                        warp_am_reduce(x.x, xi);
+                        x.y = __int_as_float(xi);
                     } else {
-                        warp_ms_reduce(y.x, y.y, scale);
-                        warp_ms_reduce(y.z, y.w, scale);
+                        warp_ms_reduce(x.x, x.y, scale);
+                        warp_ms_reduce(x.z, x.w, scale);
                     }
                     if (lane == 0) {
-                        sm.done[s][par] = 0;
-                        a.rowrec[size_t(t.r) * a.grp_stride + t.g] = y;
-                        mbar_arrive(&sm.empty[s]);  // release after the record
+                        sm.done[s] = 0;
+                        a.rowrec[size_t(t.r) * a.grp_stride + t.g] = x;
                     }
                 }
             }
             __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.empty[s]);
         } else {
             // Residual tile: this warp's share of the residual and p masses.
-            const float iSp = 1.f / t.Sp, iSq = 1.f / t.Sq;
+            const DecideState st = load_state(a, t.b);
+            const float iSp = 1.f / st.Sp, iSq = 1.f / st.Sq;
             float zr = 0.f, zp = 0.f;
             for (int v = v0 + lane; v < v1; v += 32) {
                 float x[VE], y[VE];
@@ -1299,278 +1275,89 @@ __device__ int consumer(const VerifyArgs &a, VSmem &sm, const uint8_t *ring,
                 Vec<T>::unpack(dv[v], y);
 #pragma unroll
                 for (int e = 0; e < VE; ++e) {
-                    const float pw = exp2_approx((x[e] - t.Mp) * scale);
+                    const float pw = exp2_approx((x[e] - st.Mp) * scale);
                     zp += pw;
-                    zr += fmaxf(0.f, pw * iSp - exp2_approx((y[e] - t.Mq) * scale) * iSq);
+                    zr += fmaxf(0.f, pw * iSp - exp2_approx((y[e] - st.Mq) * scale) * iSq);
                 }
             }
             const F2 dr = warp_sum_f2(f2(zr)), dp = warp_sum_f2(f2(zp));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.empty[s]);  // the stage is no longer read
             const int y = t.y0 + warp * tpw;
             const int blk = y / kSampleBlock;
+            int last = 0;
             if (lane == 0) {
                 if (blk < a.nblk)
                     a.zrec[(size_t(t.b) * a.nblk + blk) * kCW + (y % kSampleBlock) / tpw] =
                         make_float2(dr.hi + dr.lo, dp.hi + dp.lo);
                 __threadfence();
-                mbar_arrive(&sm.empty[s]);  // after the record: the producer books the tile
+                last = atomicAdd(&a.r1_cnt[t.b], 1) == a.nc * kCW - 1;
             }
-            __syncwarp();
+            if (lane == 0 && last) push_decide(a, t.b | kFinishResidual, epoch);
         }
     }
 }
 
 // ---------------------------------------------------------------------------
-// draws queued in the CTA, and the warps that make them
+// decider: warp kCW + 1 serves the decide queue
 // ---------------------------------------------------------------------------
-// Queue a draw (the decider's lane 0; the decider is the only writer of the
-// tail).  Returns false when the queue is full: the caller draws itself.
-__device__ __forceinline__ bool push_job(VSmem &sm, int ev) {
-    const int t = sm.job_tail;
-    if (t - ld_vol(&sm.job_head) >= kJobs) return false;
-    st_vol(&sm.jobs[t & (kJobs - 1)], ev);
-    __threadfence_block();
-    st_vol(&sm.job_tail, t + 1);
-    return true;
-}
-
-// Take a queued draw (lane 0 of any warp): its event code, or 0.
-__device__ __forceinline__ int claim_job(VSmem &sm) {
-    const int h = ld_vol(&sm.job_head);
-    if (h >= ld_vol(&sm.job_tail)) return 0;
-    if (atomicCAS(&sm.job_head, h, h + 1) != h) return 0;  // another warp took it
-    __threadfence_block();
-    return ld_vol(&sm.jobs[h & (kJobs - 1)]);
-}
-
 template <typename T>
-__device__ __forceinline__ void run_job(const VerifyArgs &a, const StreamShape &sh, int ev,
-                                        int lane) {
-    __threadfence();
-    if (((ev >> 24) & 3) == EV_R) finish_residual<T>(a, ev & 0xffff, lane);
-    else bonus_draw<T>(a, sh, ev & 0xffff, lane);
-}
-
-// A warp done with its part of the phase makes queued draws until the
-// decider has queued the last one.
-template <typename T>
-__device__ void helper(const VerifyArgs &a, VSmem &sm, const StreamShape &sh, int lane,
-                       int *fail) {
-    uint64_t t0 = global_timer_ns();
-    unsigned ns = 64;
-    for (;;) {
-        int ev = 0, quit = 0;
-        if (lane == 0) {
-            ev = claim_job(sm);
-            if (ev == 0) {
-                if (ld_vol(&sm.no_more) && ld_vol(&sm.job_head) >= ld_vol(&sm.job_tail)) {
-                    quit = 1;
-                } else if (global_timer_ns() - t0 > a.wait_ns) {
-                    atomicOr(a.status, kStatusQueueTimeout);
-                    atomicOr(fail, 1);
-                    quit = 1;
-                }
-            }
-        }
-        ev = __shfl_sync(0xffffffffu, ev, 0);
-        if (ev != 0) {
-            run_job<T>(a, sh, ev, lane);
-            if (lane == 0) {
-                t0 = global_timer_ns();
-                ns = 64;
-            }
-            continue;
-        }
-        if (__shfl_sync(0xffffffffu, quit, 0)) return;
-        if (lane == 0) {
-            __nanosleep(ns);
-            ns = min(ns * 2, 512u);
-        }
-        __syncwarp();
-    }
-}
-
-// ---------------------------------------------------------------------------
-// decider: warp kCW + 1
-// ---------------------------------------------------------------------------
-// Works through the events its producer posts, in order: decide a request
-// whose decision rows are in; queue the bonus draw of a request whose bonus
-// row is in and whose drafts were all accepted (join counter); queue the
-// residual draw of a request whose residual tiles are in.  Between events it
-// makes queued draws itself.  Returns once the producer has booked every unit
-// of the phase, the FIFO is empty and every draw is queued or made.
-template <typename T>
-__device__ void decider(const VerifyArgs &a, VSmem &sm, const StreamShape &sh, int epoch,
-                        int lane, int *fail) {
+__device__ void decider(const VerifyArgs &a, const StreamShape &sh, int epoch, int lane) {
     const int wpb = kSampleBlock / (a.chunk_elems / kCW);
-    uint64_t t_last = global_timer_ns();
-    unsigned ns = 32;
+    int pending = -1;
     for (;;) {
-        int v = 0, h = 0, job = 0, done = 0;
+        int b = -1;
         if (lane == 0) {
-            h = ld_vol(&sm.fifo_head);
-            v = ld_vol(&sm.fifo[h & (kFifo - 1)]);
-            if (v != 0) {
-                st_vol(&sm.fifo[h & (kFifo - 1)], 0);
-                __threadfence_block();
-                st_vol(&sm.fifo_head, h + 1);
-            } else if ((job = claim_job(sm)) != 0) {
-                // a queued draw while no event waits
-            } else if (ld_vol(&sm.prod_done) && ld_vol(&sm.fifo_tail) == h) {
-                done = 1;  // every unit booked, every event handled, every draw taken
-                st_vol(&sm.no_more, 1);
-            } else if (global_timer_ns() - t_last > a.wait_ns) {
-                atomicOr(a.status, kStatusQueueTimeout);
-                atomicOr(fail, 1);
-                st_vol(&sm.no_more, 1);
-                done = 1;
-            }
-        }
-        v = __shfl_sync(0xffffffffu, v, 0);
-        job = __shfl_sync(0xffffffffu, job, 0);
-        if (__shfl_sync(0xffffffffu, done, 0)) return;
-        if (v != 0) {
-            const int type = (v >> 24) & 3, Lb = (v >> 16) & 127, b = v & 0xffff;
-            __threadfence();
-            int draw = 0;  // a draw now due: queue it
-            if (type == EV_P) {
-                draw = decide_request<T>(a, sh, b, wpb, epoch, lane) ? ev_make(EV_Q, Lb, b) : 0;
-            } else if (type == EV_Q) {
-                if (lane == 0 && (Lb == 0 || atomicAdd(&a.join[b], 1) == 1)) draw = v;
-                draw = __shfl_sync(0xffffffffu, draw, 0);
-            } else {
-                draw = v;
-            }
-            if (draw != 0) {
-                int queued = 0;
-                if (lane == 0) queued = push_job(sm, draw);
-                if (!__shfl_sync(0xffffffffu, queued, 0)) run_job<T>(a, sh, draw, lane);
-            }
-            if (lane == 0) {
-                t_last = global_timer_ns();
-                ns = 32;
-            }
-            continue;
-        }
-        if (job != 0) {
-            run_job<T>(a, sh, job, lane);
-            if (lane == 0) {
-                t_last = global_timer_ns();
-                ns = 32;
-            }
-            continue;
-        }
-        if (lane == 0) {
-            __nanosleep(ns);
-            ns = min(ns * 2, 256u);
-        }
-        __syncwarp();
-    }
-}
-
-// Grid-wide barrier of the cooperative launch (every CTA is resident).  The
-// generation is read before arriving, so the last arrival's increment cannot
-// be missed.  Gives up after wait_ns (status bit) and returns false.
-__device__ bool grid_sync(const VerifyArgs &a, int *s_ok) {
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        int ok = 1;
-        const int gen = ld_relaxed(&a.q_ctr[Q_BARGEN]);
-        __threadfence();
-        if (atomicAdd(&a.q_ctr[Q_BAR], 1) == int(gridDim.x) - 1) {
-            a.q_ctr[Q_BAR] = 0;
-            __threadfence();
-            atomicAdd(&a.q_ctr[Q_BARGEN], 1);
-        } else {
+            if (pending < 0) pending = atomicAdd(&a.q_ctr[QB_HEAD], 1);
             const uint64_t t0 = global_timer_ns();
             unsigned ns = 32;
-            while (ld_acquire(&a.q_ctr[Q_BARGEN]) == gen) {
+            for (;;) {
+                if (pending < a.qbcap && ld_acquire(&a.qb_ready[pending]) == epoch) {
+                    b = __ldcg(a.qb_job + pending);
+                    pending = -1;
+                    break;
+                }
+                if (ld_acquire(&a.q_ctr[Q_FINISHED]) >= a.B) break;
                 if (global_timer_ns() - t0 > a.wait_ns) {
                     atomicOr(a.status, kStatusQueueTimeout);
-                    ok = 0;
                     break;
                 }
                 __nanosleep(ns);
-                ns = min(ns * 2, 128u);
+                ns = min(ns * 2, 256u);
             }
         }
+        b = __shfl_sync(0xffffffffu, b, 0);
+        if (b < 0) return;
         __threadfence();
-        *s_ok = ok;
+        if (b & kFinishResidual) finish_residual<T>(a, b & ~kFinishResidual, wpb, lane);
+        else if (b & kBonusDraw) bonus_draw<T>(a, sh, b & ~kBonusDraw, wpb, lane);
+        else decide_request<T>(a, sh, b, wpb, epoch, lane);
     }
-    __syncthreads();
-    return *s_ok != 0;
 }
 
 template <typename T>
 __global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(const VerifyArgs a) {
     extern __shared__ __align__(1024) uint8_t ring[];
     __shared__ VSmem sm;
-    __shared__ int s_fail, s_bar, s_last;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int epoch = ld_relaxed(&a.q_ctr[Q_EPOCH]) + 1;
-    if (tid < kRing) {
+    const int epoch = a.q_ctr[Q_EPOCH] + 1;
+    if (tid < kStages) {
         mbar_init(&sm.full[tid], 1);
         mbar_init(&sm.empty[tid], kCW);
-        sm.done[tid][0] = 0;
-        sm.done[tid][1] = 0;
+        sm.done[tid] = 0;
     }
-    if (tid < kFifo) sm.fifo[tid] = 0;
-    if (tid == 0) {
-        sm.fifo_tail = 0;
-        sm.fifo_head = 0;
-        sm.job_tail = 0;
-        sm.job_head = 0;
-        sm.no_more = 0;
-        sm.prod_done = 0;
-        s_fail = 0;
-        fence_barrier_init();
-    }
+    if (tid == 0) fence_barrier_init();
     __syncthreads();
     const StreamShape sh = stream_shape(a);
-    int fill = 0;  // the ring's next fill (producer and consumers keep it in step)
-
-    // Phase 1: stream the decision and bonus rows; decide each request and
-    // draw the bonus tokens.
     if (warp == kCW) {
-        bool ok = true;
-        fill = producer_stream(a, sm, ring, sh, epoch, lane, ok);
-        if (!ok && lane == 0) atomicOr(&s_fail, 1);
-        helper<T>(a, sm, sh, lane, &s_fail);
+        if (lane == 0) producer(a, sm, ring, sh, epoch);
     } else if (warp == kCW + 1) {
-        decider<T>(a, sm, sh, epoch, lane, &s_fail);
+        decider<T>(a, sh, epoch, lane);
     } else {
-        fill = consumer<T>(a, sm, ring, sh, warp, lane, 0, &s_fail);
-        helper<T>(a, sm, sh, lane, &s_fail);
+        consumer<T>(a, sm, ring, sh, warp, lane, epoch);
     }
     __syncthreads();
-    if (tid == 0) {
-        sm.prod_done = 0;
-        sm.no_more = 0;
-    }
-    // Phase 2, once every request is decided: the residual tiles of the
-    // rejected row pairs, each with its blocks' in-block picks; the CTA that
-    // completes a request's tiles draws its token.  A CTA whose ring gave up
-    // starts no copy.
-    if (!grid_sync(a, &s_bar)) atomicOr(&s_fail, 1);
-    if (ld_relaxed(&a.q_ctr[Q_NREJ]) > 0) {
-        if (warp == kCW + 1) {
-            decider<T>(a, sm, sh, epoch, lane, &s_fail);
-        } else {
-            if (!s_fail) {
-                if (warp == kCW) {
-                    bool ok = true;
-                    fill = producer_resid(a, sm, ring, sh, fill, lane, ok);
-                    if (!ok && lane == 0) atomicOr(&s_fail, 1);
-                } else {
-                    fill = consumer<T>(a, sm, ring, sh, warp, lane, fill, &s_fail);
-                }
-            } else if (warp == kCW && lane == 0) {
-                st_vol(&sm.prod_done, 1);  // nothing streams here: let the decider go
-            }
-            helper<T>(a, sm, sh, lane, &s_fail);
-        }
-    }
-
-    __syncthreads();
+    __shared__ int s_last;
     if (tid == 0) {
         __threadfence();
         s_last = atomicAdd(&a.q_ctr[Q_EXITED], 1) == int(gridDim.x) - 1;
@@ -1578,24 +1365,25 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(const VerifyA
     __syncthreads();
     if (s_last) {
         // Every CTA is done.  Bonus-row counts of requests that rejected can
-        // be partial, and joins of requests without drafts are never used:
-        // these reset here.
-        __threadfence();
+        // arrive after the request finished, so these reset here.
         for (int b = tid; b < a.B; b += kVerifyThreads) {
             a.bon_cnt[b] = 0;
             a.join[b] = 0;
         }
-    }
-    if (s_last && tid == 0) {
-        // Reset the counters for the next launch.
-        __threadfence();
-        a.q_ctr[Q_CHUNK] = 0;
-        a.q_ctr[Q_NREJ] = 0;
-        a.q_ctr[Q_EXITED] = 0;
-        a.q_ctr[Q_EPOCH] = epoch;
-        if (a.audit_totals) {
-            a.audit_totals[0] = atomicExch(&a.q_ctr[Q_AFULL], 0);
-            a.audit_totals[1] = atomicExch(&a.q_ctr[Q_ACOMMIT], 0);
+        if (tid == 0) {
+            // Reset the queues for the next launch.
+            a.q_ctr[QA_HEAD] = 0;
+            a.q_ctr[QA_TAIL] = 0;
+            a.q_ctr[QB_HEAD] = 0;
+            a.q_ctr[QB_TAIL] = 0;
+            a.q_ctr[Q_FINISHED] = 0;
+            a.q_ctr[Q_CHUNK] = 0;
+            a.q_ctr[Q_EXITED] = 0;
+            a.q_ctr[Q_EPOCH] = epoch;
+            if (a.audit_totals) {
+                a.audit_totals[0] = atomicExch(&a.q_ctr[Q_AFULL], 0);
+                a.audit_totals[1] = atomicExch(&a.q_ctr[Q_ACOMMIT], 0);
+            }
         }
         __threadfence();
     }
@@ -1621,8 +1409,8 @@ int verify_blocks_per_sm(int logit_bf16) {
 }
 
 cudaError_t launch_verify(const VerifyArgs &a, int logit_bf16, int grid, cudaStream_t s) {
-    // Cooperative launch: the phases are separated by grid barriers, so every
-    // CTA of the grid must be resident at once.
+    // Cooperative launch: producers and deciders poll device-wide queues, so
+    // every CTA of the grid must be resident at once.
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kVerifyThreads);
