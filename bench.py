@@ -16,7 +16,9 @@ gamma=16, V=129280, d=7168, bf16, c=0.35, cap T=768, sampling at Tm=1.
   between the two.
 * e2e: the same metric through the C ABI with host inputs: every step copies
   its inputs from pinned host memory and reads the results back.
-* cpu_baseline: the CPU oracle (single thread) on the same workload.
+* cpu_baseline: the CPU oracle (single thread) on the same workload;
+  cpu_baseline_omp: its OpenMP build over all host cores; parity: the GPU's
+  outputs of input set 0 against the oracle, with the near-tie counts.
 * cap_accept_arm: the audit arm on the same inputs -- the full block
   verified, the confidence-driven window committed -- with its step time and
   the utilization against the ceiling (accepted drafts kept / accepted drafts
@@ -28,7 +30,8 @@ gamma=16, V=129280, d=7168, bf16, c=0.35, cap T=768, sampling at Tm=1.
   and accept lengths of the timed step's input sets, with the fit's time.
 * latency_b1: the B=1 DeepSeek-class greedy step, microseconds per step with
   plain launches and replayed as one CUDA graph.
-* --impl reference: the CPU oracle as the reference arm (bounded samples).
+* --impl reference: the CPU oracle as the reference arm, full steps of the
+  same configuration.
 
 Multi-GPU runs are independent replicas (the step has no cross-request
 exchange without a cross-rank cap); the slowest rank sets the time.
@@ -39,6 +42,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -53,7 +57,7 @@ METRIC = "ragged verify steps/s & HBM GB/s (% of peak) at B=256, gamma=16, V=129
 DEFAULT_WORKLOAD = "mixed_B256_g16_V129280_d7168_bf16"
 FLUSH_BYTES = 256 << 20
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
-PROFILE_FILE = os.path.join(ROOT, "profiles", "verify_kernel_mixed_B256.md")
+PROFILE_FILE = os.path.join(ROOT, "profiles", "verify_kernel_mixed_B256.json")
 KERNEL_SOURCES = ["confidence_driven_speculative_gb300/csrc/verify.cu",
                   "confidence_driven_speculative_gb300/csrc/dspark_internal.cuh"]
 
@@ -231,22 +235,18 @@ def source_hash() -> str:
 
 
 def profiled_traffic():
-    """DRAM bytes per verify launch from the committed ncu summary, if it was
-    taken on the current kernel source; else None."""
+    """DRAM bytes per verify launch from the committed ncu figures, if they
+    were taken on the current kernel source; else None."""
     try:
-        text = open(PROFILE_FILE).read()
-    except OSError:
+        with open(PROFILE_FILE) as f:
+            vals = json.load(f)
+    except (OSError, ValueError):
         return None
-    vals = {}
-    for line in text.splitlines():
-        if ":" in line and line.strip().startswith(("traffic_bytes_per_launch", "source_sha256")):
-            k, v = line.split(":", 1)
-            vals[k.strip()] = v.strip().strip("`")
     if vals.get("source_sha256") != source_hash():
         return None
     try:
         return float(vals["traffic_bytes_per_launch"])
-    except (KeyError, ValueError):
+    except (KeyError, TypeError, ValueError):
         return None
 
 
@@ -482,21 +482,52 @@ def run_latency(binding, W, flush, steps: int = 200):
     return out
 
 
-def cpu_baseline_oracle(W, st, seconds: float):
-    """The CPU oracle (single-threaded C, fp64) on full steps of input set 0."""
+def cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip()
+                if key in ("model name", "Model"):
+                    return line.split(":", 1)[1].strip()
+                if key == "CPU part":
+                    return f"{platform.machine()} CPU part {line.split(':', 1)[1].strip()}"
+    except OSError:
+        pass
+    return platform.machine()
+
+
+def cpu_baseline_oracle(W, st, seconds: float, threads: int = 1):
+    """The CPU oracle (C, fp64) on full steps of input set 0: single-threaded
+    as it stands, or (threads > 1) its OpenMP build with the requests of the
+    verify spread over the host's threads."""
     import oracle
     npi = W.to_numpy(st["inp"])
-    oracle.build()
+    oracle.build(omp=threads > 1)
+    if threads > 1:
+        threads = oracle.omp_threads(threads)
     t0 = time.perf_counter()
     n = 0
     while True:
-        oracle.step(npi)
+        oracle.step(npi, threads=threads)
         n += 1
         if time.perf_counter() - t0 >= seconds:
             break
     dt = time.perf_counter() - t0
-    return {"value": n / dt, "unit": "steps/s", "cores": 1, "kind": "oracle",
+    return {"value": n / dt, "unit": "steps/s", "cores": threads,
+            "kind": "oracle" if threads == 1 else "oracle_openmp_over_requests",
+            "cpu": cpu_model(),
             "sample": f"{n} full steps of input set 0 ({npi['workload']}), {dt:.1f} s"}
+
+
+def parity_of_set0(W, st):
+    """The GPU's outputs of input set 0 (its last timed step) against the
+    oracle, with the counts of decisions left open by near ties."""
+    from tests.gpu_harness import compare_with_oracle, outputs_of
+    try:
+        stats = compare_with_oracle(W.to_numpy(st["inp"]), outputs_of(st["bufs"]))
+        return {"input_set": 0, "ok": True, **stats}
+    except AssertionError as e:
+        return {"input_set": 0, "ok": False, "error": str(e).splitlines()[0][:200]}
 
 
 def workload_config(w) -> dict:
@@ -659,9 +690,11 @@ def run_ours(args, rank, world, local):
                "ms_per_step": e2e_total, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "steps": args.e2e_steps}
 
-    cpu = None
+    cpu = cpu_omp = parity = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline_oracle(W, sets[0], args.cpu_seconds)
+        cpu_omp = cpu_baseline_oracle(W, sets[0], args.cpu_seconds, threads=os.cpu_count() or 1)
+        parity = parity_of_set0(W, sets[0])
 
     if rank != 0:
         return None
@@ -687,7 +720,8 @@ def run_ours(args, rank, world, local):
                      "early_exit_logit_bytes_per_launch": statistics.mean(
                          sets[i % P]["early_exit_bytes"] for i in range(args.steps))},
         "score_budget_compact_us": statistics.mean(sb_ms) * 1000.0,
-        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 3 * args.steps, "clocks": clocks,
+        "cpu_baseline": cpu, "cpu_baseline_omp": cpu_omp, "parity": parity,
+        "e2e": e2e, "gpu_launches": 3 * args.steps, "clocks": clocks,
         "mean_L": mean_L,
         "committed_tokens_per_step": statistics.mean(
             float(st["bufs"].num_emitted.sum().item()) for st in sets),
@@ -703,15 +737,15 @@ def run_ours(args, rank, world, local):
 # reference arm: the CPU oracle
 # --------------------------------------------------------------------------- #
 def run_reference(args, rank, world):
+    """The oracle on the metric's own configuration: input set 0 of the
+    workload, every request, the cap as configured; each step a full step."""
     if rank != 0:
         return None
     import oracle
     from confidence_driven_speculative_gb300 import workloads as W
     oracle.build()
     w = W.WORKLOADS[args.workload]
-    Bs = max(1, w.B // 8)  # a bounded sample: 1/8 of the batch per step
-    inp = W.to_numpy(W.make_inputs(w, 0, B=Bs,
-                                   cap_T=(w.cap_T * Bs) // w.B if w.cap_T >= 0 else -1))
+    inp = W.to_numpy(W.make_inputs(w, 0))
     for _ in range(args.warmup):
         oracle.step(inp)
     t = []
@@ -719,17 +753,17 @@ def run_reference(args, rank, world):
         t0 = time.perf_counter()
         oracle.step(inp)
         t.append(time.perf_counter() - t0)
-    full_s = statistics.mean(t) * (w.B / Bs)
-    value = 1.0 / full_s
-    sample = (f"each step: the oracle on {Bs} of {w.B} requests (cap scaled to "
-              f"{(w.cap_T * Bs) // w.B if w.cap_T >= 0 else -1}), time scaled by {w.B / Bs:g}")
+    step_s = statistics.mean(t)
+    value = 1.0 / step_s
+    sample = (f"each step: the oracle on the full input set 0 ({w.B} requests, "
+              f"cap {w.cap_T}), single thread, {args.steps} steps after {args.warmup} warm-up")
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": "steps/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": full_s * 1000.0, "higher_is_better": True, "scaling": "weak",
+            "ms_per_step": step_s * 1000.0, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": workload_config(w),
             "cpu_baseline": {"value": value, "unit": "steps/s", "cores": 1, "kind": "oracle",
-                             "sample": sample},
+                             "cpu": cpu_model(), "sample": sample},
             "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 

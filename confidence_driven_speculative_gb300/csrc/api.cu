@@ -462,15 +462,42 @@ static_assert(DSPARK_NOALLOC_SCRATCH_BYTES == kNoallocScratchBytes, "header and 
 // handle: the device address comes from cudaGetSymbolAddress.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
-// Per device: the array's device address and the shape of the last call.
-// The layout of the scratch follows (B, gamma, V); a new shape finds other
-// data where its counters go.
+// The scratch's last kNoallocHeader bytes record the shape (B, gamma, V)
+// whose counters and queue flags were last zeroed; the layout of a step uses
+// the bytes before them.
+constexpr size_t kNoallocHeader = 256;
+constexpr size_t kNoallocLayoutBytes = kNoallocScratchBytes - kNoallocHeader;
+
+// Per device: the array's device address.
 struct NoallocSlot {
     void *ptr = nullptr;
-    int32_t B = -1, gamma = -1, V = -1;
 };
 NoallocSlot g_noalloc[kMaxDevices];
 std::mutex g_noalloc_mu;
+
+// Runs on the stream before each no-alloc verify, so that the decision is
+// taken on the device in stream order -- a replayed graph takes it again.
+// When the shape recorded in the header differs from this call's (or reset
+// is set), zero the first `need` bytes (the layout of this shape; a multiple
+// of 256) and record the shape.  One CTA: the header is read before any
+// thread writes.
+__global__ void __launch_bounds__(1024) noalloc_prepare_kernel(unsigned char *scratch, size_t need,
+                                                               int B, int gamma, int V, int reset) {
+    __shared__ int s_zero;
+    int *hdr = reinterpret_cast<int *>(scratch + kNoallocLayoutBytes);
+    if (threadIdx.x == 0) s_zero = reset || hdr[0] != B || hdr[1] != gamma || hdr[2] != V;
+    __syncthreads();
+    if (!s_zero) return;
+    uint4 *p = reinterpret_cast<uint4 *>(scratch);
+    const size_t n16 = need / 16;
+    for (size_t i = threadIdx.x; i < n16; i += blockDim.x) p[i] = make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        hdr[0] = B;
+        hdr[1] = gamma;
+        hdr[2] = V;
+    }
+}
 
 }  // namespace
 
@@ -480,10 +507,10 @@ extern "C" dspark_status dspark_verify_noalloc(const dspark_step *s, int32_t res
     dspark_status st = check_shape(s);
     if (st) return st;
     const size_t need = dspark::workspace_layout(s->B, s->gamma, s->V).total;
-    if (need > kNoallocScratchBytes)
+    if (need > kNoallocLayoutBytes)
         return fail(DSPARK_EWORKSPACE,
                     "%s: B=%d gamma=%d V=%d needs %zu bytes of scratch; the static scratch holds %zu",
-                    fn, s->B, s->gamma, s->V, need, kNoallocScratchBytes);
+                    fn, s->B, s->gamma, s->V, need, kNoallocLayoutBytes);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
@@ -507,18 +534,12 @@ extern "C" dspark_status dspark_verify_noalloc(const dspark_step *s, int32_t res
             }
         }
         ptr = slot.ptr;
-        if (reset || s->B != slot.B || s->gamma != slot.gamma || s->V != slot.V) {
-            // The counters and queue flags of this shape must start at zero.
-            e = cudaMemsetAsync(ptr, 0, need, cs);
-            if (e != cudaSuccess) {
-                slot.B = slot.gamma = slot.V = -1;
-                return cuda_fail(e, "cudaMemsetAsync(static scratch)");
-            }
-            slot.B = s->B;
-            slot.gamma = s->gamma;
-            slot.V = s->V;
-        }
     }
+    // The counters and queue flags of this shape must start at zero.
+    noalloc_prepare_kernel<<<1, 1024, 0, cs>>>(static_cast<unsigned char *>(ptr), need, s->B,
+                                                 s->gamma, s->V, reset ? 1 : 0);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "noalloc_prepare_kernel launch");
     dspark_step local = *s;
     local.workspace = ptr;
     local.workspace_bytes = kNoallocScratchBytes;

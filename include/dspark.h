@@ -314,7 +314,8 @@ dspark_status dspark_read_device_status(const void *workspace, int32_t *status_o
 
 /*
  * Bytes of the fixed scratch that dspark_verify_noalloc uses instead of a
- * workspace: 8 MiB, enough for B = 512 at gamma = 16 and V = 151936.
+ * workspace: 8 MiB.  Its last 256 bytes record a shape; the rest holds a
+ * step's workspace layout, enough for B = 512 at gamma = 16 and V = 151936.
  */
 #define DSPARK_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
 
@@ -332,17 +333,19 @@ dspark_status dspark_read_device_status(const void *workspace, int32_t *status_o
  *
  * Inputs, outputs, errors and results are those of dspark_verify;
  * step->workspace and step->workspace_bytes are ignored.  A shape whose
- * workspace (dspark_workspace_size) exceeds DSPARK_NOALLOC_SCRATCH_BYTES is
- * rejected with DSPARK_EWORKSPACE before anything is enqueued.
+ * workspace (dspark_workspace_size) exceeds DSPARK_NOALLOC_SCRATCH_BYTES - 256
+ * is rejected with DSPARK_EWORKSPACE before anything is enqueued.
  *
  * The first call on a device sets up: with that device current it looks up
  * the device's copy of the array.  Make that first call before any stream
  * capture.  The scratch's counters and queue flags must start at zero, and
- * where they sit depends on (B, gamma, V): the first call on a device, and
- * every call whose (B, gamma, V) differs from the previous call's there,
- * zeroes the first dspark_workspace_size() bytes of the scratch
- * (cudaMemsetAsync on `stream`) before the launch.  A launch that ends with
- * a zero device status leaves them at zero for the next call of that shape.
+ * where they sit depends on (B, gamma, V).  Every call enqueues, before the
+ * verify launch, a one-CTA kernel that compares (B, gamma, V) with the shape
+ * recorded in the scratch; when they differ it zeroes the first
+ * dspark_workspace_size() bytes and records the new shape.  The check runs on
+ * the device in stream order, so a captured graph replayed after calls of
+ * other shapes zeroes again as needed.  A launch that ends with a zero device
+ * status leaves the counters at zero for the next call of that shape.
  *
  * reset:      nonzero zeroes them in any case.  Pass it after a call whose
  *             status was nonzero.

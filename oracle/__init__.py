@@ -48,23 +48,57 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_OMP_PATH = os.path.join(_HERE, "liboracle_omp.so")
 _lock = threading.Lock()
 _lib = None
+_omp = None
 
 F32, BF16 = 0, 1
 
 
-def build(force: bool = False) -> str:
-    """Compile ``oracle.c`` into ``liboracle.so`` next to it (gcc, -O2)."""
-    if (not force and os.path.exists(_LIB_PATH)
-            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
-        return _LIB_PATH
-    tmp = _LIB_PATH + f".{os.getpid()}.tmp"
-    cmd = ["gcc", "-std=gnu11", "-O2", "-ffp-contract=off", "-fPIC", "-shared",
+def _compile(path: str, extra, force: bool) -> str:
+    if (not force and os.path.exists(path)
+            and os.path.getmtime(path) >= os.path.getmtime(_SRC)):
+        return path
+    tmp = path + f".{os.getpid()}.tmp"
+    cmd = ["gcc", "-std=gnu11", "-O2", "-ffp-contract=off", "-fPIC", "-shared", *extra,
            "-o", tmp, _SRC, "-lm"]
     subprocess.run(cmd, check=True)
-    os.replace(tmp, _LIB_PATH)
-    return _LIB_PATH
+    os.replace(tmp, path)
+    return path
+
+
+def build(force: bool = False, omp: bool = False) -> str:
+    """Compile ``oracle.c`` into ``liboracle.so`` next to it (gcc, -O2); with
+    ``omp`` also ``liboracle_omp.so``, the same source with its OpenMP batch
+    verify enabled (for the benchmark's multi-core CPU baseline)."""
+    path = _compile(_LIB_PATH, [], force)
+    if omp:
+        _compile(_OMP_PATH, ["-fopenmp", "-DORC_OMP"], force)
+    return path
+
+
+def _load_omp():
+    """The OpenMP build: only its batch verify is used."""
+    global _omp
+    with _lock:
+        if _omp is None:
+            build(omp=True)
+            lib = ctypes.CDLL(_OMP_PATH)
+            P = ctypes.c_void_p
+            i32, f64, u64 = ctypes.c_int, ctypes.c_double, ctypes.c_uint64
+            lib.orc_verify_omp.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, f64, u64, f64,
+                                           f64, f64, P, P, P, P, P, P, P]
+            lib.orc_verify_omp.restype = ctypes.c_int
+            lib.orc_omp_threads.argtypes = [i32]
+            lib.orc_omp_threads.restype = ctypes.c_int
+            _omp = lib
+    return _omp
+
+
+def omp_threads(n: int = 0) -> int:
+    """Threads the OpenMP batch verify uses (n > 0 sets them)."""
+    return int(_load_omp().orc_omp_threads(int(n)))
 
 
 def _load():
@@ -87,6 +121,8 @@ def _load():
             lib.orc_compact.argtypes = [i32, i32, P, P, P, P, P, P, P, P, P, P]
             lib.orc_verify_request.argtypes = [i32, i32, i32, P, P, P, f64, P, P, P, f64, f64,
                                                f64, P, P, P, P, P]
+            lib.orc_check_request.argtypes = [i32, i32, i32, P, P, P, f64, P, P, P, f64, f64,
+                                              f64, i32, i32, P, P]
             lib.orc_verify.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, f64, u64, f64, f64,
                                        f64, P, P, P, P, P, P, P]
             for name in ("orc_score", "orc_score_entropy", "orc_fit_sts_tau",
@@ -287,13 +323,44 @@ def verify_request(L: int, drafts, tgt, dft, Tm: float, u, u2, u3, eps: float = 
     return int(a.value), int(tok.value), p[:L], q[:L], int(tie.value)
 
 
+def check_request(L: int, drafts, tgt, dft, Tm: float, u, u2, u3, a_g: int, tok_g: int,
+                  eps: float = EPS_U, eps_blk: float = EPS_BLK, eps_tok: float = EPS_TOK):
+    """Is ``(a_g, tok_g)`` an outcome this request admits once every decision
+    within its tolerance window may go either way?  Arguments as
+    :func:`verify_request`.  Returns ``(verdict, kinds)``: verdict 0 when
+    admitted (else 1 a out of range, 2 an earlier test rejects outside its
+    window, 3 the test at a accepts outside its window, 4 the token is not an
+    outcome of the draw at row a, 5 greedy mismatch; ``tok_g`` < 0 checks the
+    accept length alone); ``kinds`` counts the
+    open decisions on the outcome's path: accept tests, residual masses
+    below eps, draws with a near tie."""
+    lib = _load()
+    tgt = np.ascontiguousarray(tgt)
+    V = tgt.shape[-1]
+    if dft is None:
+        dft = np.zeros((max(L, 1), V), tgt.dtype)
+    dft = np.ascontiguousarray(dft, dtype=tgt.dtype)
+    drafts = _c(drafts, np.int32)
+    if drafts.size == 0:
+        drafts = np.zeros(1, np.int32)
+    u, u2, u3 = (_c(x, np.float64) for x in (u, u2, u3))
+    kinds = np.zeros(3, np.int32)
+    verdict = ctypes.c_int32(-1)
+    rc = lib.orc_check_request(L, V, _logit_dtype(tgt), _ptr(drafts), _ptr(tgt), _ptr(dft),
+                               float(np.float32(Tm)), _ptr(u), _ptr(u2), _ptr(u3), eps, eps_blk,
+                               eps_tok, int(a_g), int(tok_g), _ptr(kinds), ctypes.byref(verdict))
+    _check(rc, "check_request")
+    return int(verdict.value), kinds
+
+
 def verify(draft_tokens, draft_logits, target_ragged, L, row_off, draft_off, Tm: float,
            seed: int, eps: float = EPS_U, seq_lens=None, eps_blk: float = EPS_BLK,
-           eps_tok: float = EPS_TOK) -> dict:
+           eps_tok: float = EPS_TOK, threads: int = 1) -> dict:
     """Verify the batch.
 
     ``draft_logits`` [B, gamma, V]; ``target_ragged`` [N_rows, V] with request
-    b's rows at ``row_off[b] .. row_off[b] + L[b]``.
+    b's rows at ``row_off[b] .. row_off[b] + L[b]``.  ``threads`` > 1 runs the
+    requests on that many host threads (the OpenMP build; same results).
     """
     lib = _load()
     draft_tokens = _c(draft_tokens, np.int32)
@@ -315,7 +382,11 @@ def verify(draft_tokens, draft_logits, target_ragged, L, row_off, draft_off, Tm:
         "tie": np.zeros(B, np.int32),
     }
     sl = None if seq_lens is None else _c(seq_lens, np.int32).copy()
-    rc = lib.orc_verify(B, gamma, V, dt, _ptr(draft_tokens), _ptr(draft_logits),
+    fn = lib.orc_verify
+    if threads > 1:
+        omp_threads(threads)
+        fn = _load_omp().orc_verify_omp
+    rc = fn(B, gamma, V, dt, _ptr(draft_tokens), _ptr(draft_logits),
                         _ptr(target_ragged), _ptr(L), _ptr(row_off), _ptr(draft_off),
                         float(np.float32(Tm)), ctypes.c_uint64(seed), eps, eps_blk, eps_tok,
                         _ptr(out["accept_len"]), _ptr(out["num_emitted"]), _ptr(out["out_tokens"]),
@@ -342,7 +413,7 @@ def ragged_target(target_dense, L, row_off) -> np.ndarray:
 
 
 def step(inp: dict, eps_s: float = 1e-5, eps_cap: float = 2e-5, eps_u: float = EPS_U,
-         L_override=None) -> dict:
+         L_override=None, threads: int = 1) -> dict:
     """The whole step a1..a6 on one input dict (keys as produced by the
     workload generators): score, cap (or fixed budget), compact, the
     target-forward stand-in, verify.  ``L_override`` replaces the computed
@@ -366,7 +437,8 @@ def step(inp: dict, eps_s: float = 1e-5, eps_cap: float = 2e-5, eps_u: float = E
     res.update(compact(L, inp["draft_tokens"], inp.get("last_tokens"), inp.get("seq_lens")))
     tgt = ragged_target(inp["target_dense"], L, res["row_off"])
     v = verify(inp["draft_tokens"], inp["draft_logits"], tgt, L, res["row_off"],
-               res["draft_off"], inp["temperature"], inp["seed"], eps_u, inp.get("seq_lens"))
+               res["draft_off"], inp["temperature"], inp["seed"], eps_u, inp.get("seq_lens"),
+               threads=threads)
     res.update(v)
     return res
 

@@ -595,12 +595,173 @@ int orc_verify_request(int L, int V, int dtype, const int32_t *drafts,
     return 0;
 }
 
+/* ------------------------------------------------------------------------ */
+/* The outcomes a request admits once every decision inside its tolerance    */
+/* window may go either way.  A reduced-precision verify agrees with the     */
+/* fp64 definition above except where a decision's fp64 margin is below the  */
+/* error it is held to; there either side is a correct outcome.  Reading     */
+/* taken for the comparison (the pages fix no precision): an accept test is  */
+/* open when |u - r| < eps; a draw may land on any token whose interval of   */
+/* the running mass meets the window [t - e, t + e] around its target t,     */
+/* e = eps_blk * Z at the block level and eps_tok * (block mass) inside the  */
+/* block; a residual mass Z < eps leaves the residual draw and the fallback  */
+/* draw from p both open.  Everything else must be met exactly.              */
+/* ------------------------------------------------------------------------ */
+
+/* Whether token x is an outcome of the two-level draw from weights wt with */
+/* targets (u_blk, u_tok) and windows (eps_blk, eps_tok), as above. */
+static int draw_admits(const double *wt, int V, double u_blk, double u_tok, double eps_blk,
+                       double eps_tok, int64_t x)
+{
+    if (x < 0 || x >= V || !(wt[x] > 0.0)) return 0;
+    const int nb = (V + ORC_SAMPLE_BLOCK - 1) / ORC_SAMPLE_BLOCK;
+    const int jx = (int)(x / ORC_SAMPLE_BLOCK);
+    double Z = 0.0, before_x = 0.0, mass_x = 0.0;
+    int last_pos = -1;
+    for (int j = 0; j < nb; ++j) {
+        double m = 0.0;
+        const int64_t y1 = (int64_t)(j + 1) * ORC_SAMPLE_BLOCK < V ? (int64_t)(j + 1) * ORC_SAMPLE_BLOCK : V;
+        for (int64_t y = (int64_t)j * ORC_SAMPLE_BLOCK; y < y1; ++y) m += wt[y];
+        if (j == jx) { before_x = Z; mass_x = m; }
+        if (m > 0.0) last_pos = j;
+        Z += m;
+    }
+    const double t = u_blk * Z, e = eps_blk * Z;
+    /* block jx: its interval [before, before + mass) meets the window, or it
+     * is the fallback (the last block with mass) when no block crosses t */
+    const int blk_ok = (before_x <= t + e && before_x + mass_x > t - e) ||
+                       (jx == last_pos && t + e >= Z);
+    if (!blk_ok) return 0;
+    const int64_t y0 = (int64_t)jx * ORC_SAMPLE_BLOCK;
+    const int64_t y1 = y0 + ORC_SAMPLE_BLOCK < V ? y0 + ORC_SAMPLE_BLOCK : V;
+    const double t2 = u_tok * mass_x, e2 = eps_tok * mass_x;
+    double cum = 0.0, cum_x = 0.0;
+    int64_t last_tok = -1;
+    for (int64_t y = y0; y < y1; ++y) {
+        if (y == x) cum_x = cum;
+        if (wt[y] > 0.0) last_tok = y;
+        cum += wt[y];
+    }
+    return (cum_x <= t2 + e2 && cum_x + wt[x] > t2 - e2) || (x == last_tok && t2 + e2 >= cum);
+}
+
+/* Check a computed outcome (a_g accepted drafts, token tok_g) of one request
+ * (arguments as orc_verify_request) against the outcomes it admits.
+ * *verdict: 0 admitted; 1 a_g outside [0, L]; 2 a test before a_g rejects
+ * outside its window; 3 the test at a_g accepts outside its window; 4 the
+ * token is not an outcome of the draw at row a_g; 5 greedy: a_g or the
+ * token differs from the argmax rule.  tok_g < 0 checks the accept length
+ * alone (a verify whose token is not emitted).  kinds[0..2] count the open decisions
+ * on the path the outcome takes: accept tests, residual masses Z < eps, and
+ * draws with a block-level or in-block near tie (as draw_two_level counts). */
+int orc_check_request(int L, int V, int dtype, const int32_t *drafts,
+                      const void *tgt, const void *dft, double Tm,
+                      const double *u, const double *u2, const double *u3,
+                      double eps, double eps_blk, double eps_tok,
+                      int32_t a_g, int32_t tok_g, int32_t *kinds, int32_t *verdict)
+{
+    if (L < 0 || V < 1 || Tm < 0.0) return -1;
+    for (int i = 0; i < 3; ++i) kinds[i] = 0;
+    *verdict = 0;
+    if (a_g < 0 || a_g > L) { *verdict = 1; return 0; }
+    const size_t es = dtype == 0 ? 4 : 2;
+    const char *tbase = (const char *)tgt;
+    const char *dbase = (const char *)dft;
+    if (Tm == 0.0) {
+        int32_t a = L;
+        for (int k = 0; k < L && a == L; ++k)
+            if (drafts[k] != argmax_row(tbase + (size_t)k * V * es, dtype, V)) a = k;
+        if (a_g != a || (tok_g >= 0 && tok_g != argmax_row(tbase + (size_t)a * V * es, dtype, V)))
+            *verdict = 5;
+        return 0;
+    }
+    double *P = (double *)malloc(sizeof(double) * (size_t)V);
+    double *Q = (double *)malloc(sizeof(double) * (size_t)V);
+    double *W = (double *)malloc(sizeof(double) * (size_t)V);
+    if (!P || !Q || !W) { free(P); free(Q); free(W); return -2; }
+    const int last_test = a_g < L ? a_g : L - 1;
+    for (int k = 0; k <= last_test; ++k) {
+        softmax_row(tbase + (size_t)k * V * es, dtype, V, Tm, P);
+        softmax_row(dbase + (size_t)k * V * es, dtype, V, Tm, Q);
+        const int32_t d = drafts[k];
+        double r = 0.0;
+        if (d >= 0 && d < V) r = Q[d] > 0.0 ? fmin(1.0, P[d] / Q[d]) : 1.0;
+        const int open = fabs(u[k] - r) < eps;
+        kinds[0] += open;
+        const int accepts = u[k] < r;
+        if (*verdict == 0 && k < a_g && !accepts && !open) *verdict = 2;
+        if (*verdict == 0 && k == a_g && accepts && !open) *verdict = 3;
+    }
+    if (*verdict == 0 && tok_g >= 0) {
+        int32_t tie = 0, own;
+        softmax_row(tbase + (size_t)a_g * V * es, dtype, V, Tm, P);
+        if (a_g < L) {
+            softmax_row(dbase + (size_t)a_g * V * es, dtype, V, Tm, Q);
+            double Z = 0.0;
+            for (int64_t y = 0; y < V; ++y) {
+                W[y] = fmax(0.0, P[y] - Q[y]);
+                Z += W[y];
+            }
+            const int zopen = Z < eps;
+            kinds[1] += zopen;
+            int ok = 0;
+            if (Z > 0.0) {
+                own = draw_two_level(W, V, u2[a_g], u3[a_g], eps_blk, eps_tok, &tie);
+                ok = draw_admits(W, V, u2[a_g], u3[a_g], eps_blk, eps_tok, tok_g);
+            }
+            if (!(Z > 0.0) || zopen) {
+                own = draw_two_level(P, V, u2[a_g], u3[a_g], eps_blk, eps_tok, &tie);
+                ok = ok || draw_admits(P, V, u2[a_g], u3[a_g], eps_blk, eps_tok, tok_g);
+            }
+            if (!ok) *verdict = 4;
+        } else {
+            own = draw_two_level(P, V, u2[L], u3[L], eps_blk, eps_tok, &tie);
+            if (!draw_admits(P, V, u2[L], u3[L], eps_blk, eps_tok, tok_g)) *verdict = 4;
+        }
+        (void)own;
+        kinds[2] += tie;
+    }
+    free(P); free(Q); free(W);
+    return 0;
+}
+
 /* The whole batch: request b reads target rows row_off[b] .. row_off[b]+L_b */
 /* of the ragged target array and draft rows b*gamma .. b*gamma+L_b-1;       */
 /* uniforms come from Philox keyed by (seed, b, k).  Outputs: accept_len,    */
 /* num_emitted = a+1, out_tokens[b][0..gamma] = d_0..d_{a-1}, token, -1 pad; */
 /* p_tok/q_tok at draft_off[b] + k; seq_lens (if not NULL) += a+1;           */
 /* tie[b] as in orc_verify_request.                                          */
+/* Request b of the batch (its uniforms u, u2, u3 are scratch of gamma+1). */
+static int verify_one(int b, int gamma, int V, int dtype, const int32_t *draft_tokens,
+                      const void *draft_logits, const void *target_logits,
+                      const int32_t *L, const int32_t *row_off, const int32_t *draft_off,
+                      double Tm, uint64_t seed, double eps, double eps_blk, double eps_tok,
+                      int32_t *accept_len, int32_t *num_emitted, int32_t *out_tokens,
+                      double *p_tok, double *q_tok, int32_t *seq_lens, int32_t *tie,
+                      double *u, double *u2, double *u3)
+{
+    const size_t es = dtype == 0 ? 4 : 2;
+    const int Lb = L[b];
+    for (int k = 0; k <= Lb; ++k) orc_uniforms(seed, b, k, &u[k], &u2[k], &u3[k]);
+    const void *tgt = (const char *)target_logits + (size_t)row_off[b] * V * es;
+    const void *dft = (const char *)draft_logits + (size_t)b * gamma * V * es;
+    int32_t a, tok;
+    const int rc = orc_verify_request(Lb, V, dtype, draft_tokens + (size_t)b * gamma, tgt, dft,
+                                      Tm, u, u2, u3, eps, eps_blk, eps_tok, &a, &tok,
+                                      p_tok + draft_off[b], q_tok + draft_off[b], &tie[b]);
+    if (rc) return rc;
+    accept_len[b] = a;
+    num_emitted[b] = a + 1;
+    for (int j = 0; j <= gamma; ++j) {
+        int32_t v = -1;
+        if (j < a) v = draft_tokens[(size_t)b * gamma + j];
+        else if (j == a) v = tok;
+        out_tokens[(size_t)b * (gamma + 1) + j] = v;
+    }
+    if (seq_lens) seq_lens[b] += a + 1;
+    return 0;
+}
+
 int orc_verify(int B, int gamma, int V, int dtype, const int32_t *draft_tokens,
                const void *draft_logits, const void *target_logits,
                const int32_t *L, const int32_t *row_off, const int32_t *draft_off,
@@ -609,34 +770,57 @@ int orc_verify(int B, int gamma, int V, int dtype, const int32_t *draft_tokens,
                double *p_tok, double *q_tok, int32_t *seq_lens, int32_t *tie)
 {
     if (B < 0 || gamma < 1 || V < 1) return -1;
-    const size_t es = dtype == 0 ? 4 : 2;
     double *u = (double *)malloc(sizeof(double) * (size_t)(gamma + 1));
     double *u2 = (double *)malloc(sizeof(double) * (size_t)(gamma + 1));
     double *u3 = (double *)malloc(sizeof(double) * (size_t)(gamma + 1));
     if (!u || !u2 || !u3) { free(u); free(u2); free(u3); return -2; }
     int rc = 0;
-    for (int b = 0; b < B && rc == 0; ++b) {
-        const int Lb = L[b];
-        for (int k = 0; k <= Lb; ++k) orc_uniforms(seed, b, k, &u[k], &u2[k], &u3[k]);
-        const void *tgt = (const char *)target_logits + (size_t)row_off[b] * V * es;
-        const void *dft = (const char *)draft_logits + (size_t)b * gamma * V * es;
-        int32_t a, tok;
-        rc = orc_verify_request(Lb, V, dtype, draft_tokens + (size_t)b * gamma, tgt, dft,
-                                Tm, u, u2, u3, eps, eps_blk, eps_tok, &a, &tok,
-                                p_tok + draft_off[b], q_tok + draft_off[b], &tie[b]);
-        if (rc) break;
-        accept_len[b] = a;
-        num_emitted[b] = a + 1;
-        for (int j = 0; j <= gamma; ++j) {
-            int32_t v = -1;
-            if (j < a) v = draft_tokens[(size_t)b * gamma + j];
-            else if (j == a) v = tok;
-            out_tokens[(size_t)b * (gamma + 1) + j] = v;
-        }
-        if (seq_lens) seq_lens[b] += a + 1;
-    }
+    for (int b = 0; b < B && rc == 0; ++b)
+        rc = verify_one(b, gamma, V, dtype, draft_tokens, draft_logits, target_logits, L,
+                        row_off, draft_off, Tm, seed, eps, eps_blk, eps_tok, accept_len,
+                        num_emitted, out_tokens, p_tok, q_tok, seq_lens, tie, u, u2, u3);
     free(u);
     free(u2);
     free(u3);
     return rc;
 }
+
+#ifdef ORC_OMP
+/* The batch verify with the requests spread over the host's threads
+ * (OpenMP), for the benchmark's multi-core CPU baseline only.  It is built
+ * separately (liboracle_omp.so, -fopenmp -DORC_OMP); the plain library above
+ * stays single-threaded.  Requests are independent, so the results are those
+ * of orc_verify. */
+#include <omp.h>
+
+int orc_omp_threads(int n)
+{
+    if (n > 0) omp_set_num_threads(n);
+    return omp_get_max_threads();
+}
+
+int orc_verify_omp(int B, int gamma, int V, int dtype, const int32_t *draft_tokens,
+                   const void *draft_logits, const void *target_logits,
+                   const int32_t *L, const int32_t *row_off, const int32_t *draft_off,
+                   double Tm, uint64_t seed, double eps, double eps_blk, double eps_tok,
+                   int32_t *accept_len, int32_t *num_emitted, int32_t *out_tokens,
+                   double *p_tok, double *q_tok, int32_t *seq_lens, int32_t *tie)
+{
+    if (B < 0 || gamma < 1 || V < 1) return -1;
+    int rc = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : rc)
+    for (int b = 0; b < B; ++b) {
+        double *u = (double *)malloc(sizeof(double) * (size_t)(gamma + 1) * 3);
+        if (!u) {
+            rc |= 2;
+            continue;
+        }
+        rc |= verify_one(b, gamma, V, dtype, draft_tokens, draft_logits, target_logits, L,
+                         row_off, draft_off, Tm, seed, eps, eps_blk, eps_tok, accept_len,
+                         num_emitted, out_tokens, p_tok, q_tok, seq_lens, tie, u,
+                         u + gamma + 1, u + 2 * (gamma + 1)) != 0;
+        free(u);
+    }
+    return rc ? -2 : 0;
+}
+#endif

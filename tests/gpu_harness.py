@@ -1,12 +1,15 @@
 """Helpers for the GPU parity tests: run the CUDA step through the C ABI and
 compare it with the oracle, decision by decision.
 
-Tolerances (derived in DESIGN.md, section "Parity"): conf and survival agree
-within TOL_S absolute; p(d), q(d) within 1e-3 relative (floor 1e-30).  Every
+Tolerances (from the fp32 arithmetic of the kernels against the fp64
+oracle): conf and survival agree within TOL_S absolute; p(d), q(d) within
+1e-3 relative (floor 1e-30).  Every
 integer output is compared exactly, except a decision the oracle flags as a
-near tie (its fp64 margin below the tolerance the fp32 kernels are held to);
-there the GPU's choice is checked for validity and adopted, and the oracle
-continues from it.
+near tie (its fp64 margin below the tolerance the fp32 kernels are held to).
+There only that decision may go the GPU's way: a flagged budget or cap
+boundary is checked valid and the oracle continues from the GPU's lengths;
+in a flagged request every other accept test and draw must still match
+(oracle.check_request).  The counts of open decisions are returned.
 """
 from __future__ import annotations
 
@@ -58,11 +61,17 @@ def gpu_step(inp_dev: dict, seq_lens_commit: bool = True, bufs=None, stream=None
     binding.dspark_verify(bufs.step, stream)
     torch.cuda.synchronize()
     assert bufs.device_status() == 0
+    return outputs_of(bufs, commit), bufs
+
+
+def outputs_of(bufs, commit=None) -> dict:
+    """Host copies of every output a step wrote into ``bufs`` (the dict that
+    ``compare_with_oracle`` takes)."""
     out = {k: getattr(bufs, k).cpu().numpy() for k in (
         "conf", "survival", "L0", "L", "draft_off", "row_off", "packed_ids", "packed_pos",
         "row_req", "row_k", "accept_len", "num_emitted", "out_tokens", "p_tok", "q_tok")}
     out["seq_lens_commit"] = commit.cpu().numpy() if commit is not None else None
-    return out, bufs
+    return out
 
 
 def check_L_valid(S, c, L0, L, T, tol=TOL_S):
@@ -143,7 +152,7 @@ def compare_with_oracle(inp_np: dict, gpu: dict, max_flag_frac: float = 0.05,
     n = int(cpt["draft_off"][B])
     flagged = ver["tie"] > 0
     stats["verify_ties"] = int(flagged.sum())
-    assert stats["verify_ties"] <= max(2, int(max_flag_frac * B)), stats
+    assert stats["verify_ties"] <= max(3, int(max_flag_frac * B)), stats
     ok = ~flagged
     assert np.array_equal(gpu["accept_len"][ok], ver["accept_len"][ok]), "accept lengths differ"
     assert np.array_equal(gpu["num_emitted"][ok], ver["num_emitted"][ok])
@@ -153,14 +162,26 @@ def compare_with_oracle(inp_np: dict, gpu: dict, max_flag_frac: float = 0.05,
         p_g, q_g = gpu["p_tok"][:n].astype(np.float64), gpu["q_tok"][:n].astype(np.float64)
         np.testing.assert_allclose(p_g, p_o, rtol=RTOL_P, atol=1e-30)
         np.testing.assert_allclose(q_g, q_o, rtol=RTOL_P, atol=1e-30)
-    # flagged requests: still a valid outcome
-    V = inp_np["draft_logits"].shape[-1]
+    # A flagged request: the oracle's decisions hold exactly except the ones
+    # inside their tolerance window, where the GPU's side is taken; its
+    # accept length and token must be such an outcome.
+    kinds = np.zeros(3, np.int64)
     for b in np.nonzero(flagged)[0]:
-        a = gpu["accept_len"][b]
-        assert 0 <= a <= L[b]
+        a = int(gpu["accept_len"][b])
+        Lb = int(L[b])
+        assert 0 <= a <= Lb
         assert np.array_equal(gpu["out_tokens"][b, :a], inp_np["draft_tokens"][b, :a])
-        assert 0 <= gpu["out_tokens"][b, a] < V
         assert np.all(gpu["out_tokens"][b, a + 1:] == -1)
+        assert gpu["num_emitted"][b] == a + 1
+        r0 = int(cpt["row_off"][b])
+        un = np.array([oracle.uniforms(inp_np["seed"], int(b), k) for k in range(Lb + 1)])
+        verdict, kb = oracle.check_request(
+            Lb, inp_np["draft_tokens"][b, :max(Lb, 1)], tgt[r0:r0 + Lb + 1],
+            inp_np["draft_logits"][b, :max(Lb, 1)], inp_np["temperature"],
+            un[:, 0], un[:, 1], un[:, 2], a, int(gpu["out_tokens"][b, a]), eps=EPS_U)
+        assert verdict == 0, (int(b), verdict, a, int(gpu["out_tokens"][b, a]))
+        kinds += kb
+    stats["open_accept"], stats["open_zmass"], stats["open_draw"] = (int(x) for x in kinds)
     if gpu.get("seq_lens_commit") is not None:
         assert np.array_equal(gpu["seq_lens_commit"], inp_np["seq_lens"] + gpu["accept_len"] + 1)
     stats["mean_L"] = float(L.mean()) if B else 0.0

@@ -172,6 +172,28 @@ def test_version(lib):
     assert "sm_103a" in binding.version()
 
 
+def test_noalloc_scratch_holds_the_documented_shape(lib):
+    """The fixed scratch of dspark_verify_noalloc (less its 256-byte shape
+    record) holds the workspace of B=512, gamma=16, V=151936, as the header
+    states, and not that of B=1024."""
+    room = binding.DSPARK_NOALLOC_SCRATCH_BYTES - 256
+    assert binding.dspark_workspace_size(512, 16, 151936, 4096) <= room
+    assert binding.dspark_workspace_size(1024, 16, 151936, 4096) > room
+
+
+def test_wait_bound_setter(lib):
+    """The bound of the device waits is a host value read at each launch: set,
+    read back, and 0 restores the 2 s default (no GPU needed)."""
+    default = binding.dspark_wait_timeout_ns()
+    assert default == 2_000_000_000
+    try:
+        assert binding.dspark_set_wait_timeout_ns(12345) == binding.DSPARK_OK
+        assert binding.dspark_wait_timeout_ns() == 12345
+    finally:
+        binding.dspark_set_wait_timeout_ns(0)
+    assert binding.dspark_wait_timeout_ns() == default
+
+
 def test_cap_accept_needs_a_window(lib):
     s = valid_step()
     assert lib.dspark_verify_cap_accept(ctypes.byref(s), None, None, None, None) == binding.DSPARK_EINVAL

@@ -7,7 +7,10 @@ V logits each ("DFlash to DSpark in SGLang", "Ragged verify under full CUDA
 graphs": the packed rows are the scheduled verify tokens plus one row per
 request).  The mixed B=256 workload's figures are worked by hand here.
 """
+import json
+
 import numpy as np
+
 import pytest
 import torch
 
@@ -57,12 +60,18 @@ def test_both_arms_name_the_workload_alike():
 
 def test_profiled_traffic_follows_the_kernel_source(tmp_path, monkeypatch):
     """The committed ncu traffic is reported only while the verify source
-    it was taken on is unchanged."""
-    good = tmp_path / "p.md"
-    good.write_text(f"traffic_bytes_per_launch: 123\nsource_sha256: {bench.source_hash()}\n")
+    it was taken on is unchanged; the figures are read from JSON."""
+    good = tmp_path / "p.json"
+    good.write_text(json.dumps({"traffic_bytes_per_launch": 123,
+                                "source_sha256": bench.source_hash()}))
     monkeypatch.setattr(bench, "PROFILE_FILE", str(good))
     assert bench.profiled_traffic() == 123.0
-    stale = tmp_path / "q.md"
-    stale.write_text("traffic_bytes_per_launch: 123\nsource_sha256: 0000000000000000\n")
+    stale = tmp_path / "q.json"
+    stale.write_text(json.dumps({"traffic_bytes_per_launch": 123,
+                                 "source_sha256": "0000000000000000"}))
     monkeypatch.setattr(bench, "PROFILE_FILE", str(stale))
+    assert bench.profiled_traffic() is None
+    bad = tmp_path / "r.json"
+    bad.write_text("traffic_bytes_per_launch: 123\n")
+    monkeypatch.setattr(bench, "PROFILE_FILE", str(bad))
     assert bench.profiled_traffic() is None

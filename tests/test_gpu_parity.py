@@ -12,7 +12,7 @@ import pytest
 import torch
 
 from confidence_driven_speculative_gb300 import workloads as W
-from tests.gpu_harness import compare_with_oracle, gpu_step, to_device
+from tests.gpu_harness import compare_with_oracle, gpu_step, outputs_of, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -20,6 +20,9 @@ pytestmark = pytest.mark.gpu
 def run_and_compare(inp_cpu, **kw):
     gpu, bufs = gpu_step(to_device(inp_cpu))
     stats = compare_with_oracle(W.to_numpy(inp_cpu), gpu, **kw)
+    # the near-tie counts of every case (shown with pytest -s)
+    print(f"parity {inp_cpu['workload']} B={inp_cpu['B']} V={inp_cpu['V']} "
+          f"Tm={inp_cpu['temperature']}: {stats}")
     return gpu, stats, bufs
 
 
@@ -149,10 +152,11 @@ def test_repeated_calls_reuse_the_workspace(cuda_lib):
 def test_graph_replay_matches_direct_calls(cuda_lib, Tm):
     """The three calls captured as one CUDA graph (the cooperative verify and
     the dependent compaction included) and replayed twice give the outputs of
-    direct calls, bit for bit, on the same buffers."""
+    direct calls, bit for bit, on the same buffers, and each replay equals
+    the oracle."""
     from confidence_driven_speculative_gb300 import binding
-    inp = to_device(W.make_inputs(W.MIXED_B256, 9, B=24, V=20000, d=128, cap_T=60,
-                                  temperature=Tm))
+    inp_cpu = W.make_inputs(W.MIXED_B256, 9, B=24, V=20000, d=128, cap_T=60, temperature=Tm)
+    inp = to_device(inp_cpu)
     ref, bufs = gpu_step(inp)  # direct calls; binds the ragged target rows
     names = ("L", "row_off", "packed_ids", "accept_len", "num_emitted", "out_tokens",
              "p_tok", "q_tok")
@@ -176,20 +180,20 @@ def test_graph_replay_matches_direct_calls(cuda_lib, Tm):
         for k in names:
             assert np.array_equal(getattr(bufs, k).cpu().numpy(), ref[k]), k
         assert np.array_equal(commit.cpu().numpy(), ref["seq_lens_commit"])
+        compare_with_oracle(W.to_numpy(inp_cpu), outputs_of(bufs, commit))
 
 
-def test_one_graph_serves_every_packed_total(cuda_lib):
+def _graph_over_totals(workload, steps, B, V, d, min_totals, temperature=1.0):
     """One capture of the step -- score, compact, a fixed-shape target
-    stand-in over the batch's capacity of rows, verify -- replayed on
-    several batches whose packed totals differ.  Each replay equals direct
-    calls on that batch: the kernels take the total from device memory, so
-    no per-total graph tier is needed."""
+    stand-in over the batch's capacity of rows, verify -- replayed on input
+    sets whose packed totals differ.  Each replay equals direct calls on that
+    set and the oracle.  Returns the packed totals seen."""
     from confidence_driven_speculative_gb300 import binding
-    B, V, d = 24, 20000, 128
-    sets = [to_device(W.make_inputs(W.MIXED_B256, 40 + i, B=B, V=V, d=d, cap_T=-1,
-                                    temperature=1.0)) for i in range(4)]
-    for st in sets:
+    sets_cpu = [W.make_inputs(workload, s, B=B, V=V, d=d, cap_T=-1, temperature=temperature)
+                for s in steps]
+    for st in sets_cpu:
         st["seed"] = 5                      # a host scalar fixed at capture
+    sets = [to_device(st) for st in sets_cpu]
     keys = ("hidden", "head_w", "head_bias", "sts_tau", "draft_tokens", "draft_logits",
             "target_dense", "last_tokens", "seq_lens")
     live = {k: (v.clone() if k in keys else v) for k, v in sets[0].items()}
@@ -218,7 +222,7 @@ def test_one_graph_serves_every_packed_total(cuda_lib):
             step()
     torch.cuda.current_stream().wait_stream(side)
     totals = []
-    for st in sets:
+    for st, st_cpu in zip(sets, sets_cpu):
         ref, _ = gpu_step(st)
         for k in keys:
             live[k].copy_(st[k])
@@ -234,8 +238,26 @@ def test_one_graph_serves_every_packed_total(cuda_lib):
         for k in ("p_tok", "q_tok"):
             assert np.array_equal(getattr(bufs, k).cpu().numpy()[:n], ref[k][:n]), k
         assert np.array_equal(commit.cpu().numpy(), ref["seq_lens_commit"])
+        compare_with_oracle(W.to_numpy(st_cpu), outputs_of(bufs, commit))
         totals.append(int(ref["row_off"][B]))
-    assert len(set(totals)) > 1, totals
+    assert len(set(totals)) >= min_totals, totals
+    return totals
+
+
+def test_one_graph_serves_every_packed_total(cuda_lib):
+    """Four batches of B=24 through one captured graph, at least three
+    distinct packed totals: the kernels take the total from device memory, so
+    no per-total graph tier is needed."""
+    _graph_over_totals(W.MIXED_B256, range(40, 44), 24, 20000, 128, min_totals=3)
+
+
+def test_one_graph_serves_the_b1_latency_shape(cuda_lib):
+    """The B=1 latency shape (V = 129280, d = 7168) through one captured
+    graph over several steps (its own greedy verify, then sampling), each
+    replay checked against the oracle."""
+    w = W.LATENCY_B1
+    for Tm in (None, 1.0):
+        _graph_over_totals(w, range(5), 1, w.V, w.d, min_totals=1, temperature=Tm)
 
 
 def test_empty_batch(cuda_lib):

@@ -78,3 +78,53 @@ def test_noalloc_rejects_a_shape_beyond_its_scratch(cuda_lib):
     assert st == 0
     for k in VERIFY_OUTPUTS:
         assert np.array_equal(ref[k], got[k], equal_nan=True), k
+
+
+def test_graph_replay_after_a_call_of_another_shape(cuda_lib):
+    """Capture a no-alloc verify of shape A, make an eager call of shape B
+    (which re-zeroes the scratch for B's layout), then replay A's graph: the
+    shape check runs on the device in stream order, so the replay zeroes for
+    A again and equals dspark_verify with a workspace."""
+    inp_a = to_device(_inputs("ragged_sampling"))
+    ref_a, bufs_a = gpu_step(inp_a)
+    inp_b = to_device(_inputs("tiny_sampling"))
+    ref_b, bufs_b = gpu_step(inp_b)
+    status = torch.empty(1, dtype=torch.int32, device="cuda")
+    got, st = _run_noalloc(bufs_a, inp_a, status)  # eager A, before any capture
+    assert st == 0
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            binding.dspark_verify_noalloc(bufs_a.step, status_out=status)
+    torch.cuda.current_stream().wait_stream(side)
+    for _ in range(2):
+        got_b, st_b = _run_noalloc(bufs_b, inp_b, status)  # eager B
+        assert st_b == 0
+        for k in VERIFY_OUTPUTS:
+            assert np.array_equal(ref_b[k], got_b[k], equal_nan=True), k
+        for k in ("accept_len", "num_emitted", "out_tokens"):
+            getattr(bufs_a, k).fill_(-7)
+        commit = bufs_a._keep["seq_lens_commit"]
+        commit.copy_(inp_a["seq_lens"])
+        status.fill_(-1)
+        g.replay()
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        for k in VERIFY_OUTPUTS:
+            assert np.array_equal(ref_a[k], getattr(bufs_a, k).cpu().numpy(), equal_nan=True), k
+        assert np.array_equal(ref_a["seq_lens_commit"], commit.cpu().numpy())
+
+
+@pytest.mark.slow
+def test_noalloc_accepts_the_largest_documented_shape(cuda_lib):
+    """B=512, gamma=16, V=151936 (the header's stated limit) is accepted and
+    its device status is clean."""
+    w = W.QWEN3_8B
+    inp = to_device(W.make_inputs(w, 0, B=512, d=256, cap_T=-1))
+    ref, bufs = gpu_step(inp)
+    got, st = _run_noalloc(bufs, inp, torch.empty(1, dtype=torch.int32, device="cuda"))
+    assert st == 0
+    for k in VERIFY_OUTPUTS:
+        assert np.array_equal(ref[k], got[k], equal_nan=True), k
