@@ -218,6 +218,11 @@ def score_bytes(B: int, gamma: int, d: int, hidden_size: int) -> int:
     return B * gamma * d * hidden_size + 4 * d + 4 * (B + gamma) + 4 * (3 * B * gamma + 4 * B)
 
 
+# GB300 HBM3e nominal bandwidth (vendor figure), reported beside the
+# measured copy bandwidth.
+SPEC_HBM_GBS = 7900.0
+
+
 def measured_peak():
     try:
         with open(PEAKS_FILE) as f:
@@ -711,11 +716,13 @@ def run_ours(args, rank, world, local):
         "us_per_step": ms_per_step * 1000.0,
         "hbm_gbs_step": step_bytes / (ms_per_step * 1e-3) / 1e9,
         "hbm_frac_step": step_bytes / (ms_per_step * 1e-3) / 1e9 / peak,
+        "hbm_frac_step_of_spec": step_bytes / (ms_per_step * 1e-3) / 1e9 / SPEC_HBM_GBS,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak,
                      # the committed capture is of the default workload only
                      "traffic": profiled_traffic() if w.name == DEFAULT_WORKLOAD else None,
                      "kernel": "verify_kernel", "peak_kind": peak_kind,
+                     "frac_of_spec": achieved / SPEC_HBM_GBS, "spec_peak": SPEC_HBM_GBS,
                      "bytes_per_launch": statistics.mean(vb), "launch_us": ver_mean * 1000.0,
                      "early_exit_logit_bytes_per_launch": statistics.mean(
                          sets[i % P]["early_exit_bytes"] for i in range(args.steps))},
