@@ -399,8 +399,8 @@ static dspark_status verify_impl(const dspark_step *s, const int32_t *commit_len
                                         reinterpret_cast<cudaStream_t>(stream));
         if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(accept_full)");
     }
-    // One CTA per resident slot: the cooperative launch requires it, and the
-    // work is spread over the grid inside the kernel.
+    // One CTA per resident slot; the work is spread over the grid inside the
+    // kernel.
     const int grid = dev->sms * dev->verify_blocks[bf];
     cudaError_t e = dspark::launch_verify(a, bf, grid, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "verify_kernel launch");

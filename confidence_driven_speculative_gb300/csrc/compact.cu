@@ -20,6 +20,8 @@ __global__ void __launch_bounds__(kThreads) compact_kernel(const CompactArgs a) 
     // stream: wait here until that grid has completed and its writes (L,
     // row_off) are visible.  Without such a grid this returns at once.
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    // The verify that follows may be scheduled now (it waits for this grid).
+    asm volatile("griddepcontrol.launch_dependents;");
     const int g1 = a.gamma + 1;
     const int cap = a.B * g1;
     const int t = blockIdx.x * kThreads + threadIdx.x;

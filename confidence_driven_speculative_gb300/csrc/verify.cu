@@ -14,7 +14,7 @@
 // Design (GB300).  The pass is HBM-bound: every packed target row (sum L + B)
 // and every kept draft row (sum L) is read at most once, V logits each.
 //
-//  * One persistent cooperative grid, 2 CTAs per SM; each CTA is a producer
+//  * One persistent grid, 2 CTAs per SM; each CTA is a producer
 //    warp, 8 consumer warps and a decider warp.  The producer's lane 0 fills
 //    a 3-stage shared-memory ring with 1-D bulk TMA copies (cp.async.bulk)
 //    completing on "full" mbarriers with byte counts; each consumer warp
@@ -1339,6 +1339,10 @@ template <typename T>
 __global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(const VerifyArgs a) {
     extern __shared__ __align__(1024) uint8_t ring[];
     __shared__ VSmem sm;
+    // Launched as a programmatic dependent: wait until the grid before it has
+    // completed and its writes (offsets, packed rows) are visible.  Without
+    // such a grid this returns at once.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int epoch = a.q_ctr[Q_EPOCH] + 1;
     if (tid < kStages) {
@@ -1409,16 +1413,19 @@ int verify_blocks_per_sm(int logit_bf16) {
 }
 
 cudaError_t launch_verify(const VerifyArgs &a, int logit_bf16, int grid, cudaStream_t s) {
-    // Cooperative launch: producers and deciders poll device-wide queues, so
-    // every CTA of the grid must be resident at once.
+    // A programmatic dependent of the kernel before it (the compaction): the
+    // grid is scheduled while that kernel runs and waits for it at its start
+    // (griddepcontrol.wait).  Not cooperative: every unit of work -- stream
+    // chunks, residual tiles, decider jobs -- is claimed by a running CTA, so
+    // no CTA waits on one that has not started.
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kVerifyThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (logit_bf16) return cudaLaunchKernelEx(&cfg, verify_kernel<uint16_t>, a);
