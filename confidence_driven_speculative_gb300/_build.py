@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OBJ_DIR = os.path.join(PKG, "lib", "obj")
 LIB_PATH = os.path.join(PKG, "lib", "libdspark.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["api.cu", "score_budget.cu", "compact.cu", "verify.cu", "sts_fit.cu"]
+SOURCES = ["api.cu", "score_budget.cu", "compact.cu", "verify.cu", "verify_small.cu", "sts_fit.cu"]
 
 
 def nvcc() -> str:

@@ -399,10 +399,20 @@ static dspark_status verify_impl(const dspark_step *s, const int32_t *commit_len
                                         reinterpret_cast<cudaStream_t>(stream));
         if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(accept_full)");
     }
+    cudaError_t e;
+    if (dspark::verify_small_fits(s->B, s->V, commit_len != nullptr)) {
+        // Few requests: units of (row, 8192-id slice) over a plain grid, the
+        // CTA that completes a request decides it (verify_small.cu).
+        const long long units = (long long)s->B * (s->gamma + 1) * dspark::verify_small_slices(s->V);
+        const int grid = int(std::min<long long>(units, (long long)dev->sms * 8));
+        e = dspark::launch_verify_small(a, bf, grid, reinterpret_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(e, "verify_small_kernel launch");
+        return DSPARK_OK;
+    }
     // One CTA per resident slot; the work is spread over the grid inside the
     // kernel.
     const int grid = dev->sms * dev->verify_blocks[bf];
-    cudaError_t e = dspark::launch_verify(a, bf, grid, reinterpret_cast<cudaStream_t>(stream));
+    e = dspark::launch_verify(a, bf, grid, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "verify_kernel launch");
     return DSPARK_OK;
 }

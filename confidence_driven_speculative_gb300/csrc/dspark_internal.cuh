@@ -376,6 +376,12 @@ int entropy_blocks_per_sm(int logit_bf16);
 cudaError_t launch_fixed_budget(const FixedArgs &a, cudaStream_t s);
 cudaError_t launch_compact(const CompactArgs &a, cudaStream_t s);
 cudaError_t launch_verify(const VerifyArgs &a, int logit_bf16, int grid, cudaStream_t s);
+// The small-batch verify (verify_small.cu): which batches it takes, its row
+// slices, and its launch.
+constexpr int kSmallBatchMax = 16;
+bool verify_small_fits(int B, int V, bool audit);
+int verify_small_slices(int V);
+cudaError_t launch_verify_small(const VerifyArgs &a, int logit_bf16, int grid, cudaStream_t s);
 // The bound of every device wait in the next launches (0 restores kWaitTimeoutNs).
 void set_wait_timeout_ns(uint64_t ns);
 uint64_t wait_timeout_ns();

@@ -165,12 +165,15 @@ def test_window_covering_the_block_is_the_static_verify(cuda_lib):
     g = inp["gamma"]
     gpu, _, _ = run_and_compare(inp, np.full(16, g, np.int32))
     assert np.array_equal(gpu["accept_len"], gpu["accept_full"])
-    # the same block through dspark_verify
+    # the same block through dspark_verify (at B = 16 its small-batch path,
+    # which sums the softmax in another order: p and q agree to rounding)
     from tests.gpu_harness import gpu_step
     inp_s = dict(inp, fixed_budget=g)
     st, _ = gpu_step(to_device(inp_s))
-    for k in ("accept_len", "num_emitted", "out_tokens", "p_tok", "q_tok"):
+    for k in ("accept_len", "num_emitted", "out_tokens"):
         assert np.array_equal(st[k], gpu[k]), k
+    for k in ("p_tok", "q_tok"):
+        np.testing.assert_allclose(st[k], gpu[k], rtol=1e-5, atol=1e-30)
 
 
 def test_latency_b1_scheduler_window(cuda_lib):

@@ -82,6 +82,9 @@ SHAPES = [
     (5, 16, 12292, 100, "f32"),    # 4 fp32 tiles, ragged
     (300, 4, 520, 64, "bf16"),     # many requests, one tile each
     (9, 64, 1000, 16, "bf16"),     # the largest gamma
+    (12, 16, 70000, 64, "bf16"),   # the small-batch kernel: 9 slices of 8192 ids
+    (16, 12, 40000, 32, "f32"),    # the small-batch kernel, fp32, its largest batch
+    (17, 12, 40000, 32, "bf16"),   # one past it: the persistent kernel
 ]
 
 

@@ -24,7 +24,9 @@ STATUS_QUEUE = 2  # a wait on other warps or CTAs gave up
 
 @pytest.mark.parametrize("Tm", [0.0, 1.0])
 def test_short_wait_bound_gives_up_and_workspace_recovers(cuda_lib, Tm):
-    inp_cpu = W.make_inputs(W.MIXED_B256, 12, B=64, V=20000, d=128, cap_T=-1, temperature=Tm)
+    # B = 96: the persistent verify kernel, whose producers, consumers and
+    # deciders wait on one another (the small-batch kernel has no waits)
+    inp_cpu = W.make_inputs(W.MIXED_B256, 12, B=96, V=20000, d=128, cap_T=-1, temperature=Tm)
     inp = to_device(inp_cpu)
     _, bufs = gpu_step(inp)  # a clean step binds every buffer
     default = binding.dspark_wait_timeout_ns()
