@@ -1,7 +1,8 @@
 #!/usr/bin/env python3
 """Benchmark of the confidence-driven variable-length verify step.
 
-One step = dspark_score_budget + dspark_compact + dspark_verify (C ABI, one
+One step = dspark_score_compact (steps a1-a4 in one launch: what
+dspark_score_budget + dspark_compact compute) + dspark_verify (C ABI, one
 stream) over one batch of the mixed-traffic workload: B=256 requests,
 gamma=16, V=129280, d=7168, bf16, c=0.35, cap T=768, sampling at Tm=1.
 
@@ -268,10 +269,10 @@ def prepare_set(W, binding, w, step: int, fixed_budget: int = -1, entropy_theta=
     commit = inp["seq_lens"].clone()
     bufs.bind(inp, seq_lens_commit=commit)
     if entropy_theta is None:
-        binding.dspark_score_budget(bufs.step)
+        binding.dspark_score_compact(bufs.step)
     else:
         binding.dspark_score_entropy(bufs.step, entropy_theta)
-    binding.dspark_compact(bufs.step)
+        binding.dspark_compact(bufs.step)
     torch.cuda.synchronize()
     n_rows = int(bufs.row_off[inp["B"]].item())
     # Stand-in for the target forward over the packed rows (not timed).
@@ -338,8 +339,7 @@ def audit_loop(binding, audit, K, W_, flush, stream):
         if e:
             e[0].record()
         binding.dspark_score_budget(win.step, stream)
-        binding.dspark_score_budget(s, stream)
-        binding.dspark_compact(s, stream)
+        binding.dspark_score_compact(s, stream)
         if e:
             e[1].record()
         binding.dspark_verify_cap_accept(s, win.L, st["accept_full"], st["totals"], stream)
@@ -384,8 +384,7 @@ def run_steps(binding, sets, K, W_, flush, stream):
     for i in range(W_):
         s = sets[i % P]["bufs"].step
         flush.zero_()
-        binding.dspark_score_budget(s, stream)
-        binding.dspark_compact(s, stream)
+        binding.dspark_score_compact(s, stream)
         binding.dspark_verify(s, stream)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True)) for _ in range(K)]
@@ -399,8 +398,7 @@ def timed_loop(binding, sets, ev, flush, stream):
         s = sets[i % P]["bufs"].step
         flush.zero_()
         e0.record()
-        binding.dspark_score_budget(s, stream)
-        binding.dspark_compact(s, stream)
+        binding.dspark_score_compact(s, stream)
         e1.record()
         binding.dspark_verify(s, stream)
         e2.record()
@@ -408,7 +406,7 @@ def timed_loop(binding, sets, ev, flush, stream):
 
 def run_e2e(binding, W, st, steps, stream):
     """Steps through the C ABI with host inputs: H2D of every input from pinned
-    memory, the three calls, D2H of the results, inside the timed region.
+    memory, the step's calls, D2H of the results, inside the timed region.
     (Spreading the copies over several streams measured no faster.)"""
     import torch
     inp, bufs = st["inp"], st["bufs"]
@@ -429,8 +427,7 @@ def run_e2e(binding, W, st, steps, stream):
         e0.record()
         for k in host:
             dev[k].copy_(host[k], non_blocking=True)
-        binding.dspark_score_budget(bufs.step, stream)
-        binding.dspark_compact(bufs.step, stream)
+        binding.dspark_score_compact(bufs.step, stream)
         binding.dspark_verify(bufs.step, stream)
         for o, h in zip(outs, host_out):
             h.copy_(o, non_blocking=True)
@@ -450,8 +447,7 @@ def run_latency(binding, W, flush, steps: int = 200):
     step = st["bufs"].step
 
     def one():
-        binding.dspark_score_budget(step)
-        binding.dspark_compact(step)
+        binding.dspark_score_compact(step)
         binding.dspark_verify(step)
 
     def timed(fn):
@@ -728,7 +724,7 @@ def run_ours(args, rank, world, local):
                          sets[i % P]["early_exit_bytes"] for i in range(args.steps))},
         "score_budget_compact_us": statistics.mean(sb_ms) * 1000.0,
         "cpu_baseline": cpu, "cpu_baseline_omp": cpu_omp, "parity": parity,
-        "e2e": e2e, "gpu_launches": 3 * args.steps, "clocks": clocks,
+        "e2e": e2e, "gpu_launches": 2 * args.steps, "clocks": clocks,
         "mean_L": mean_L,
         "committed_tokens_per_step": statistics.mean(
             float(st["bufs"].num_emitted.sum().item()) for st in sets),

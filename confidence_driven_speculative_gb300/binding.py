@@ -5,7 +5,8 @@ kernels behind the C ABI.  PyTorch provides device memory and the stream.
 If the library has not been built this module raises; there is no fallback.
 
 The three entry points keep their C names: :func:`dspark_score_budget`,
-:func:`dspark_compact`, :func:`dspark_verify` (plus the workspace helpers).
+:func:`dspark_compact`, :func:`dspark_verify` (plus the workspace helpers);
+:func:`dspark_score_compact` is the first two in one launch.
 :class:`StepBuffers` allocates the caller-owned outputs and workspace of one
 step shape and fills the ``dspark_step`` struct.
 """
@@ -65,7 +66,8 @@ def load():
                 f"{path} is missing: build it first (python -c 'import __graft_entry__ as g; g.build()')")
         lib = ctypes.CDLL(path)
         SP = ctypes.POINTER(DsparkStep)
-        for name in ("dspark_score_budget", "dspark_compact", "dspark_verify"):
+        for name in ("dspark_score_budget", "dspark_score_compact", "dspark_compact",
+                     "dspark_verify"):
             fn = getattr(lib, name)
             fn.argtypes = [SP, _P]
             fn.restype = ctypes.c_int
@@ -130,6 +132,11 @@ def dspark_score_entropy(step: DsparkStep, theta: float, stream=None, check: boo
 
 def dspark_compact(step: DsparkStep, stream=None, check: bool = True) -> int:
     return _call("dspark_compact", step, stream, check)
+
+
+def dspark_score_compact(step: DsparkStep, stream=None, check: bool = True) -> int:
+    """dspark_score_budget then dspark_compact, in one kernel launch."""
+    return _call("dspark_score_compact", step, stream, check)
 
 
 def dspark_verify(step: DsparkStep, stream=None, check: bool = True) -> int:

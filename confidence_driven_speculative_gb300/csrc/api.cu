@@ -149,15 +149,23 @@ dspark_status dspark_workspace_init(void *workspace, size_t workspace_bytes, dsp
     return DSPARK_OK;
 }
 
-dspark_status dspark_score_budget(const dspark_step *s, dspark_stream_t stream) {
-    NvtxRange range("dspark_score_budget");
-    const char *fn = "dspark_score_budget";
+// Steps a1-a3 (and, with pack, a4) of dspark_score_budget and
+// dspark_score_compact.
+static dspark_status score_impl(const dspark_step *s, bool pack, dspark_stream_t stream,
+                                const char *fn) {
     dspark_status st = check_shape(s);
     if (st) return st;
     if (s->B == 0) return DSPARK_OK;
     REQUIRE(s->L);
     REQUIRE(s->draft_off);
     REQUIRE(s->row_off);
+    if (pack) {
+        REQUIRE(s->draft_tokens);
+        REQUIRE(s->packed_ids);
+        REQUIRE(s->packed_pos);
+        REQUIRE(s->row_req);
+        REQUIRE(s->row_k);
+    }
     const bool fixed = s->fixed_budget >= 0;
     if (fixed && s->cap_T >= 0)
         return fail(DSPARK_EINVAL, "%s: a fixed budget (%d) cannot be combined with a cap (%d)", fn,
@@ -166,9 +174,12 @@ dspark_status dspark_score_budget(const dspark_step *s, dspark_stream_t stream) 
     DeviceInfo *dev;
     if (fixed) {
         if ((st = device_info(&dev))) return st;
-        dspark::FixedArgs a{s->B, s->gamma, s->fixed_budget, s->L, s->draft_off, s->row_off};
+        dspark::FixedArgs a{s->B, s->gamma, s->fixed_budget, s->L, s->draft_off, s->row_off,
+                            pack ? 1 : 0, s->draft_tokens, s->last_tokens, s->seq_lens_in,
+                            s->packed_ids, s->packed_pos, s->row_req, s->row_k};
         cudaError_t e = dspark::launch_fixed_budget(a, cs);
-        if (e != cudaSuccess) return cuda_fail(e, "fixed_budget_kernel launch");
+        if (e != cudaSuccess)
+            return cuda_fail(e, pack ? "fixed_pack_kernel launch" : "fixed_budget_kernel launch");
         return DSPARK_OK;
     }
     REQUIRE(s->hidden);
@@ -203,9 +214,29 @@ dspark_status dspark_score_budget(const dspark_step *s, dspark_stream_t stream) 
     a.row_ctr = ws_at<int32_t>(s, lay.score_rows);
     a.status = ws_at<int32_t>(s, lay.status);
     a.wait_ns = g_wait_ns.load();
+    if (pack) {
+        a.pack = 1;
+        a.draft_tokens = s->draft_tokens;
+        a.last_tokens = s->last_tokens;
+        a.seq_lens = s->seq_lens_in;
+        a.packed_ids = s->packed_ids;
+        a.packed_pos = s->packed_pos;
+        a.row_req = s->row_req;
+        a.row_k = s->row_k;
+    }
     cudaError_t e = dspark::launch_score_budget(a, grid, cs);
     if (e != cudaSuccess) return cuda_fail(e, "score_budget_kernel launch");
     return DSPARK_OK;
+}
+
+dspark_status dspark_score_budget(const dspark_step *s, dspark_stream_t stream) {
+    NvtxRange range("dspark_score_budget");
+    return score_impl(s, false, stream, "dspark_score_budget");
+}
+
+dspark_status dspark_score_compact(const dspark_step *s, dspark_stream_t stream) {
+    NvtxRange range("dspark_score_compact");
+    return score_impl(s, true, stream, "dspark_score_compact");
 }
 
 dspark_status dspark_score_entropy(const dspark_step *s, float theta, dspark_stream_t stream) {

@@ -322,11 +322,19 @@ struct ScoreArgs {
     // and ent_scale = log2(e) / theta.
     float ent_scale;
     uint64_t wait_ns;  // bound of every wait
+    // pack != 0: the finishing CTA also writes the ragged packing (step a4)
+    int pack;
+    const int32_t *draft_tokens, *last_tokens, *seq_lens;
+    int32_t *packed_ids, *packed_pos, *row_req, *row_k;
 };
 
 struct FixedArgs {
     int B, gamma, F;
     int32_t *L, *draft_off, *row_off;
+    // pack != 0: also the ragged packing (step a4), one thread per slot
+    int pack;
+    const int32_t *draft_tokens, *last_tokens, *seq_lens;
+    int32_t *packed_ids, *packed_pos, *row_req, *row_k;
 };
 
 struct CompactArgs {

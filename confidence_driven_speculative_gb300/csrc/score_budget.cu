@@ -1,4 +1,5 @@
-// score_budget.cu -- steps a1-a3 and the scans of a4 in one kernel.
+// score_budget.cu -- steps a1-a3 and the scans of a4 in one kernel (and,
+// for dspark_score_compact, the packing of a4 as well).
 //
 // "DFlash to DSpark in SGLang", section "DSpark: a sequential head and a
 // verify budget": a linear projection plus sigmoid on the drafter hidden
@@ -23,13 +24,17 @@
 // the pre-cap length L0_b, and runs the cap: an
 // MSB-first radix select over the fp32 bit patterns of the candidate gains
 // S_{b,k} (non-negative floats order like their bit patterns), ties resolved
-// by request then position, followed by the exclusive scans.  Counters reset
+// by request then position, followed by the exclusive scans and, when asked,
+// the ragged packing.  Up to 256 requests this finish keeps everything on
+// chip (finish_fast); larger batches take finish_general.  Counters reset
 // themselves, so no CTA waits on another and the kernel is safe to replay.
 //
 // score_entropy_kernel is the same kernel with the draft logit rows as its
 // rows and an entropy consumer in place of the dot product: the confidence of
 // a draft is exp(-H) of its distribution ("SGLang Integrates DSpark ...",
 // "DSpark's Core Idea: Only Verify the Parts You're Confident About").
+#include <algorithm>
+
 #include "dspark_internal.cuh"
 
 namespace dspark {
@@ -86,6 +91,11 @@ __device__ void write_offsets(int B, const int32_t *L, int32_t *draft_off, int32
         draft_off[B] = carry;
         row_off[B] = carry + B;
     }
+}
+
+// A hint to bring the 128-byte line holding p into L2.
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
 constexpr int kScoreStages = 4;
@@ -526,7 +536,33 @@ __device__ void select_digit(FinishSmem &fs, int need, int tid) {
     }
 }
 
-__device__ void finish_and_budget(const ScoreArgs &a, uint8_t *ring) {
+// Step a4 in the finishing CTA of the general path, slot by slot as the
+// compaction kernel does it: slot (b, j) of the B*(gamma+1) capacity writes
+// packed row row_off[b] + j when j <= L_b, and slot t >= N_rows writes the
+// padding of row t.  L and row_off were written by this CTA.
+__device__ void pack_slots(const ScoreArgs &a) {
+    const int g1 = a.gamma + 1, cap = a.B * g1;
+    const int n_rows = a.row_off[a.B];
+    for (int t = threadIdx.x; t < cap; t += kThreads) {
+        const int b = t / g1, j = t - b * g1;
+        if (j <= a.L[b]) {
+            const int r = a.row_off[b] + j;
+            a.packed_ids[r] = j == 0 ? (a.last_tokens ? a.last_tokens[b] : -1)
+                                     : a.draft_tokens[size_t(b) * a.gamma + j - 1];
+            a.packed_pos[r] = (a.seq_lens ? a.seq_lens[b] : 0) + j;
+            a.row_req[r] = b;
+            a.row_k[r] = j;
+        }
+        if (t >= n_rows) {
+            a.packed_ids[t] = -1;
+            a.packed_pos[t] = 0;
+            a.row_req[t] = -1;
+            a.row_k[t] = -1;
+        }
+    }
+}
+
+__device__ void finish_general(const ScoreArgs &a, uint8_t *ring) {
     __shared__ FinishSmem fs;
     const int B = a.B, g = a.gamma, tid = threadIdx.x, lane = tid & 31;
     const int pitch = g | 1;
@@ -673,6 +709,440 @@ __device__ void finish_and_budget(const ScoreArgs &a, uint8_t *ring) {
     }
     sync256();
     write_offsets(B, a.L, a.draft_off, a.row_off, fs.sh);
+    if (a.pack) {
+        sync256();  // L and row_off, written above by this CTA, are read back
+        pack_slots(a);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Fast finish: B <= kThreads, one request per thread, everything in the
+// ring.  The same outputs as finish_general, with fewer round trips:
+//   * each thread loads its request's gamma confidences straight into
+//     registers, forms S_{b,1..gamma} and L0_b there and keeps the keys
+//     S_{b,1..L0_b} in shared memory at b * pitch;
+//   * one block reduction gives sum L0, the largest key (some S_{b,1}) and
+//     the smallest (some S_{b,L0_b});
+//   * the cap's radix select (fast_select) takes 4-bit digits from the
+//     first bit in which those two differ, counted in registers, one
+//     barrier a pass, until at most 32 candidates are left, which every
+//     warp then finishes bit by bit with ballots.  (Measured on the B = 256
+//     shape: 8-bit digits counted by shared atomics serialised on the few
+//     bins the clustered keys fall into, ~1.4 us a pass; 4-bit passes to
+//     the last bit cost ~0.4-0.7 us each, seven of them.)
+//   * the packing (when asked for) reads the draft tokens, last tokens and
+//     cached lengths into shared memory at the start, behind the
+//     confidences, and writes the packed rows coalesced at the end.
+// Ring layout in 32-bit words:
+//   [0, B * pitch)                     keys S_{b,k+1} at b * pitch + k
+//   [tok, + B * gamma)                 draft tokens      } packing only
+//   [last, + B), [seq, + B)            last tokens, cached lengths
+// and, after the cap, [0, cap) the request of each packed row and
+// [cap, cap + B) the row offsets (cap = B * (gamma + 1)).
+// ---------------------------------------------------------------------------
+constexpr int kRingWords = int(kScoreSmemBytes / 4);
+
+struct FastLayout {
+    int tok, last, seq, roff, total;
+};
+
+__device__ __forceinline__ FastLayout fast_layout(int B, int g, int pack) {
+    FastLayout f;
+    const int pitch = g | 1, cap = B * (g + 1);
+    f.roff = cap;
+    f.tok = pack ? max(B * pitch, cap + B) : B * pitch;
+    f.last = f.tok + (pack ? B * g : 0);
+    f.seq = f.last + (pack ? B : 0);
+    f.total = f.seq + (pack ? B : 0);
+    return f;
+}
+
+__device__ __forceinline__ bool fast_finish_fits(const ScoreArgs &a) {
+    return a.B <= kThreads && fast_layout(a.B, a.gamma, a.pack).total <= kRingWords;
+}
+
+struct FastSmem {
+    int red[kWarps][3];         // per-warp sum of L0, largest key, smallest key
+    unsigned wh[2][kWarps][8];  // per-warp digit counts, two 16-bit bins a word,
+                                // by pass parity
+    unsigned cand[32];          // the last <= 32 candidate keys of the select
+    int ncand;                  // their count, as they are gathered
+    int sh[kWarps + 1];         // block scans
+};
+
+// Copy n ints from global to shared, 16 loads in flight per thread.
+__device__ __forceinline__ void stage_ints(int *dst, const int32_t *src, int n) {
+    for (int base = 0; base < n; base += 16 * kThreads) {
+        int v[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const int i = base + j * kThreads + int(threadIdx.x);
+            v[j] = i < n ? __ldg(src + i) : 0;
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const int i = base + j * kThreads + int(threadIdx.x);
+            if (i < n) dst[i] = v[j];
+        }
+    }
+}
+
+// Confidences k0 .. k0 + 15 of one request (0 past gamma): four 16-byte
+// loads when gamma % 4 == 0 and the rows are 16-byte aligned.
+__device__ __forceinline__ void load_conf16(const float *crow, int k0, int g, bool vec,
+                                            float (&c)[16]) {
+    if (vec) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (k0 + 4 * q < g) v = __ldcg(reinterpret_cast<const float4 *>(crow + k0) + q);
+            c[4 * q] = v.x;
+            c[4 * q + 1] = v.y;
+            c[4 * q + 2] = v.z;
+            c[4 * q + 3] = v.w;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) c[j] = k0 + j < g ? __ldcg(crow + k0 + j) : 0.f;
+    }
+}
+
+// Add a key's 4-bit digit at `shift` to a thread's 16 byte-wide bins (h0:
+// digits 0-7, h1: 8-15; a request has at most 64 keys, so no byte
+// overflows) when the key is valid and matches the prefix.
+__device__ __forceinline__ void count_digit(unsigned key, bool valid, unsigned mask,
+                                            unsigned prefix, int shift,
+                                            unsigned long long &h0, unsigned long long &h1) {
+    if (valid && (key & mask) == prefix) {
+        const unsigned dg = (key >> shift) & 15u;
+        const unsigned long long inc = 1ull << ((dg & 7u) * 8u);
+        if (dg & 8u) h1 += inc;
+        else h0 += inc;
+    }
+}
+
+// The cap_T-th largest key (as bits) and how many keys equal to it are
+// kept, over the keys of every request (thread b: S_{b,1..l0}, in the
+// registers c[] when gamma <= 16, else srow[0, l0)).
+//
+// Four bits a pass, from the first bit in which the largest and smallest key
+// differ (every key shares the bits above).  A request's keys do not
+// increase with k, so the keys that match a prefix form one run
+// [lo_b, hi_b) of its list and a thread counts only that run, into byte
+// bins in registers.  The warps sum the bins (16-bit fields, one reduction
+// per two bins) and write them to shared memory; after one barrier every
+// warp reads all eight and picks the digit itself by a suffix scan, so one
+// barrier a pass suffices (the counts are double-buffered by pass).  Once
+// the chosen digit holds at most 32 keys, those keys are gathered into
+// shared memory and every warp settles the remaining bits one at a time
+// with ballots, without further barriers.
+__device__ void fast_select(const ScoreArgs &a, FastSmem &fs, const float *srow,
+                            const float (&c)[16], bool regs, int l0, unsigned kmax,
+                            unsigned kmin, unsigned *K_out, int *need_out) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    int need = a.cap_T;  // rank still to place among the keys matching prefix
+    const unsigned diff = kmax ^ kmin;
+    if (diff == 0u) {  // every key is the same value
+        *K_out = kmax;
+        *need_out = need;
+        return;
+    }
+    int shift = (31 - __clz(int(diff))) & ~3;
+    unsigned mask = shift >= 28 ? 0u : ~0u << (shift + 4);
+    unsigned prefix = kmax & mask;
+    int lo = 0, hi = l0;  // this request's keys that match prefix
+    for (int pass = 0;; ++pass) {
+        unsigned long long h0 = 0ull, h1 = 0ull;
+        int nlo = hi, nhi = lo;
+        if (regs) {
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const unsigned key = __float_as_uint(c[k]);
+                const bool v = k >= lo && k < hi && (key & mask) == prefix;
+                count_digit(key, v, mask, prefix, shift, h0, h1);
+                if (v) {
+                    nlo = min(nlo, k);
+                    nhi = k + 1;
+                }
+            }
+        } else {
+            for (int k = lo; k < hi; ++k) {
+                const unsigned key = __float_as_uint(srow[k]);
+                const bool v = (key & mask) == prefix;
+                count_digit(key, v, mask, prefix, shift, h0, h1);
+                if (v) {
+                    nlo = min(nlo, k);
+                    nhi = k + 1;
+                }
+            }
+        }
+        lo = nlo;
+        hi = max(nhi, nlo);
+        // bins 2q and 2q+1 as the 16-bit halves of word q
+        const unsigned x0 = unsigned(h0), x1 = unsigned(h0 >> 32);
+        const unsigned x2 = unsigned(h1), x3 = unsigned(h1 >> 32);
+        unsigned w[8] = {__byte_perm(x0, 0u, 0x4140), __byte_perm(x0, 0u, 0x4342),
+                         __byte_perm(x1, 0u, 0x4140), __byte_perm(x1, 0u, 0x4342),
+                         __byte_perm(x2, 0u, 0x4140), __byte_perm(x2, 0u, 0x4342),
+                         __byte_perm(x3, 0u, 0x4140), __byte_perm(x3, 0u, 0x4342)};
+        unsigned (&wh)[kWarps][8] = fs.wh[pass & 1];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) w[q] = __reduce_add_sync(0xffffffffu, w[q]);
+        if (lane == 0) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) wh[warp][q] = w[q];
+        }
+        sync256();
+        // lane t < 16 owns digit t: keys with digit >= t by a suffix scan
+        unsigned cnt = 0u;
+        if (lane < 16) {
+#pragma unroll
+            for (int v = 0; v < kWarps; ++v) cnt += wh[v][lane >> 1];
+            cnt = (lane & 1) ? cnt >> 16 : cnt & 0xffffu;
+        }
+        unsigned suf = cnt;
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) {
+            const unsigned n = __shfl_down_sync(0xffffffffu, suf, o);
+            if (lane + o < 16) suf += n;
+        }
+        const unsigned gt = suf - cnt;  // keys with a larger digit
+        const unsigned hit = __ballot_sync(0xffffffffu, lane < 16 && gt < unsigned(need) &&
+                                                            unsigned(need) <= suf);
+        const int d = __ffs(int(hit)) - 1;  // exactly one lane holds the rank
+        need -= int(__shfl_sync(0xffffffffu, gt, d));
+        const int m = int(__shfl_sync(0xffffffffu, cnt, d));  // keys with digit d
+        prefix |= unsigned(d) << shift;
+        mask |= 15u << shift;
+        if (shift == 0) break;
+        if (m <= 32) {
+            // Gather the m keys that match prefix (a warp scan of each
+            // thread's count, one shared add per warp for its base).
+            int mine = 0;
+            if (regs) {
+#pragma unroll
+                for (int k = 0; k < 16; ++k)
+                    mine += k >= lo && k < hi && (__float_as_uint(c[k]) & mask) == prefix;
+            } else {
+                for (int k = lo; k < hi; ++k) mine += (__float_as_uint(srow[k]) & mask) == prefix;
+            }
+            int incl = mine;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int n = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += n;
+            }
+            int base = 0;
+            if (lane == 31 && incl > 0) base = atomicAdd(&fs.ncand, incl);
+            base = __shfl_sync(0xffffffffu, base, 31) + incl - mine;
+            if (mine > 0) {
+                if (regs) {
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) {
+                        const unsigned key = __float_as_uint(c[k]);
+                        if (k >= lo && k < hi && (key & mask) == prefix) fs.cand[base++] = key;
+                    }
+                } else {
+                    for (int k = lo; k < hi; ++k) {
+                        const unsigned key = __float_as_uint(srow[k]);
+                        if ((key & mask) == prefix) fs.cand[base++] = key;
+                    }
+                }
+            }
+            sync256();
+            // Every warp settles the remaining bits from the same m keys.
+            const unsigned key = lane < m ? fs.cand[lane] : 0u;
+            for (int bit = shift - 1; bit >= 0; --bit) {
+                const unsigned ones = unsigned(__popc(int(__ballot_sync(
+                    0xffffffffu, lane < m && (key & mask) == prefix && ((key >> bit) & 1u)))));
+                if (unsigned(need) <= ones) prefix |= 1u << bit;
+                else need -= int(ones);
+                mask |= 1u << bit;
+            }
+            break;
+        }
+        shift -= 4;
+    }
+    *K_out = prefix;
+    *need_out = need;
+}
+
+__device__ void finish_fast(const ScoreArgs &a, uint8_t *ring) {
+    __shared__ FastSmem fs;
+    const int B = a.B, g = a.gamma, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int pitch = g | 1;
+    const FastLayout f = fast_layout(B, g, a.pack);
+    int *ri = reinterpret_cast<int *>(ring);
+    float *keys = reinterpret_cast<float *>(ring);
+    const int b = tid;
+    const bool own = b < B;
+    float *srow = keys + b * pitch;
+    if (tid == 0) fs.ncand = 0;  // ordered before its use by the barriers between
+
+    // Survival curve and L0 of request b, 16 positions at a time.  S does
+    // not increase with k (each factor is at most 1 and rounding is
+    // monotone), so the k >= 1 with S_k >= c are exactly 1..L0_b.  The
+    // first 16 confidences are loaded before the packing inputs are staged,
+    // so that both sets of loads are in flight together.
+    int l0 = 0;
+    unsigned kfirst = 0u, klast = ~0u;
+    const bool vec = (g & 3) == 0 &&
+                     ((reinterpret_cast<uintptr_t>(a.conf) |
+                       reinterpret_cast<uintptr_t>(a.survival)) & 15) == 0;
+    const float *crow = a.conf + size_t(own ? b : 0) * g;
+    float *orow = a.survival + size_t(own ? b : 0) * g;
+    float c[16];
+    load_conf16(crow, 0, own ? g : 0, vec, c);
+    if (a.pack) {
+        const int ntok = B * g;
+        int tv[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const int i = j * kThreads + tid;
+            tv[j] = i < ntok ? __ldg(a.draft_tokens + i) : 0;
+        }
+        const int lt = own && a.last_tokens ? __ldg(a.last_tokens + b) : -1;
+        const int sq = own && a.seq_lens ? __ldg(a.seq_lens + b) : 0;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const int i = j * kThreads + tid;
+            if (i < ntok) ri[f.tok + i] = tv[j];
+        }
+        if (own) {
+            ri[f.last + b] = lt;
+            ri[f.seq + b] = sq;
+        }
+        if (ntok > 16 * kThreads)
+            stage_ints(ri + f.tok + 16 * kThreads, a.draft_tokens + 16 * kThreads,
+                       ntok - 16 * kThreads);
+    }
+    if (own) {
+        float S = 1.f;
+        for (int k0 = 0; k0 < g; k0 += 16) {
+            if (k0 > 0) load_conf16(crow, k0, g, vec, c);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                if (k0 + j < g) {
+                    S *= c[j];
+                    c[j] = S;
+                    srow[k0 + j] = S;
+                    l0 += S >= a.cost_c;
+                }
+            }
+            if (vec) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (k0 + 4 * q < g)
+                        reinterpret_cast<float4 *>(orow + k0)[q] =
+                            make_float4(c[4 * q], c[4 * q + 1], c[4 * q + 2], c[4 * q + 3]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    if (k0 + j < g) orow[k0 + j] = c[j];
+            }
+        }
+        a.L0[b] = l0;
+        if (l0 > 0) {
+            kfirst = __float_as_uint(srow[0]);
+            klast = __float_as_uint(srow[l0 - 1]);
+        }
+    }
+
+    // sum L0, largest and smallest key
+    {
+        const int ws = __reduce_add_sync(0xffffffffu, l0);
+        const unsigned wmax = __reduce_max_sync(0xffffffffu, kfirst);
+        const unsigned wmin = __reduce_min_sync(0xffffffffu, klast);
+        if (lane == 0) {
+            fs.red[warp][0] = ws;
+            fs.red[warp][1] = int(wmax);
+            fs.red[warp][2] = int(wmin);
+        }
+    }
+    sync256();
+    int total = 0;
+    unsigned kmax = 0u, kmin = ~0u;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        total += fs.red[w][0];
+        kmax = max(kmax, unsigned(fs.red[w][1]));
+        kmin = min(kmin, unsigned(fs.red[w][2]));
+    }
+
+    int L = l0;
+    if (a.cap_T >= 0 && total > a.cap_T) {
+        if (a.cap_T == 0) {
+            L = 0;
+        } else {
+            unsigned K;
+            int need;
+            const bool regs = g <= 16;
+            fast_select(a, fs, srow, c, regs, l0, kmax, kmin, &K, &need);
+            // Keys above K are kept; of those equal to K, the first `need`
+            // in (b, k) order.
+            int above = 0, equal = 0;
+            if (regs) {
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const unsigned key = __float_as_uint(c[k]);
+                    above += k < l0 && key > K;
+                    equal += k < l0 && key == K;
+                }
+            } else {
+                for (int k = 0; k < l0; ++k) {
+                    const unsigned key = __float_as_uint(srow[k]);
+                    above += key > K;
+                    equal += key == K;
+                }
+            }
+            int tot_eq;
+            const int ex = block_excl_scan_int(equal, &tot_eq, fs.sh);
+            L = above + min(max(need - ex, 0), equal);
+        }
+    }
+
+    // Offsets (the scan's barriers also retire every read of the keys).
+    int tot_L;
+    const int ex = block_excl_scan_int(L, &tot_L, fs.sh);
+    if (own) {
+        a.L[b] = L;
+        a.draft_off[b] = ex;
+        a.row_off[b] = ex + b;
+    }
+    if (tid == 0) {
+        a.draft_off[B] = tot_L;
+        a.row_off[B] = tot_L + B;
+    }
+    if (!a.pack) return;
+
+    // Packing: the request of every packed row into shared memory, then
+    // the four packed arrays written row by row.
+    const int cap = B * (g + 1), n_rows = tot_L + B;
+    if (own) {
+        ri[f.roff + b] = ex + b;
+        for (int j = 0; j <= L; ++j) ri[ex + b + j] = b;
+    }
+    sync256();
+#pragma unroll 4
+    for (int r = tid; r < n_rows; r += kThreads) {
+        const int rb = ri[r], j = r - ri[f.roff + rb];
+        a.packed_ids[r] = j == 0 ? ri[f.last + rb] : ri[f.tok + rb * g + j - 1];
+        a.packed_pos[r] = ri[f.seq + rb] + j;
+        a.row_req[r] = rb;
+        a.row_k[r] = j;
+    }
+#pragma unroll 4
+    for (int r = n_rows + tid; r < cap; r += kThreads) {
+        a.packed_ids[r] = -1;
+        a.packed_pos[r] = 0;
+        a.row_req[r] = -1;
+        a.row_k[r] = -1;
+    }
+}
+
+__device__ void finish_batch(const ScoreArgs &a, uint8_t *ring) {
+    if (fast_finish_fits(a)) finish_fast(a, ring);
+    else finish_general(a, ring);
 }
 
 // Steps a1-a3: streaming confidence head (or, with kEntropy, the entropy of
@@ -683,10 +1153,6 @@ __device__ __forceinline__ void score_main(const ScoreArgs &a) {
     extern __shared__ __align__(1024) uint8_t ring[];
     __shared__ ScoreSmem sm;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // Let the next kernel on the stream (the compaction, a programmatic
-    // dependent launch) be scheduled now; it waits for this grid to complete
-    // before it reads anything.
-    asm volatile("griddepcontrol.launch_dependents;");
     if (tid < kScoreStages) {
         mbar_init(&sm.full[tid], 1);
         mbar_init(&sm.empty[tid], kWarps);
@@ -697,6 +1163,18 @@ __device__ __forceinline__ void score_main(const ScoreArgs &a) {
         fence_barrier_init();
     }
     if (!kEntropy && tid < a.gamma) sm.tau[tid] = a.sts_tau[tid];
+    if (a.pack) {
+        // Only the finishing CTA reads the packing inputs, at the end: bring
+        // them into L2 now, one 128-byte line per thread across the grid.
+        const size_t line = size_t(blockIdx.x) * kScoreThreads + tid;
+        const size_t tok_lines = (size_t(a.B) * a.gamma * 4 + 127) / 128;
+        const size_t req_lines = (size_t(a.B) * 4 + 127) / 128;
+        if (line < tok_lines) prefetch_l2(a.draft_tokens + line * 32);
+        else if (line < tok_lines + req_lines && a.last_tokens)
+            prefetch_l2(a.last_tokens + (line - tok_lines) * 32);
+        else if (line < tok_lines + 2 * req_lines && a.seq_lens)
+            prefetch_l2(a.seq_lens + (line - tok_lines - req_lines) * 32);
+    }
     __syncthreads();
     const RowShape rs = row_shape(a, int(sizeof(T)));
     if (warp == kWarps) {
@@ -706,14 +1184,26 @@ __device__ __forceinline__ void score_main(const ScoreArgs &a) {
     const int nrows = kEntropy ? entropy_consumer<T>(a, sm, ring, rs, warp, lane)
                                : score_consumer<T>(a, sm, ring, rs, warp, lane);
     // Publish this CTA's confidences; the CTA that adds the batch's last
-    // rows finishes every request and runs the cap.
-    __threadfence();
+    // rows finishes every request and runs the cap.  The barrier orders
+    // every warp's confidence stores before thread 0's release fence and
+    // count; the finishing CTA's thread 0 fences again (acquire) before the
+    // barrier that lets its warps read every CTA's confidences from L2.
     sync256();
-    if (tid == 0) sm.run_cap = atomicAdd(a.done_cnt, nrows) + nrows == rs.rows;
+    if (tid == 0) {
+        __threadfence();
+        sm.run_cap = atomicAdd(a.done_cnt, nrows) + nrows == rs.rows;
+        if (sm.run_cap) __threadfence();
+    }
     sync256();
     if (!sm.run_cap) return;
-    __threadfence();
-    finish_and_budget(a, ring);
+    // Let the next kernel on the stream (the compaction or the verify, a
+    // programmatic dependent launch) be scheduled now: every other CTA has
+    // exited, so its CTAs take the freed slots in order.  It waits for this
+    // grid to complete before it reads anything.  (Triggered at the start of
+    // the kernel instead, its CTAs took slots as streaming CTAs exited and
+    // the verify ran ~5 us slower.)
+    asm volatile("griddepcontrol.launch_dependents;");
+    finish_batch(a, ring);
     if (tid == 0) {
         *a.done_cnt = 0;
         *a.row_ctr = 0;
@@ -732,10 +1222,43 @@ __global__ void __launch_bounds__(kScoreThreads, 3) score_entropy_kernel(const S
 
 __global__ void __launch_bounds__(kThreads) fixed_budget_kernel(const FixedArgs a) {
     __shared__ int sh[kWarps + 1];
+    asm volatile("griddepcontrol.launch_dependents;");
     const int l = a.F < a.gamma ? a.F : a.gamma;
     for (int b = threadIdx.x; b < a.B; b += kThreads) a.L[b] = l;
     __syncthreads();
     write_offsets(a.B, a.L, a.draft_off, a.row_off, sh);
+}
+
+// Fixed budget with the packing (steps a3 and a4 of the fixed mode): every
+// L_b = l = min(F, gamma), so draft_off[b] = b * l and row_off[b] =
+// b * (l + 1) in closed form and every slot is independent: one thread per
+// slot (b, j) of the B*(gamma+1) capacity, as in the compaction kernel.
+__global__ void __launch_bounds__(kThreads) fixed_pack_kernel(const FixedArgs a) {
+    asm volatile("griddepcontrol.launch_dependents;");
+    const int l = a.F < a.gamma ? a.F : a.gamma;
+    const int g1 = a.gamma + 1, cap = a.B * g1, n_rows = a.B * (l + 1);
+    const int t = blockIdx.x * kThreads + threadIdx.x;
+    if (t <= a.B) {
+        if (t < a.B) a.L[t] = l;
+        a.draft_off[t] = t * l;
+        a.row_off[t] = t * (l + 1);
+    }
+    if (t >= cap) return;
+    const int b = t / g1, j = t - b * g1;
+    if (j <= l) {
+        const int r = b * (l + 1) + j;
+        a.packed_ids[r] = j == 0 ? (a.last_tokens ? a.last_tokens[b] : -1)
+                                 : a.draft_tokens[size_t(b) * a.gamma + j - 1];
+        a.packed_pos[r] = (a.seq_lens ? a.seq_lens[b] : 0) + j;
+        a.row_req[r] = b;
+        a.row_k[r] = j;
+    }
+    if (t >= n_rows) {
+        a.packed_ids[t] = -1;
+        a.packed_pos[t] = 0;
+        a.row_req[t] = -1;
+        a.row_k[t] = -1;
+    }
 }
 
 }  // namespace
@@ -774,7 +1297,12 @@ cudaError_t launch_score_entropy(const ScoreArgs &a, int grid, cudaStream_t s) {
 }
 
 cudaError_t launch_fixed_budget(const FixedArgs &a, cudaStream_t s) {
-    fixed_budget_kernel<<<1, kThreads, 0, s>>>(a);
+    if (a.pack) {
+        const long long slots = std::max<long long>((long long)a.B * (a.gamma + 1), a.B + 1LL);
+        fixed_pack_kernel<<<int((slots + kThreads - 1) / kThreads), kThreads, 0, s>>>(a);
+    } else {
+        fixed_budget_kernel<<<1, kThreads, 0, s>>>(a);
+    }
     return cudaGetLastError();
 }
 

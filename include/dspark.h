@@ -13,6 +13,9 @@
  *   dspark_verify        vocab-wide softmax of target and draft rows,
  *                        accept / resample / bonus, commit.
  *
+ * dspark_score_compact is the first two calls in one kernel launch, with
+ * the same outputs.
+ *
  * Variants: dspark_score_entropy scores drafts by the entropy of their
  * distribution instead of the head; dspark_verify_cap_accept is the audit arm
  * that verifies the full block and commits the scheduled window;
@@ -184,6 +187,19 @@ dspark_status dspark_workspace_init(void *workspace, size_t workspace_bytes,
  * draft_off, row_off.
  */
 dspark_status dspark_score_budget(const dspark_step *step, dspark_stream_t stream);
+
+/*
+ * Steps a1-a4 in one launch: dspark_score_budget followed by dspark_compact,
+ * with the same outputs bit for bit.  The CTA that computes the batch's
+ * lengths also writes the packing, so no second kernel and no launch gap
+ * sit between the budget and the packed rows.  With fixed_budget >= 0 one
+ * thread per packing slot writes L, the offsets (closed form) and the
+ * packing.
+ * Reads what the two calls read; writes what they write.  Errors: those of
+ * dspark_score_budget, and DSPARK_EINVAL for a NULL draft_tokens, packed_ids,
+ * packed_pos, row_req or row_k.
+ */
+dspark_status dspark_score_compact(const dspark_step *step, dspark_stream_t stream);
 
 /*
  * Steps a1-a3 with the entropy-confidence variant of step a1.  [KC] "DSpark's

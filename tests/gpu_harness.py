@@ -38,19 +38,24 @@ def to_device(inp: dict, device="cuda") -> dict:
 
 
 def gpu_step(inp_dev: dict, seq_lens_commit: bool = True, bufs=None, stream=None,
-             entropy_theta=None):
+             entropy_theta=None, fused: bool = False):
     """score_budget (or score_entropy) -> compact -> (target-forward
-    stand-in) -> verify."""
+    stand-in) -> verify.  ``fused``: dspark_score_compact in place of the
+    first two calls."""
     B, g, V, d = inp_dev["B"], inp_dev["gamma"], inp_dev["V"], inp_dev["d"]
     if bufs is None:
         bufs = binding.StepBuffers(B, g, V, d, stream=stream)
     commit = inp_dev["seq_lens"].clone() if seq_lens_commit else None
     bufs.bind(inp_dev, seq_lens_commit=commit)
-    if entropy_theta is None:
-        binding.dspark_score_budget(bufs.step, stream)
+    if fused:
+        assert entropy_theta is None
+        binding.dspark_score_compact(bufs.step, stream)
     else:
-        binding.dspark_score_entropy(bufs.step, entropy_theta, stream)
-    binding.dspark_compact(bufs.step, stream)
+        if entropy_theta is None:
+            binding.dspark_score_budget(bufs.step, stream)
+        else:
+            binding.dspark_score_entropy(bufs.step, entropy_theta, stream)
+        binding.dspark_compact(bufs.step, stream)
     torch.cuda.synchronize()
     n_rows = int(bufs.row_off[B].item()) if B > 0 else 0
     tgt = workloads.ragged_target_rows(inp_dev["target_dense"], bufs.row_req, bufs.row_k,

@@ -93,7 +93,7 @@ def valid_step(B=4, gamma=8, V=1024, d=256):
     return s
 
 
-CALLS = ["dspark_score_budget", "dspark_compact", "dspark_verify"]
+CALLS = ["dspark_score_budget", "dspark_score_compact", "dspark_compact", "dspark_verify"]
 
 
 @pytest.mark.parametrize("call", CALLS)
@@ -119,8 +119,9 @@ def test_empty_batch_is_a_no_op(lib, call):
     assert getattr(lib, call)(ctypes.byref(s), None) == binding.DSPARK_OK
 
 
-def test_score_budget_validation(lib):
-    f = lib.dspark_score_budget
+@pytest.mark.parametrize("call", ["dspark_score_budget", "dspark_score_compact"])
+def test_score_budget_validation(lib, call):
+    f = getattr(lib, call)
     s = valid_step(); s.L = None
     assert f(ctypes.byref(s), None) == binding.DSPARK_EINVAL
     s = valid_step(); s.hidden = None
@@ -140,6 +141,23 @@ def test_score_budget_validation(lib):
     assert f(ctypes.byref(s), None) == binding.DSPARK_EWORKSPACE
     s = valid_step(); s.workspace = FAKE + 16
     assert f(ctypes.byref(s), None) == binding.DSPARK_EWORKSPACE
+
+
+@pytest.mark.parametrize("field", ["draft_tokens", "packed_ids", "packed_pos", "row_req", "row_k"])
+@pytest.mark.parametrize("fixed", [False, True])
+def test_score_compact_needs_the_packing_buffers(lib, field, fixed):
+    s = valid_step()
+    if fixed:
+        s.fixed_budget = 3
+    setattr(s, field, None)
+    assert lib.dspark_score_compact(ctypes.byref(s), None) == binding.DSPARK_EINVAL
+    assert field in binding.last_error() and "dspark_score_compact" in binding.last_error()
+    # the unfused call does not read them
+    if field != "draft_tokens":
+        s2 = valid_step()
+        setattr(s2, field, None)
+        s2.workspace = None  # stops before any launch
+        assert lib.dspark_score_budget(ctypes.byref(s2), None) == binding.DSPARK_EWORKSPACE
 
 
 def test_compact_validation(lib):

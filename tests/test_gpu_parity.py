@@ -17,8 +17,8 @@ from tests.gpu_harness import compare_with_oracle, gpu_step, outputs_of, to_devi
 pytestmark = pytest.mark.gpu
 
 
-def run_and_compare(inp_cpu, **kw):
-    gpu, bufs = gpu_step(to_device(inp_cpu))
+def run_and_compare(inp_cpu, fused=False, **kw):
+    gpu, bufs = gpu_step(to_device(inp_cpu), fused=fused)
     stats = compare_with_oracle(W.to_numpy(inp_cpu), gpu, **kw)
     # the near-tie counts of every case (shown with pytest -s)
     print(f"parity {inp_cpu['workload']} B={inp_cpu['B']} V={inp_cpu['V']} "
@@ -59,9 +59,11 @@ def test_fixed_budget(cuda_lib, F):
 
 
 # The cap's candidate sets on either side of the kernel's shared-memory
-# limits: 4096 listed keys, 8192 survival values held on chip.
+# limits.  Up to 256 requests one thread each holds a request's keys (the
+# fast finish); past that the general finish lists up to 4096 keys and holds
+# up to 8192 survival values on chip.
 @pytest.mark.parametrize("B,T,c", [
-    (256, 1000, 0.0),    # exactly 4096 candidates: the listed select
+    (256, 1000, 0.0),    # 4096 candidates, one request per thread
     (400, 2000, 0.0),    # 6400 candidates, curves on chip: the unlisted select
     (600, 5000, 0.0),    # 9600 candidates, curves re-read from memory
     (600, 700, 0.45),    # curves re-read from memory, fewer candidates
@@ -186,11 +188,12 @@ def test_graph_replay_matches_direct_calls(cuda_lib, Tm):
         compare_with_oracle(W.to_numpy(inp_cpu), outputs_of(bufs, commit))
 
 
-def _graph_over_totals(workload, steps, B, V, d, min_totals, temperature=1.0):
-    """One capture of the step -- score, compact, a fixed-shape target
-    stand-in over the batch's capacity of rows, verify -- replayed on input
-    sets whose packed totals differ.  Each replay equals direct calls on that
-    set and the oracle.  Returns the packed totals seen."""
+def _graph_over_totals(workload, steps, B, V, d, min_totals, temperature=1.0, fused=False):
+    """One capture of the step -- score, compact (or the fused
+    dspark_score_compact), a fixed-shape target stand-in over the batch's
+    capacity of rows, verify -- replayed on input sets whose packed totals
+    differ.  Each replay equals direct calls on that set and the oracle.
+    Returns the packed totals seen."""
     from confidence_driven_speculative_gb300 import binding
     sets_cpu = [W.make_inputs(workload, s, B=B, V=V, d=d, cap_T=-1, temperature=temperature)
                 for s in steps]
@@ -209,8 +212,11 @@ def _graph_over_totals(workload, steps, B, V, d, min_totals, temperature=1.0):
     flat = live["target_dense"].view(B * g1, V)
 
     def step():
-        binding.dspark_score_budget(bufs.step)
-        binding.dspark_compact(bufs.step)
+        if fused:
+            binding.dspark_score_compact(bufs.step)
+        else:
+            binding.dspark_score_budget(bufs.step)
+            binding.dspark_compact(bufs.step)
         idx = (bufs.row_req.clamp(min=0) * g1 + bufs.row_k.clamp(min=0)).long()
         torch.index_select(flat, 0, idx, out=tgt)
         binding.dspark_verify(bufs.step)
@@ -254,37 +260,46 @@ def test_one_graph_serves_every_packed_total(cuda_lib):
     _graph_over_totals(W.MIXED_B256, range(40, 44), 24, 20000, 128, min_totals=3)
 
 
+def test_one_graph_of_the_fused_call_serves_every_packed_total(cuda_lib):
+    """As above with dspark_score_compact captured in place of the first
+    two calls (the verify then depends on the score kernel directly)."""
+    _graph_over_totals(W.MIXED_B256, range(40, 44), 24, 20000, 128, min_totals=3, fused=True)
+
+
 def test_one_graph_serves_the_b1_latency_shape(cuda_lib):
     """The B=1 latency shape (V = 129280, d = 7168) through one captured
     graph over several steps (its own greedy verify, then sampling), each
     replay checked against the oracle."""
     w = W.LATENCY_B1
     for Tm in (None, 1.0):
-        _graph_over_totals(w, range(5), 1, w.V, w.d, min_totals=1, temperature=Tm)
+        for fused in (False, True):
+            _graph_over_totals(w, range(5), 1, w.V, w.d, min_totals=1, temperature=Tm,
+                               fused=fused)
 
 
 def test_empty_batch(cuda_lib):
     from confidence_driven_speculative_gb300 import binding
     step = binding.DsparkStep()
     step.B, step.gamma, step.V, step.d = 0, 4, 16, 8
-    for fn in (binding.dspark_score_budget, binding.dspark_compact, binding.dspark_verify):
+    for fn in (binding.dspark_score_budget, binding.dspark_score_compact, binding.dspark_compact,
+               binding.dspark_verify):
         assert fn(step) == binding.DSPARK_OK
 
 
 def test_qwen3_8b_shape(cuda_lib):
     for step in range(2):
-        run_and_compare(W.make_inputs(W.QWEN3_8B, step))
+        run_and_compare(W.make_inputs(W.QWEN3_8B, step), fused=step == 1)
 
 
 def test_latency_b1(cuda_lib):
     for step in range(3):
-        run_and_compare(W.make_inputs(W.LATENCY_B1, step))
+        run_and_compare(W.make_inputs(W.LATENCY_B1, step), fused=step > 0)
 
 
 @pytest.mark.slow
 def test_mixed_b256_dynamic(cuda_lib):
     for step in range(2):
-        _, stats, _ = run_and_compare(W.make_inputs(W.MIXED_B256, step))
+        _, stats, _ = run_and_compare(W.make_inputs(W.MIXED_B256, step), fused=step == 1)
 
 
 @pytest.mark.slow
