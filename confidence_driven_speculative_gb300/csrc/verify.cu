@@ -131,6 +131,13 @@ __device__ __forceinline__ int ld_relaxed(const int *p) {
 __device__ __forceinline__ void st_relaxed(int *p, int v) {
     asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
+// Release / acquire at GPU scope for the queues, books and join counters:
+// with a relaxed store or atomic after it, a release pattern; with one
+// before it, an acquire pattern.  Lighter than the sequentially consistent
+// fence, which nothing here needs.
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
 
 // Cross-CTA state is read through L2 only (never a possibly stale L1 line).
 __device__ __forceinline__ DecideState load_state(const VerifyArgs &a, int b) {
@@ -277,7 +284,7 @@ __device__ void push_resid_jobs(const VerifyArgs &a, int b, int epoch) {
     const int pos = atomicAdd(&a.q_ctr[QA_TAIL], a.nc);
     for (int i = 0; i < a.nc; ++i)
         if (pos + i < a.qcap) a.q_job[pos + i] = make_int2(b, i);
-    __threadfence();  // every payload (and the caller's state) before any ready word
+    fence_acq_rel_gpu();  // every payload (and the caller's state) before any ready word
     for (int i = 0; i < a.nc; ++i)
         if (pos + i < a.qcap) st_relaxed(&a.q_ready[pos + i], epoch);
 }
@@ -289,7 +296,7 @@ __device__ void push_decide(const VerifyArgs &a, int job, int epoch) {
     const int pos = atomicAdd(&a.q_ctr[QB_TAIL], 1);
     if (pos < a.qbcap) {
         a.qb_job[pos] = job;
-        __threadfence();
+        fence_acq_rel_gpu();
         st_relaxed(&a.qb_ready[pos], epoch);
     }
 }
@@ -376,11 +383,14 @@ __device__ __forceinline__ void fetch_step(const VerifyArgs &a, const StreamShap
     }
 }
 
-// Books of the stages the producer gets back: stream tiles are counted per
+// Books of the stages the producer gets back: tiles are counted per
 // (request, kind) locally and published with one fenced atomic per change.
 // Decision-row tiles complete a request's decide job.  Bonus-row tiles
 // complete its bonus row; the bonus draw then runs once the decide has
 // accepted every draft (join counter), at once when there are no drafts.
+// Residual tiles complete the request's residual masses and start the
+// draw.  (Counted instead by a fenced atomic in each consumer warp, the
+// residual tiles stalled the warps behind those fences.)
 constexpr int kFinishResidual = 1 << 30;  // decider job: finish the residual draw
 constexpr int kBonusDraw = 1 << 29;       // decider job: the bonus draw
 
@@ -397,6 +407,7 @@ __device__ void check_books(const VerifyArgs &a, Books &bk, int epoch) {
     const int b = bk.chk_b;
     if (bk.chk_old == bk.chk_end) {
         if (bk.chk_kind == 0) push_decide(a, b, epoch);
+        else if (bk.chk_kind == 2) push_decide(a, b | kFinishResidual, epoch);
         else if (bk.chk_Lb == 0 || atomicAdd(&a.join[b], 1) == 1) push_decide(a, b | kBonusDraw, epoch);
     }
     bk.chk_b = -1;
@@ -405,9 +416,10 @@ __device__ void check_books(const VerifyArgs &a, Books &bk, int epoch) {
 __device__ void flush_books(const VerifyArgs &a, Books &bk, int epoch) {
     if (bk.acc_n == 0) return;
     check_books(a, bk, epoch);
-    __threadfence();
+    fence_acq_rel_gpu();
     const int b = bk.acc_b;
-    bk.chk_old = atomicAdd(bk.acc_kind == 0 ? &a.req_cnt[b] : &a.bon_cnt[b], bk.acc_n);
+    int *cnt = bk.acc_kind == 0 ? a.req_cnt : bk.acc_kind == 1 ? a.bon_cnt : a.r1_cnt;
+    bk.chk_old = atomicAdd(&cnt[b], bk.acc_n);
     bk.chk_b = b;
     bk.chk_kind = bk.acc_kind;
     bk.chk_end = bk.acc_total - bk.acc_n;  // the count before ours when ours completes it
@@ -417,8 +429,9 @@ __device__ void flush_books(const VerifyArgs &a, Books &bk, int epoch) {
 
 __device__ __forceinline__ void account(const VerifyArgs &a, Books &bk, const TaskInfo &t,
                                         int epoch) {
-    if (t.type != T_STREAM) return;
-    const int kind = t.k < t.Lb ? 0 : 1;
+    if (t.type == T_EXIT) return;
+    // 0: decision rows, 1: bonus row, 2: residual row
+    const int kind = t.type == T_RESID ? 2 : t.k < t.Lb ? 0 : 1;
     if (t.b != bk.acc_b || kind != bk.acc_kind) {
         flush_books(a, bk, epoch);
         bk.acc_b = t.b;
@@ -630,7 +643,9 @@ __device__ void finish_request(const VerifyArgs &a, int b, int acc, int token, c
         a.req_cnt[b] = 0;
         a.r1_cnt[b] = 0;
     }
-    __threadfence();
+    // No fence: nothing in the kernel reads the outputs; the count only
+    // tells the waiting warps when to leave, and the kernel's end publishes
+    // the outputs.
     __syncwarp();
     if (lane == 0) atomicAdd(&a.q_ctr[Q_FINISHED], 1);
 }
@@ -1065,11 +1080,11 @@ __device__ void decide_request(const VerifyArgs &a, const StreamShape &sh, int b
     // Every draft accepted: the bonus draw, if the bonus row is in already.
     int go = 0;
     if (lane == 0) {
-        __threadfence();
+        fence_acq_rel_gpu();
         go = atomicAdd(&a.join[b], 1) == 1;
     }
     if (__shfl_sync(0xffffffffu, go, 0)) {
-        __threadfence();
+        fence_acq_rel_gpu();
         bonus_draw<T>(a, sh, b, wpb, lane);
     }
 }
@@ -1281,19 +1296,16 @@ __device__ void consumer(const VerifyArgs &a, VSmem &sm, const uint8_t *ring,
                 }
             }
             const F2 dr = warp_sum_f2(f2(zr)), dp = warp_sum_f2(f2(zp));
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.empty[s]);  // the stage is no longer read
+            // The masses are written before the stage is released: the
+            // producer books the tile (and publishes it) once all eight warps
+            // have released it.
             const int y = t.y0 + warp * tpw;
             const int blk = y / kSampleBlock;
-            int last = 0;
-            if (lane == 0) {
-                if (blk < a.nblk)
-                    a.zrec[(size_t(t.b) * a.nblk + blk) * kCW + (y % kSampleBlock) / tpw] =
-                        make_float2(dr.hi + dr.lo, dp.hi + dp.lo);
-                __threadfence();
-                last = atomicAdd(&a.r1_cnt[t.b], 1) == a.nc * kCW - 1;
-            }
-            if (lane == 0 && last) push_decide(a, t.b | kFinishResidual, epoch);
+            if (lane == 0 && blk < a.nblk)
+                a.zrec[(size_t(t.b) * a.nblk + blk) * kCW + (y % kSampleBlock) / tpw] =
+                    make_float2(dr.hi + dr.lo, dp.hi + dp.lo);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.empty[s]);
         }
     }
 }
@@ -1327,8 +1339,7 @@ __device__ void decider(const VerifyArgs &a, const StreamShape &sh, int epoch, i
             }
         }
         b = __shfl_sync(0xffffffffu, b, 0);
-        if (b < 0) return;
-        __threadfence();
+        if (b < 0) return;  // the ready word was read with acquire: no fence needed
         if (b & kFinishResidual) finish_residual<T>(a, b & ~kFinishResidual, wpb, lane);
         else if (b & kBonusDraw) bonus_draw<T>(a, sh, b & ~kBonusDraw, wpb, lane);
         else decide_request<T>(a, sh, b, wpb, epoch, lane);
