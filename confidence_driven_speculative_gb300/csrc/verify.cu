@@ -269,6 +269,15 @@ __device__ __forceinline__ F2 warp_sum_f2(F2 v) {
     return v;
 }
 
+// Two-float sum of eight floats, pairwise (three levels instead of a chain
+// of eight).
+__device__ __forceinline__ F2 sum8_f2(const float (&v)[kConsumerWarps]) {
+    static_assert(kConsumerWarps == 8, "eight slots");
+    const F2 a = (f2(v[0]) + f2(v[1])) + (f2(v[2]) + f2(v[3]));
+    const F2 b = (f2(v[4]) + f2(v[5])) + (f2(v[6]) + f2(v[7]));
+    return a + b;
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -652,9 +661,31 @@ __device__ void finish_request(const VerifyArgs &a, int b, int acc, int token, c
 
 // Choose a sampling block: the smallest i whose running mass exceeds
 // u * total; the last block with positive mass if rounding leaves no
-// crossing.  mass(i) is evaluated by the lane that owns i.
+// crossing.  mass(i) is evaluated by the lane that owns i.  Up to 64
+// blocks, each lane's masses are evaluated once and the total is the last
+// running mass (so it agrees with the scan exactly); more blocks take two
+// sweeps.
 template <typename F>
 __device__ int choose_block(int nblk, float u, F mass, int lane) {
+    if (nblk <= 64) {
+        const F2 m0 = lane < nblk ? mass(lane) : f2(0.f);
+        const F2 m1 = lane + 32 < nblk ? mass(lane + 32) : f2(0.f);
+        const F2 i0 = warp_scan_incl(m0, lane);
+        F2 i1 = f2(0.f), total = f2_shfl(i0, 31);
+        if (nblk > 32) {
+            i1 = total + warp_scan_incl(m1, lane);
+            total = f2_shfl(i1, 31);
+        }
+        const F2 target = f2_scale(total, u);
+        unsigned hit = __ballot_sync(0xffffffffu, lane < nblk && f2_gt(i0, target));
+        if (hit) return __ffs(hit) - 1;
+        hit = __ballot_sync(0xffffffffu, lane + 32 < nblk && f2_gt(i1, target));
+        if (hit) return 32 + __ffs(hit) - 1;
+        unsigned pos = __ballot_sync(0xffffffffu, lane + 32 < nblk && m1.hi > 0.f);
+        if (pos) return 32 + 31 - __clz(pos);
+        pos = __ballot_sync(0xffffffffu, lane < nblk && m0.hi > 0.f);
+        return pos ? 31 - __clz(pos) : 0;
+    }
     F2 total = f2(0.f);
     for (int t0 = 0; t0 < nblk; t0 += 32) {
         const int i = t0 + lane;
@@ -906,9 +937,12 @@ __device__ void bonus_draw(const VerifyArgs &a, const StreamShape &sh, int b, in
         if (q < kCache) {
 #pragma unroll
             for (int c = 0; c < kCache; ++c)
-                if (q == c)
+                if (q == c) {
+                    float v[kCW];
 #pragma unroll
-                    for (int w = 0; w < kCW; ++w) m = m + f2(smass(sl[c][w]));
+                    for (int w = 0; w < kCW; ++w) v[w] = smass(sl[c][w]);
+                    m = sum8_f2(v);
+                }
         } else {
             const float2 *p = a.blkrec + (size_t(b) * a.nblk + i) * kCW;
             for (int w = 0; w < wpb; ++w) m = m + f2(smass(__ldcg(p + w)));
@@ -1113,9 +1147,12 @@ __device__ void finish_residual(const VerifyArgs &a, int b, int wpb, int lane) {
         if (q < kCache) {
 #pragma unroll
             for (int c = 0; c < kCache; ++c)
-                if (q == c)
+                if (q == c) {
+                    float v[kCW];
 #pragma unroll
-                    for (int w = 0; w < kCW; ++w) m = m + f2(residual ? sl[c][w].x : sl[c][w].y);
+                    for (int w = 0; w < kCW; ++w) v[w] = residual ? sl[c][w].x : sl[c][w].y;
+                    m = sum8_f2(v);
+                }
         } else {
             for (int w = 0; w < wpb; ++w) {
                 const float2 x = __ldcg(z + size_t(i) * kCW + w);
