@@ -41,6 +41,7 @@ struct DeviceInfo {
     bool ready = false;
     int sms = 0;
     int verify_blocks[2] = {0, 0};  // per logit dtype (0 = fp32, 1 = bf16)
+    int tail_blocks[2] = {0, 0};    // the small verify's tail kernel, per logit dtype
     int score_blocks[2] = {0, 0};   // per hidden dtype
     int entropy_blocks[2] = {0, 0}; // per logit dtype
 };
@@ -69,6 +70,9 @@ dspark_status device_info(DeviceInfo **out) {
             if (d.verify_blocks[bf] <= 0)
                 return fail(DSPARK_ECUDA, "verify kernel cannot be resident (smem %zu bytes)",
                             dspark::verify_smem_bytes());
+            d.tail_blocks[bf] = dspark::verify_tail_blocks_per_sm(bf);
+            if (d.tail_blocks[bf] <= 0)
+                return fail(DSPARK_ECUDA, "verify tail kernel cannot be resident");
             d.score_blocks[bf] = dspark::score_blocks_per_sm(bf);
             if (d.score_blocks[bf] <= 0)
                 return fail(DSPARK_ECUDA, "score kernel cannot be resident");
@@ -436,8 +440,24 @@ static dspark_status verify_impl(const dspark_step *s, const int32_t *commit_len
         // CTA that completes a request decides it (verify_small.cu).
         const long long units = (long long)s->B * (s->gamma + 1) * dspark::verify_small_slices(s->V);
         const int grid = int(std::min<long long>(units, (long long)dev->sms * 8));
+        // Rows of four tiles or more and four requests or more: a
+        // rejection's second pass goes to the tail kernel (parts over the
+        // grid).  Smaller rows are cheaper in the deciding CTA than a second
+        // launch, and one to three requests reject too rarely for it to pay
+        // (measured: B = 8 and 16 at V = 151 936 ~10 us faster a step, B = 1
+        // 1.5 us slower, V = 1024 1 us slower).
+        a.small_tail = !greedy && a.nc >= 4 && s->B >= 4;
         e = dspark::launch_verify_small(a, bf, grid, reinterpret_cast<cudaStream_t>(stream));
         if (e != cudaSuccess) return cuda_fail(e, "verify_small_kernel launch");
+        if (a.small_tail) {
+            // The rejections' residual rows, in parts over the grid, and their
+            // draws (at most one row per request, four parts each).
+            const int tgrid = int(std::min<long long>((long long)s->B * 4,
+                                                      (long long)dev->sms * dev->tail_blocks[bf]));
+            e = dspark::launch_verify_tail(a, bf, std::max(tgrid, 1),
+                                           reinterpret_cast<cudaStream_t>(stream));
+            if (e != cudaSuccess) return cuda_fail(e, "verify_tail_kernel launch");
+        }
         return DSPARK_OK;
     }
     // One CTA per resident slot; the work is spread over the grid inside the

@@ -28,6 +28,15 @@ constexpr int32_t kStatusWaitTimeout = 1;   // a wait on the shared-memory copy 
 constexpr int32_t kStatusQueueTimeout = 2;  // a wait on other warps or CTAs (events, grid
                                             // barrier) gave up
 
+// Draw modes of a request (DecideState::mode): the bonus draw from p at row
+// L_b, the residual norm(max(0, p - q)) at row a_b, or p at the drawn row.
+enum : int { D_BONUS = 0, D_RESID = 1, D_FALLBACK = 2 };
+
+// Workspace q_ctr words shared by the small-batch verify and the tail kernel
+// (the persistent verify uses words 0-9).
+constexpr int kQTailExit = 10;   // tail CTAs exited
+constexpr int kQSmallList = 11;  // rows listed for the tail kernel
+
 // Per-request draw state written by the verify kernel's decide step.
 struct DecideState {
     int a;                   // accepted drafts a_b
@@ -375,6 +384,9 @@ struct VerifyArgs {
     const int32_t *commit_len;
     int32_t *accept_full, *audit_totals;
     uint64_t wait_ns;  // bound of every wait
+    // Small-batch verify with sampling: rejections are listed for the tail
+    // kernel instead of drawn by the deciding CTA (rows of >= 4 tiles).
+    int small_tail;
 };
 
 cudaError_t launch_score_budget(const ScoreArgs &a, int grid, cudaStream_t s);
@@ -384,6 +396,11 @@ int entropy_blocks_per_sm(int logit_bf16);
 cudaError_t launch_fixed_budget(const FixedArgs &a, cudaStream_t s);
 cudaError_t launch_compact(const CompactArgs &a, cudaStream_t s);
 cudaError_t launch_verify(const VerifyArgs &a, int logit_bf16, int grid, cudaStream_t s);
+// The residual rows of the requests the small-batch verify listed (row and
+// draw state at q_job / dstate positions 0 .. q_ctr[kQSmallList]), in parts
+// over the grid, and their draws; launched right after launch_verify_small.
+int verify_tail_blocks_per_sm(int logit_bf16);
+cudaError_t launch_verify_tail(const VerifyArgs &a, int logit_bf16, int grid, cudaStream_t s);
 // The small-batch verify (verify_small.cu): which batches it takes, its row
 // slices, and its launch.
 constexpr int kSmallBatchMax = 16;

@@ -65,7 +65,6 @@ constexpr int kStageBytes = 2 * kChunkBytes;  // target tile + draft tile
 constexpr size_t kSmemBytes = size_t(kStages) * kStageBytes;
 
 enum : int { T_EXIT = 0, T_STREAM = 1, T_RESID = 2 };
-enum : int { D_BONUS = 0, D_RESID = 1, D_FALLBACK = 2 };
 // q_ctr words: residual-tile queue head / tail, finished requests, exited CTAs,
 // launch epoch, stream-chunk counter, decide queue head / tail, audit sums.
 enum : int { QA_HEAD = 0, QA_TAIL = 1, Q_FINISHED = 2, Q_EXITED = 3, Q_EPOCH = 4, Q_CHUNK = 5,
@@ -1126,10 +1125,9 @@ __device__ void decide_request(const VerifyArgs &a, const StreamShape &sh, int b
 // Every residual slot of request b is in: choose the block from the masses,
 // then the slot, then the token.
 template <typename T>
-__device__ void finish_residual(const VerifyArgs &a, int b, int wpb, int lane) {
-    // One round of independent loads: state, row offset, drafts, masses.
-    DecideState st = load_state(a, b);
-    const int r0 = a.row_off[b];
+__device__ void finish_residual_at(const VerifyArgs &a, int b, int r, DecideState st, int wpb,
+                                   int lane) {
+    // One round of independent loads: drafts, masses.
     const Drafts dr = load_drafts(a, b, lane);
     const float2 *z = a.zrec + size_t(b) * a.nblk * kCW;
     constexpr int kCache = 2;  // blocks per lane kept in registers (nblk <= 64)
@@ -1192,9 +1190,15 @@ __device__ void finish_residual(const VerifyArgs &a, int b, int wpb, int lane) {
             slot_mass[w] = w < wpb ? m : 0.f;
         }
     }
-    const int token =
-        block_pick<T>(a, st, b, r0 + st.a, blk, slot_mass, wpb, kSampleBlock / wpb, lane);
+    const int token = block_pick<T>(a, st, b, r, blk, slot_mass, wpb, kSampleBlock / wpb, lane);
     finish_request(a, b, st.a, token, dr, lane);
+}
+
+// The residual draw of request b from its state (the stream kernel's).
+template <typename T>
+__device__ void finish_residual(const VerifyArgs &a, int b, int wpb, int lane) {
+    const DecideState st = load_state(a, b);
+    finish_residual_at<T>(a, b, a.row_off[b] + st.a, st, wpb, lane);
 }
 
 // ---------------------------------------------------------------------------
@@ -1441,6 +1445,118 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(const VerifyA
     }
 }
 
+// ---------------------------------------------------------------------------
+// tail kernel (sampling): residual rows and draws
+// ---------------------------------------------------------------------------
+// After the small-batch verify: the second pass over the row of each
+// rejection it listed (the row's residual masses) and the residual draw.
+// One CTA alone needs ~25 us for a 300 KB row pair (a few dozen KB in flight
+// per round trip); here each row is cut into parts over the whole GPU.
+constexpr int kTailThreads = kCW * 32;
+constexpr int kTailRun = kChunkBytes / 16 / kCW / 32;  // 16-byte vectors a lane sums per slot
+constexpr int kTailParts = 4;                          // units per listed row
+constexpr int kTailBatch = 2;                          // tiles whose loads are in flight together
+
+// Tiles [t0, t1) of a listed row -- target row r and draft row (b, a_b):
+// warp w sums max(0, p - q) and p over slot w of each tile, with the lanes
+// and order the stream kernel's consumers use for a slot, and writes the
+// slot's masses.
+template <typename T>
+__device__ void residual_part(const VerifyArgs &a, const DecideState &st, int b, int r, int t0,
+                              int t1, int warp, int lane) {
+    constexpr int VE = Vec<T>::kElems;
+    const int tpw = a.chunk_elems / kCW, vpw = tpw / VE;
+    const float scale = a.scale, iSp = 1.f / st.Sp, iSq = 1.f / st.Sq;
+    const char *trow = static_cast<const char *>(a.target_logits) + size_t(r) * a.row_bytes;
+    const char *drow = static_cast<const char *>(a.draft_logits) +
+                       (size_t(b) * a.gamma + st.a) * size_t(a.row_bytes);
+    for (int j0 = t0; j0 < t1; j0 += kTailBatch) {
+        uint4 xs[kTailBatch][kTailRun], ys[kTailBatch][kTailRun];
+        int v0[kTailBatch], v1[kTailBatch];
+#pragma unroll
+        for (int h = 0; h < kTailBatch; ++h) {
+            const int j = j0 + h;
+            const int nvec = j < t1 ? min(kChunkBytes, a.row_bytes - j * kChunkBytes) / 16 : 0;
+            v0[h] = min(nvec, warp * vpw);
+            v1[h] = min(nvec, v0[h] + vpw);
+            const uint4 *tv = reinterpret_cast<const uint4 *>(trow + size_t(j) * kChunkBytes);
+            const uint4 *dv = reinterpret_cast<const uint4 *>(drow + size_t(j) * kChunkBytes);
+#pragma unroll
+            for (int q = 0; q < kTailRun; ++q) {
+                const int v = v0[h] + lane + 32 * q;
+                xs[h][q] = v < v1[h] ? __ldcg(tv + v) : make_uint4(0, 0, 0, 0);
+                ys[h][q] = v < v1[h] ? __ldcg(dv + v) : make_uint4(0, 0, 0, 0);
+            }
+        }
+#pragma unroll
+        for (int h = 0; h < kTailBatch; ++h) {
+            const int j = j0 + h;
+            if (j >= t1) break;
+            float zr = 0.f, zp = 0.f;
+#pragma unroll
+            for (int q = 0; q < kTailRun; ++q) {
+                if (v0[h] + lane + 32 * q >= v1[h]) continue;
+                float x[VE], y[VE];
+                Vec<T>::unpack(xs[h][q], x);
+                Vec<T>::unpack(ys[h][q], y);
+#pragma unroll
+                for (int e = 0; e < VE; ++e) {
+                    const float pw = exp2_approx((x[e] - st.Mp) * scale);
+                    zp += pw;
+                    zr += fmaxf(0.f, pw * iSp - exp2_approx((y[e] - st.Mq) * scale) * iSq);
+                }
+            }
+            const F2 dr = warp_sum_f2(f2(zr)), dp = warp_sum_f2(f2(zp));
+            const int y = j * a.chunk_elems + warp * tpw;
+            const int blk = y / kSampleBlock;
+            if (lane == 0 && blk < a.nblk)
+                a.zrec[(size_t(b) * a.nblk + blk) * kCW + (y % kSampleBlock) / tpw] =
+                    make_float2(dr.hi + dr.lo, dp.hi + dp.lo);
+        }
+    }
+}
+
+// Units: each listed row in kTailParts parts; the CTA that completes a row
+// makes its draw.
+template <typename T>
+__global__ void __launch_bounds__(kTailThreads) verify_tail_kernel(const VerifyArgs a) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    __shared__ int s_flag;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int n_rows = min(a.q_ctr[kQSmallList], a.B);
+    const int n_res = n_rows * kTailParts;
+    const int wpb = kSampleBlock / (a.chunk_elems / kCW);
+    const int per = (a.nc + kTailParts - 1) / kTailParts;  // tiles per part
+    const int parts = (a.nc + per - 1) / per;               // parts a row has
+    for (int u = blockIdx.x; u < n_res; u += gridDim.x) {
+        const int i = u / kTailParts, part = u - i * kTailParts;
+        if (part >= parts) continue;
+        const int2 jb = __ldcg(a.q_job + i);  // (b, r)
+        const DecideState st = load_state(a, i);
+        residual_part<T>(a, st, jb.x, jb.y, part * per, min(a.nc, (part + 1) * per), warp,
+                         lane);
+        __syncthreads();
+        if (tid == 0) {
+            __threadfence();  // every warp's masses (the barrier) before the count
+            s_flag = atomicAdd(&a.r1_cnt[jb.x], 1) == parts - 1;
+            if (s_flag) __threadfence();  // and every other CTA's, before they are read
+        }
+        __syncthreads();
+        if (s_flag && warp == 0) finish_residual_at<T>(a, jb.x, jb.y, st, wpb, lane);
+    }
+    // The last CTA out resets the list for the next launch.
+    __syncthreads();
+    if (tid == 0) {
+        __threadfence();
+        s_flag = atomicAdd(&a.q_ctr[kQTailExit], 1) == int(gridDim.x) - 1;
+    }
+    __syncthreads();
+    if (s_flag && tid == 0) {
+        a.q_ctr[kQSmallList] = 0;
+        a.q_ctr[kQTailExit] = 0;
+    }
+}
+
 }  // namespace
 
 size_t verify_smem_bytes() { return kSmemBytes; }
@@ -1478,6 +1594,32 @@ cudaError_t launch_verify(const VerifyArgs &a, int logit_bf16, int grid, cudaStr
     cfg.numAttrs = 1;
     if (logit_bf16) return cudaLaunchKernelEx(&cfg, verify_kernel<uint16_t>, a);
     return cudaLaunchKernelEx(&cfg, verify_kernel<float>, a);
+}
+
+int verify_tail_blocks_per_sm(int logit_bf16) {
+    int n = 0;
+    const cudaError_t e =
+        logit_bf16 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, verify_tail_kernel<uint16_t>,
+                                                                   kTailThreads, 0)
+                   : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, verify_tail_kernel<float>,
+                                                                   kTailThreads, 0);
+    return e == cudaSuccess ? n : -1;
+}
+
+cudaError_t launch_verify_tail(const VerifyArgs &a, int logit_bf16, int grid, cudaStream_t s) {
+    // A programmatic dependent of the small-batch verify: its CTAs take the
+    // slots that grid's CTAs leave, and wait for it to complete.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kTailThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (logit_bf16) return cudaLaunchKernelEx(&cfg, verify_tail_kernel<uint16_t>, a);
+    return cudaLaunchKernelEx(&cfg, verify_tail_kernel<float>, a);
 }
 
 }  // namespace dspark

@@ -20,7 +20,12 @@
 // decides it with all 256 threads: accept tests from the row records, then
 // the residual draw (it streams the rejected row pair once more, block masses
 // per warp, in two-float sums) or the bonus draw from the bonus row's block
-// records, each a block by u' and an id inside it by u''.
+// records, each a block by u' and an id inside it by u''.  With rows of four
+// tiles or more and four requests or more (small_tail), a rejection is listed
+// instead for the tail kernel
+// (verify.cu), which takes the row pair's second pass in parts over the
+// whole GPU and makes the residual draw: one CTA alone needs ~25 us for a
+// 300 KB row pair, a second launch a few us.
 //
 // Waits: none.  Every CTA runs to completion on its own units.
 #include <climits>
@@ -467,8 +472,34 @@ __device__ void finish_request_small(const VerifyArgs &a, SmallSmem &sm, int b, 
         step_uniforms(a.seed, b, acc, u, u_blk, u_tok);
         DrawRows w;
         w.scale = scale;
+        if (acc < Lb && a.small_tail) {
+            // The residual at row acc (from p if its mass is zero) is the tail
+            // kernel's: listed with the row and the draw state, the row's
+            // second pass is cut into parts over the whole GPU there (one CTA
+            // alone took ~25 us for a 300 KB row pair).  It writes the outputs.
+            if (tid == 0) {
+                const float4 nm = sm.norm[acc];
+                DecideState st;
+                st.a = acc;
+                st.mode = D_RESID;
+                st.Mp = nm.x;
+                st.Sp = nm.y;
+                st.Mq = nm.z;
+                st.Sq = nm.w;
+                st.u_blk = u_blk;
+                st.u_tok = u_tok;
+                const int pos = atomicAdd(&a.q_ctr[kQSmallList], 1);  // each request once: < B
+                if (pos < a.B) {
+                    a.q_job[pos] = make_int2(b, r0 + acc);
+                    a.dstate[pos] = st;
+                }
+                a.req_cnt[b] = 0;  // complete here: reset for the next launch
+            }
+            return;
+        }
         if (acc < Lb) {
-            // residual at row acc, from p if its mass is zero
+            // residual at row acc, from p if its mass is zero (rows of a few
+            // tiles: one CTA's pass costs less than a second launch)
             const float4 nm = sm.norm[acc];
             w.tv = reinterpret_cast<const uint4 *>(static_cast<const char *>(a.target_logits) +
                                                    size_t(r0 + acc) * a.row_bytes);
@@ -532,8 +563,11 @@ __device__ void finish_request_small(const VerifyArgs &a, SmallSmem &sm, int b, 
 
 template <typename T>
 __global__ void __launch_bounds__(kSmallThreads) verify_small_kernel(const VerifyArgs a, int S) {
-    // Launched as a programmatic dependent of the compaction: wait for it.
+    // Launched as a programmatic dependent of the kernel before it: wait for
+    // it.  The tail kernel after it may be scheduled as this grid's CTAs
+    // leave (it waits for this grid to complete).
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
     __shared__ SmallSmem sm;
     const int tid = threadIdx.x;
     const int n_rows = min(max(a.row_off[a.B], 0), a.B * (a.gamma + 1));

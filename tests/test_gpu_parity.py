@@ -87,6 +87,7 @@ SHAPES = [
     (12, 16, 70000, 64, "bf16"),   # the small-batch kernel: 9 slices of 8192 ids
     (16, 12, 40000, 32, "f32"),    # the small-batch kernel, fp32, its largest batch
     (17, 12, 40000, 32, "bf16"),   # one past it: the persistent kernel
+    (8, 16, 151936, 64, "bf16"),   # small batch, rows of 19 tiles: rejections go to the tail kernel
 ]
 
 
