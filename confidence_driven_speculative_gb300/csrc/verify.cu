@@ -618,8 +618,11 @@ __device__ void producer(const VerifyArgs &a, VSmem &sm, uint8_t *ring, const St
 // ---------------------------------------------------------------------------
 // Draft tokens d_{b, lane} and d_{b, lane + 32} of a request, loaded once per
 // decision (gamma <= 64).
+// (lane 0 also holds the request's cached length, loaded with the drafts so
+// that the commit at the end of the chain is a store, not a round trip)
 struct Drafts {
     int t[2];
+    int seq;
 };
 
 __device__ __forceinline__ Drafts load_drafts(const VerifyArgs &a, int b, int lane) {
@@ -629,6 +632,7 @@ __device__ __forceinline__ Drafts load_drafts(const VerifyArgs &a, int b, int la
         const int k = lane + 32 * i;
         d.t[i] = k < a.gamma ? __ldcg(a.draft_tokens + size_t(b) * a.gamma + k) : -1;
     }
+    d.seq = lane == 0 && a.seq_lens_commit ? __ldcg(a.seq_lens_commit + b) : 0;
     return d;
 }
 
@@ -647,7 +651,7 @@ __device__ void finish_request(const VerifyArgs &a, int b, int acc, int token, c
     if (lane == 0) {
         a.accept_len[b] = acc;
         a.num_emitted[b] = acc + 1;
-        if (a.seq_lens_commit) a.seq_lens_commit[b] += acc + 1;
+        if (a.seq_lens_commit) a.seq_lens_commit[b] = dr.seq + acc + 1;
         a.req_cnt[b] = 0;
         a.r1_cnt[b] = 0;
     }
