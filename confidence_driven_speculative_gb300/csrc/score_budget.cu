@@ -137,7 +137,9 @@ __device__ void score_producer(const ScoreArgs &a, ScoreSmem &sm, uint8_t *ring,
     int next = blockIdx.x;  // the first row needs no claim
     for (int fill = 0;;) {
         const int r = next;
-        if (r < rs.rows) next = int(gridDim.x) + atomicAdd(a.row_ctr, 1);
+        // (a grid with a CTA per row has nothing to claim: no round trip)
+        if (r < rs.rows)
+            next = rs.rows <= int(gridDim.x) ? rs.rows : int(gridDim.x) + atomicAdd(a.row_ctr, 1);
         for (int q = 0; q < (r < rs.rows ? rs.ntr : 1); ++q, ++fill) {
             const int s = fill % kScoreStages, n = fill / kScoreStages;
             if (n > 0 && !mbar_wait_bounded(&sm.empty[s], (n - 1) & 1, a.wait_ns)) {

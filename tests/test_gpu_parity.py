@@ -88,6 +88,7 @@ SHAPES = [
     (16, 12, 40000, 32, "f32"),    # the small-batch kernel, fp32, its largest batch
     (17, 12, 40000, 32, "bf16"),   # one past it: the persistent kernel
     (8, 16, 151936, 64, "bf16"),   # small batch, rows of 19 tiles: rejections go to the tail kernel
+    (6, 40, 40000, 16, "bf16"),    # the tail kernel with a long block (gamma = 40)
 ]
 
 
@@ -110,19 +111,22 @@ def test_draft_equals_target_accepts_everything(cuda_lib):
 
 
 @pytest.mark.parametrize("Tm", [0.0, 1.0])
-def test_first_drafts_rejected(cuda_lib, Tm):
+@pytest.mark.parametrize("B,V", [(64, 20000), (12, 70000)])
+def test_first_drafts_rejected(cuda_lib, Tm, B, V):
     """Drafts from an unrelated distribution: nearly every request rejects
     at its first draft, so most decisions take the residual path (sampling)
     or the argmax correction (greedy), and the bonus rows of those requests
-    are not needed -- the verify may skip them."""
-    inp = W.make_inputs(W.MIXED_B256, 7, B=64, V=20000, d=64, cap_T=-1, cost_c=0.0,
+    are not needed -- the verify may skip them.  At B = 12 with rows of nine
+    tiles the small-batch verify lists nearly every request for its tail
+    kernel."""
+    inp = W.make_inputs(W.MIXED_B256, 7, B=B, V=V, d=64, cap_T=-1, cost_c=0.0,
                         temperature=Tm)
     g = torch.Generator().manual_seed(77)
     dl = torch.randn(inp["draft_logits"].shape, generator=g) * 4.0
     inp["draft_logits"] = dl.to(inp["draft_logits"].dtype)
     if Tm == 0.0:
         # greedy drafts that are never the target's argmax
-        inp["draft_tokens"] = (inp["target_dense"][:, :-1].float().argmax(-1) + 1).to(torch.int32) % 20000
+        inp["draft_tokens"] = (inp["target_dense"][:, :-1].float().argmax(-1) + 1).to(torch.int32) % V
     else:
         gum = -torch.log(-torch.log(torch.rand(dl.shape, generator=g).clamp_min(1e-20)))
         inp["draft_tokens"] = (dl.float() + gum).argmax(-1).to(torch.int32)
