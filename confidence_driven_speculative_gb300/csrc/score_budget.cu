@@ -111,7 +111,6 @@ struct ScoreSmem {
     float part[kScoreStages][kWarps];  // warp partials of a row's last tile
     int done[kScoreStages];            // warps past a row's last tile
     int run_cap;                       // this CTA finished the batch
-    float tau[DSPARK_MAX_GAMMA];       // STS temperatures
 };
 
 struct RowShape {
@@ -203,9 +202,12 @@ __device__ int score_consumer(const ScoreArgs &a, ScoreSmem &sm, const uint8_t *
         const int r = sm.row[s], q = sm.tile[s];
         if (r < 0) return nrows;
         if (q == 0) acc = 0.f;
-        // The row's bias is needed at its end; load it now, behind the FMAs.
+        // The row's bias and temperature are needed at its end; load them
+        // now, behind the FMAs.
         const int rb = r / a.gamma;
-        const float bias = q + 1 == rs.ntr ? __ldg(&a.head_bias[rb]) : 0.f;
+        const bool last_tile = q + 1 == rs.ntr;
+        const float bias = last_tile ? __ldg(&a.head_bias[rb]) : 0.f;
+        const float tau = last_tile ? __ldg(&a.sts_tau[r - rb * a.gamma]) : 1.f;
         const int nvec = min(kScoreTile, rs.row_bytes - q * kScoreTile) / 16;
         const uint4 *tv = reinterpret_cast<const uint4 *>(ring + size_t(s) * kScoreTile);
         uint4 x[NV];
@@ -271,7 +273,7 @@ __device__ int score_consumer(const ScoreArgs &a, ScoreSmem &sm, const uint8_t *
             sm.done[s] = 0;
             mbar_arrive(&sm.empty[s]);
             // conf = sigmoid((w . h + bias_b) / tau_i) of this row
-            const float x = (dot + bias) / sm.tau[r - rb * a.gamma];
+            const float x = (dot + bias) / tau;
             a.conf[r] = 1.f / (1.f + expf(-x));
         }
         __syncwarp();
@@ -1164,7 +1166,6 @@ __device__ __forceinline__ void score_main(const ScoreArgs &a) {
         sm.run_cap = 0;
         fence_barrier_init();
     }
-    if (!kEntropy && tid < a.gamma) sm.tau[tid] = a.sts_tau[tid];
     if (a.pack) {
         // Only the finishing CTA reads the packing inputs, at the end: bring
         // them into L2 now, one 128-byte line per thread across the grid.

@@ -570,18 +570,28 @@ __global__ void __launch_bounds__(kSmallThreads) verify_small_kernel(const Verif
     asm volatile("griddepcontrol.launch_dependents;");
     __shared__ SmallSmem sm;
     const int tid = threadIdx.x;
-    const int n_rows = min(max(a.row_off[a.B], 0), a.B * (a.gamma + 1));
+    const int cap = a.B * (a.gamma + 1);
+    // The first unit's row ids go out with the packed total (the row-id
+    // arrays hold the batch's capacity): one round trip less before its data.
+    const int r_first = int(blockIdx.x) / S;
+    const int b_first = r_first < cap ? a.row_req[r_first] : 0;
+    const int k_first = r_first < cap ? a.row_k[r_first] : 0;
+    const int n_rows = min(max(a.row_off[a.B], 0), cap);
     const int units = n_rows * S;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
         const int r = u / S, j = u - r * S;
-        const int b = min(max(a.row_req[r], 0), a.B - 1);
-        const int k = max(a.row_k[r], 0);
-        const int Lb = min(max(a.L[b], 0), a.gamma);
+        const bool first = u == int(blockIdx.x);
+        const int b = min(max(first ? b_first : a.row_req[r], 0), a.B - 1);
+        const int k = max(first ? k_first : a.row_k[r], 0);
+        // Greedy units read the target row only: L_b's load (needed for the
+        // count) goes out beside theirs instead of before them.
+        const int L_raw = a.L[b];
+        const int Lb = a.greedy ? 0 : min(max(L_raw, 0), a.gamma);
         run_unit<T>(a, sm, r, j, b, k, Lb);
         __syncthreads();
         if (tid == 0) {
             __threadfence();
-            sm.last = atomicAdd(&a.req_cnt[b], 1) == (Lb + 1) * S - 1;
+            sm.last = atomicAdd(&a.req_cnt[b], 1) == (min(max(L_raw, 0), a.gamma) + 1) * S - 1;
         }
         __syncthreads();
         if (sm.last) {
