@@ -465,10 +465,21 @@ __device__ bool reclaim(const VerifyArgs &a, VSmem &sm, Books &bk, int &booked, 
 }
 
 __device__ void producer(const VerifyArgs &a, VSmem &sm, uint8_t *ring, const StreamShape &sh,
-                         int epoch) {
+                         int epoch, int pre_b, int pre_k) {
     ChunkFetch nextc;
     nextc.stage = 1;       // the first chunk is the CTA's own index; the counter
     nextc.c = blockIdx.x;  // hands out the rest from gridDim.x on
+    if (int(blockIdx.x) < sh.nA && pre_b >= 0) {
+        // Whole rows lead the stream, so that chunk is row blockIdx.x, whose
+        // ids were loaded with the packed total.
+        nextc.q = 0;
+        nextc.r = blockIdx.x;
+        nextc.g = 0;
+        nextc.b = pre_b;
+        nextc.k = pre_k;
+        nextc.rej = 0;
+        nextc.stage = 2;
+    }
     int cr = 0, cg = 0, cb = 0, ck = 0, cLb = 0, cd = -1, cj = 0, cj_end = 0;
     bool in_chunk = false;
     Books bk{-1, 0, 0, 0, 0, -1, 0, 0, 0, 0};
@@ -1401,6 +1412,13 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(const VerifyA
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int epoch = a.q_ctr[Q_EPOCH] + 1;
+    // The producer's first row ids go out with the packed total (the row-id
+    // arrays hold the batch's capacity): one round trip less before the
+    // CTA's first copy.
+    const bool prod = warp == kCW && lane == 0;
+    const int pre_b = prod && int(blockIdx.x) < a.B * (a.gamma + 1) ? a.row_req[blockIdx.x] : -1;
+    const int pre_k = prod && int(blockIdx.x) < a.B * (a.gamma + 1) ? a.row_k[blockIdx.x] : 0;
+    const StreamShape sh = stream_shape(a);
     if (tid < kStages) {
         mbar_init(&sm.full[tid], 1);
         mbar_init(&sm.empty[tid], kCW);
@@ -1408,9 +1426,8 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(const VerifyA
     }
     if (tid == 0) fence_barrier_init();
     __syncthreads();
-    const StreamShape sh = stream_shape(a);
     if (warp == kCW) {
-        if (lane == 0) producer(a, sm, ring, sh, epoch);
+        if (lane == 0) producer(a, sm, ring, sh, epoch, pre_b, pre_k);
     } else if (warp == kCW + 1) {
         decider<T>(a, sh, epoch, lane);
     } else {
