@@ -160,8 +160,8 @@ def test_repeated_calls_reuse_the_workspace(cuda_lib):
 
 @pytest.mark.parametrize("Tm", [0.0, 1.0])
 def test_graph_replay_matches_direct_calls(cuda_lib, Tm):
-    """The three calls captured as one CUDA graph (the cooperative verify and
-    the dependent compaction included) and replayed twice give the outputs of
+    """The three calls captured as one CUDA graph (the compaction and the
+    verify are programmatic dependents of the kernel before each) and replayed twice give the outputs of
     direct calls, bit for bit, on the same buffers, and each replay equals
     the oracle."""
     from confidence_driven_speculative_gb300 import binding
