@@ -1598,11 +1598,12 @@ int verify_blocks_per_sm(int logit_bf16) {
 }
 
 cudaError_t launch_verify(const VerifyArgs &a, int logit_bf16, int grid, cudaStream_t s) {
-    // A programmatic dependent of the kernel before it (the compaction): the
-    // grid is scheduled while that kernel runs and waits for it at its start
-    // (griddepcontrol.wait).  Not cooperative: every unit of work -- stream
-    // chunks, residual tiles, decider jobs -- is claimed by a running CTA, so
-    // no CTA waits on one that has not started.
+    // A programmatic dependent of the kernel before it (the score kernel or
+    // the compaction): the grid is scheduled while that kernel finishes and
+    // waits for it at its start (griddepcontrol.wait).  Not cooperative: one
+    // CTA per resident slot, so every CTA runs at once; the stream chunks
+    // after each CTA's first, the residual tiles and the decider jobs are
+    // claimed by running CTAs, and every wait is bounded.
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kVerifyThreads);
