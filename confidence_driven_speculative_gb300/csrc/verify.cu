@@ -28,8 +28,10 @@
 //    requests already known to reject: the method never reads past the
 //    first rejection.
 //  * A consumer warp owns one eighth of every tile.  For a pair row its
-//    lanes keep online (max, sum of 2^(z log2(e)/Tm - max)) accumulators for
-//    p and q across the tiles of the chunk and reduce once, at the chunk's
+//    lanes keep (m, sum of 2^(z log2(e)/Tm - m)) accumulators for p and q
+//    across the tiles of the chunk -- m a reference set by the lane's first
+//    vector, raised only when a tile's terms would pass 2^64, so most
+//    vectors cost no maximum -- and reduce once, at the chunk's
 //    end, into a record slot of the row (plain stores: deterministic).  A
 //    bonus row stores one slot per tile and warp, which gives the per-block
 //    masses of the draw.  Greedy rows keep (max, lowest argmax).
@@ -208,6 +210,66 @@ __device__ __forceinline__ void online_update(float &m, float &s, const float (&
 #pragma unroll
         for (int e = 0; e + w < VE; e += 2 * w) t[e] += t[e + w];
     s += t[0];
+}
+
+// One tile's share of a lane -- vectors v0 + lane + 32 i < v1 -- of NR rows
+// folded into the lane's (m, s) pairs.  The pair (m, s) stands for
+// sum 2^(z s - m) with m any reference, not necessarily the maximum: the
+// lane's first vector of the chunk sets it, and later terms are summed
+// against it without a running maximum.  A share whose sum exceeds 2^64 (a
+// term far above the reference; inf or NaN included) is folded again with a
+// running maximum, so every term stays below 2^64 relative to the reference
+// and the sum is at least 1 (the reference's own term), as accurate as with
+// the maximum.
+template <typename T, int NR>
+__device__ __forceinline__ void tile_fold(float (&m)[NR], float (&s)[NR],
+                                          const uint4 *const (&xv)[NR], int v0, int v1,
+                                          int lane, float scale) {
+    constexpr int VE = Vec<T>::kElems;
+    constexpr float kRefCap = 18446744073709551616.f;  // 2^64
+    const int vb = v0 + lane;
+    if (vb >= v1) return;
+    float c[NR], ts[NR];
+#pragma unroll
+    for (int h = 0; h < NR; ++h) {
+        if (m[h] == -INFINITY) {
+            float x[VE];
+            Vec<T>::unpack(xv[h][vb], x);
+            float vm = x[0];
+#pragma unroll
+            for (int e = 1; e < VE; ++e) vm = fmaxf(vm, x[e]);
+            m[h] = vm;
+        }
+        c[h] = -(m[h] * scale);
+        ts[h] = 0.f;
+    }
+    for (int v = vb; v < v1; v += 32) {
+#pragma unroll
+        for (int h = 0; h < NR; ++h) {
+            float x[VE], t[VE];
+            Vec<T>::unpack(xv[h][v], x);
+#pragma unroll
+            for (int e = 0; e < VE; ++e) t[e] = exp2_approx(fmaf(x[e], scale, c[h]));
+#pragma unroll
+            for (int w = 1; w < VE; w <<= 1)
+#pragma unroll
+                for (int e = 0; e + w < VE; e += 2 * w) t[e] += t[e + w];
+            ts[h] += t[0];
+        }
+    }
+#pragma unroll
+    for (int h = 0; h < NR; ++h) {
+        if (ts[h] <= kRefCap) {
+            s[h] += ts[h];
+            continue;
+        }
+#pragma unroll 1
+        for (int v = vb; v < v1; v += 32) {
+            float x[VE];
+            Vec<T>::unpack(xv[h][v], x);
+            online_update<VE>(m[h], s[h], x, scale);
+        }
+    }
 }
 
 // Two-float numbers: the unevaluated sum hi + lo, |lo| <= ulp(hi) / 2.
@@ -1228,7 +1290,7 @@ __device__ void consumer(const VerifyArgs &a, VSmem &sm, const uint8_t *ring,
     const int vpw = tpw / VE;             // vectors per warp in a tile
     // Row accumulators of pair rows (sampling) / of every row (greedy),
     // carried across the tiles of a chunk.
-    float mp = -INFINITY, sp = 0.f, mq = -INFINITY, sq = 0.f;
+    float mr[2] = {-INFINITY, -INFINITY}, sr[2] = {0.f, 0.f};  // (p, q) of a pair row
     float bv = -INFINITY;
     int bi = INT_MAX;
     for (int fill = 0;; ++fill) {
@@ -1263,13 +1325,8 @@ __device__ void consumer(const VerifyArgs &a, VSmem &sm, const uint8_t *ring,
                     }
                 }
             } else if (t.pair) {
-                for (int v = v0 + lane; v < v1; v += 32) {
-                    float z[VE];
-                    Vec<T>::unpack(tv[v], z);
-                    online_update<VE>(mp, sp, z, scale);
-                    Vec<T>::unpack(dv[v], z);
-                    online_update<VE>(mq, sq, z, scale);
-                }
+                const uint4 *const rows[2] = {tv, dv};
+                tile_fold<T, 2>(mr, sr, rows, v0, v1, lane, scale);
                 if (lane == 0) {
                     const int lo = t.y0 + v0 * VE, hi = t.y0 + v1 * VE;
                     if (t.d >= lo && t.d < hi)
@@ -1282,18 +1339,15 @@ __device__ void consumer(const VerifyArgs &a, VSmem &sm, const uint8_t *ring,
                     const uint4 *xv = h ? dv : tv;
                     const int nv = (h ? t.bytes2 : t.bytes) / 16;
                     const int va = min(nv, warp * vpw), vb = min(nv, va + vpw);
-                    float bm = -INFINITY, bs = 0.f;
-                    for (int v = va + lane; v < vb; v += 32) {
-                        float z[VE];
-                        Vec<T>::unpack(xv[v], z);
-                        online_update<VE>(bm, bs, z, scale);
-                    }
-                    warp_ms_reduce(bm, bs, scale);
+                    float bm[1] = {-INFINITY}, bs[1] = {0.f};
+                    const uint4 *const rows[1] = {xv};
+                    tile_fold<T, 1>(bm, bs, rows, va, vb, lane, scale);
+                    warp_ms_reduce(bm[0], bs[0], scale);
                     const int y = t.y0 + h * a.chunk_elems + warp * tpw;
                     const int blk = y / kSampleBlock;
                     if (lane == 0 && blk < a.nblk)
                         a.blkrec[(size_t(t.b) * a.nblk + blk) * kCW + (y % kSampleBlock) / tpw] =
-                            make_float2(bm, bs);
+                            make_float2(bm[0], bs[0]);
                 }
             }
             if (t.flush && (a.greedy || t.pair)) {
@@ -1302,12 +1356,12 @@ __device__ void consumer(const VerifyArgs &a, VSmem &sm, const uint8_t *ring,
                     warp_am_reduce(bv, bi);
                     if (lane == 0) sm.part[s][warp] = make_float4(bv, __int_as_float(bi), 0.f, 0.f);
                 } else {
-                    warp_ms_reduce(mp, sp, scale);
-                    warp_ms_reduce(mq, sq, scale);
-                    if (lane == 0) sm.part[s][warp] = make_float4(mp, sp, mq, sq);
+                    warp_ms_reduce(mr[0], sr[0], scale);
+                    warp_ms_reduce(mr[1], sr[1], scale);
+                    if (lane == 0) sm.part[s][warp] = make_float4(mr[0], sr[0], mr[1], sr[1]);
                 }
-                mp = mq = bv = -INFINITY;
-                sp = sq = 0.f;
+                mr[0] = mr[1] = bv = -INFINITY;
+                sr[0] = sr[1] = 0.f;
                 bi = INT_MAX;
                 int last = 0;
                 if (lane == 0) {
