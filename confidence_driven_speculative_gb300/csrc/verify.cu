@@ -42,8 +42,11 @@
 //    (a join counter), makes the bonus-draw job.  Decider warps serve these
 //    jobs from a device-wide queue.  A rejection queues residual-mass jobs
 //    (one tile of the rejecting row pair, read again while it is still in
-//    L2), which producers serve through their rings before their own chunks;
-//    the last of them queues the residual draw.
+//    L2), served through the producers' rings: an idle decider warp claims
+//    one and leaves its task in its CTA's shared-memory mailbox, which the
+//    producer takes before its own chunks (so the producer's loop reads no
+//    global word while it streams); a producer whose stream is done claims
+//    from the queue itself.  The last of them queues the residual draw.
 //  * Draws are two-level: a 4096-id block by mass (u'), then an id inside it
 //    (u''); in-block running sums are fp32 over short lane runs combined in
 //    two-float (TwoSum) arithmetic, as exact as fp64 on the fast fp32 pipe.
@@ -86,6 +89,7 @@ struct TaskInfo {
     int bytes2; // target-only rows: the row's next tile in the second half (0: none)
     int d;      // stream pair: drafted id (its gather target)
     int flush;  // stream: last tile of the chunk
+    float Mp, Sp, Mq, Sq;  // residual: normalisers of the row pair (the decide's)
 };
 
 struct VSmem {
@@ -93,6 +97,11 @@ struct VSmem {
     TaskInfo task[kStages];
     float4 part[kStages][kCW];  // per-warp row partials of a chunk's last tile
     int done[kStages];          // warps finished with a chunk's last tile
+    // A residual tile handed from the decider warp to the producer, so that
+    // the producer reads no global word to find residual work while it
+    // streams: mbox_full is 1 from the decider's write to the producer's take.
+    TaskInfo mbox;
+    int mbox_full;
 };
 
 // Grid-wide shape of the stream work, the same in every thread.  Two
@@ -138,6 +147,15 @@ __device__ __forceinline__ void st_relaxed(int *p, int v) {
 // fence, which nothing here needs.
 __device__ __forceinline__ void fence_acq_rel_gpu() {
     asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+// q_ctr words 0-3 (residual head / tail, finished, exited) in one load.
+__device__ __forceinline__ int4 ld_acquire_ctr4(const int *p) {
+    int4 v;
+    asm volatile("ld.acquire.gpu.global.v4.s32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p)
+                 : "memory");
+    return v;
 }
 
 // Cross-CTA state is read through L2 only (never a possibly stale L1 line).
@@ -382,11 +400,36 @@ __device__ TaskInfo resid_task(const VerifyArgs &a, int2 jb) {
     const DecideState st = load_state(a, t.b);
     t.k = st.a;
     t.r = a.row_off[t.b] + st.a;
+    t.Mp = st.Mp;
+    t.Sp = st.Sp;
+    t.Mq = st.Mq;
+    t.Sq = st.Sq;
     t.pair = 1;
     t.y0 = t.j * a.chunk_elems;
     t.bytes = min(kChunkBytes, a.row_bytes - t.j * kChunkBytes);
     t.bytes2 = 0;
     return t;
+}
+
+// The CTA's residual-tile mailbox: one task, written by the decider warp's
+// lane 0, taken by the producer.  The flag is read and written volatile;
+// the block fences order the task's words against it on both sides.
+__device__ __forceinline__ bool mbox_empty(VSmem &sm) {
+    return *reinterpret_cast<volatile int *>(&sm.mbox_full) == 0;
+}
+__device__ __forceinline__ void mbox_put(VSmem &sm, const TaskInfo &t) {
+    __threadfence_block();  // the slot was seen empty before it is written
+    sm.mbox = t;
+    __threadfence_block();  // the task before the flag
+    *reinterpret_cast<volatile int *>(&sm.mbox_full) = 1;
+}
+__device__ __forceinline__ bool mbox_take(VSmem &sm, TaskInfo &t) {
+    if (mbox_empty(sm)) return false;
+    __threadfence_block();  // the flag before the task
+    t = sm.mbox;
+    __threadfence_block();  // the task read before the slot is freed
+    *reinterpret_cast<volatile int *>(&sm.mbox_full) = 0;
+    return true;
 }
 
 // ---------------------------------------------------------------------------
@@ -546,28 +589,17 @@ __device__ void producer(const VerifyArgs &a, VSmem &sm, uint8_t *ring, const St
     bool in_chunk = false;
     Books bk{-1, 0, 0, 0, 0, -1, 0, 0, 0, 0};
     int booked = 0;
-    // Residual-tile queue, polled on every fourth fill: the values read at
-    // the end of a polling fill are used at the start of the next one, so a
-    // global load does not stall the issue of a copy while the stream runs
-    // (with free stages a fill is shorter than an L2 round trip).
-    int pending = -1;      // a claimed queue index
-    int pend_rdy = 0;      // its ready word, read four fills earlier
-    int2 pend_job = make_int2(0, 0);
-    int obs_head = 0, obs_tail = 0;
+    // Residual tiles reach the producer through the CTA's mailbox, which the
+    // decider warp fills (a global load in this loop would stall the issue
+    // of a copy: with free stages a fill is shorter than an L2 round trip).
+    // Once its stream is done the producer also claims from the queue itself.
+    int pending = -1;  // a residual-queue index claimed by the producer
     for (int fill = 0;; ++fill) {
         TaskInfo t;
         t.type = T_EXIT;
         bool have = false, ok = true;
-        const bool poll = (fill & 3) == 0;
         // 1. residual tiles first
-        if (poll && pending >= 0 && pend_rdy == epoch) {
-            t = resid_task(a, pend_job);
-            pending = -1;
-            have = true;
-        } else if (poll && pending < 0 && obs_head < obs_tail) {
-            pending = atomicAdd(&a.q_ctr[QA_HEAD], 1);
-            pend_rdy = 0;
-        }
+        if (mbox_take(sm, t)) have = true;
         // 2. then the stream chunks
         if (!have && !in_chunk) {
             while (nextc.stage < 4) fetch_step(a, sh, nextc, epoch);
@@ -621,6 +653,10 @@ __device__ void producer(const VerifyArgs &a, VSmem &sm, uint8_t *ring, const St
             const uint64_t t0 = global_timer_ns();
             unsigned ns = 32;
             while (ok) {
+                if (mbox_take(sm, t)) {
+                    have = true;
+                    break;
+                }
                 if (pending < a.qcap && ld_acquire(&a.q_ready[pending]) == epoch) {
                     t = resid_task(a, __ldcg(a.q_job + pending));
                     pending = -1;
@@ -673,15 +709,6 @@ __device__ void producer(const VerifyArgs &a, VSmem &sm, uint8_t *ring, const St
         while (booked < fill && mbar_test_wait(&sm.empty[booked % kStages], (booked / kStages) & 1)) {
             account(a, bk, sm.task[booked % kStages], epoch);
             ++booked;
-        }
-        // 6. look at the residual queue for the next polling fill
-        if (poll) {
-            obs_head = ld_relaxed(&a.q_ctr[QA_HEAD]);
-            obs_tail = ld_relaxed(&a.q_ctr[QA_TAIL]);
-            if (pending >= 0 && pending < a.qcap) {
-                pend_rdy = ld_acquire(&a.q_ready[pending]);
-                pend_job = __ldcg(a.q_job + pending);
-            }
         }
     }
 }
@@ -1391,8 +1418,7 @@ __device__ void consumer(const VerifyArgs &a, VSmem &sm, const uint8_t *ring,
             if (lane == 0) mbar_arrive(&sm.empty[s]);
         } else {
             // Residual tile: this warp's share of the residual and p masses.
-            const DecideState st = load_state(a, t.b);
-            const float iSp = 1.f / st.Sp, iSq = 1.f / st.Sq;
+            const float iSp = 1.f / t.Sp, iSq = 1.f / t.Sq;
             float zr = 0.f, zp = 0.f;
             for (int v = v0 + lane; v < v1; v += 32) {
                 float x[VE], y[VE];
@@ -1400,9 +1426,9 @@ __device__ void consumer(const VerifyArgs &a, VSmem &sm, const uint8_t *ring,
                 Vec<T>::unpack(dv[v], y);
 #pragma unroll
                 for (int e = 0; e < VE; ++e) {
-                    const float pw = exp2_approx((x[e] - st.Mp) * scale);
+                    const float pw = exp2_approx((x[e] - t.Mp) * scale);
                     zp += pw;
-                    zr += fmaxf(0.f, pw * iSp - exp2_approx((y[e] - st.Mq) * scale) * iSq);
+                    zr += fmaxf(0.f, pw * iSp - exp2_approx((y[e] - t.Mq) * scale) * iSq);
                 }
             }
             const F2 dr = warp_sum_f2(f2(zr)), dp = warp_sum_f2(f2(zp));
@@ -1421,12 +1447,16 @@ __device__ void consumer(const VerifyArgs &a, VSmem &sm, const uint8_t *ring,
 }
 
 // ---------------------------------------------------------------------------
-// decider: warp kCW + 1 serves the decide queue
+// decider: warp kCW + 1 serves the decide queue, and between jobs feeds its
+// producer's residual-tile mailbox
 // ---------------------------------------------------------------------------
 template <typename T>
-__device__ void decider(const VerifyArgs &a, const StreamShape &sh, int epoch, int lane) {
+__device__ void decider(const VerifyArgs &a, VSmem &sm, const StreamShape &sh, int epoch,
+                        int lane) {
+    static_assert(QA_HEAD == 0 && QA_TAIL == 1 && Q_FINISHED == 2, "one vector load");
     const int wpb = kSampleBlock / (a.chunk_elems / kCW);
-    int pending = -1;
+    int pending = -1;  // decide-queue index
+    int rclaim = -1;   // residual-queue index claimed for this CTA's producer
     for (;;) {
         int b = -1;
         if (lane == 0) {
@@ -1434,12 +1464,32 @@ __device__ void decider(const VerifyArgs &a, const StreamShape &sh, int epoch, i
             const uint64_t t0 = global_timer_ns();
             unsigned ns = 32;
             for (;;) {
-                if (pending < a.qbcap && ld_acquire(&a.qb_ready[pending]) == epoch) {
-                    b = __ldcg(a.qb_job + pending);
-                    pending = -1;
-                    break;
+                if (rclaim >= 0) {
+                    // A claimed residual tile goes out before anything else:
+                    // its job was queued when it was claimed, so its ready
+                    // word follows within the pusher's few stores.
+                    if (ld_acquire(&a.q_ready[rclaim]) == epoch) {
+                        mbox_put(sm, resid_task(a, __ldcg(a.q_job + rclaim)));
+                        rclaim = -1;
+                        ns = 32;
+                        continue;
+                    }
+                } else {
+                    if (pending < a.qbcap && ld_acquire(&a.qb_ready[pending]) == epoch) {
+                        b = __ldcg(a.qb_job + pending);
+                        pending = -1;
+                        break;
+                    }
+                    const int4 q = ld_acquire_ctr4(a.q_ctr);
+                    if (q.z >= a.B) break;
+                    // The mailbox is empty and a residual tile is queued:
+                    // claim its index, never one past the tail, so that a
+                    // claim is always served at once.
+                    if (q.x < q.y && q.x < a.qcap && mbox_empty(sm) &&
+                        atomicCAS(&a.q_ctr[QA_HEAD], q.x, q.x + 1) == q.x)
+                        rclaim = q.x;
+                    if (rclaim >= 0) continue;
                 }
-                if (ld_acquire(&a.q_ctr[Q_FINISHED]) >= a.B) break;
                 if (global_timer_ns() - t0 > a.wait_ns) {
                     atomicOr(a.status, kStatusQueueTimeout);
                     break;
@@ -1478,12 +1528,13 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(const VerifyA
         mbar_init(&sm.empty[tid], kCW);
         sm.done[tid] = 0;
     }
+    if (tid == 0) sm.mbox_full = 0;
     if (tid == 0) fence_barrier_init();
     __syncthreads();
     if (warp == kCW) {
         if (lane == 0) producer(a, sm, ring, sh, epoch, pre_b, pre_k);
     } else if (warp == kCW + 1) {
-        decider<T>(a, sh, epoch, lane);
+        decider<T>(a, sm, sh, epoch, lane);
     } else {
         consumer<T>(a, sm, ring, sh, warp, lane, epoch);
     }
