@@ -331,9 +331,12 @@ __device__ __forceinline__ F2 f2_shfl(F2 v, int src) {
     return F2{__shfl_sync(0xffffffffu, v.hi, src), __shfl_sync(0xffffffffu, v.lo, src)};
 }
 
-// Inclusive warp scan (lane order).
+// Inclusive warp scan (lane order).  The two-float scans and sums run only
+// in the draws and residual tiles; kept as loops, their code stays small,
+// which measurably shortens the draw chains (that code is cold beside the
+// consumers' hot loop and is fetched as it runs).
 __device__ __forceinline__ F2 warp_scan_incl(F2 v, int lane) {
-#pragma unroll
+#pragma unroll 1
     for (int o = 1; o < 32; o <<= 1) {
         const F2 n = f2_shfl_up(v, o);
         if (lane >= o) v = v + n;
@@ -342,7 +345,7 @@ __device__ __forceinline__ F2 warp_scan_incl(F2 v, int lane) {
 }
 
 __device__ __forceinline__ F2 warp_sum_f2(F2 v) {
-#pragma unroll
+#pragma unroll 1
     for (int o = 16; o > 0; o >>= 1)
         v = v + F2{__shfl_xor_sync(0xffffffffu, v.hi, o), __shfl_xor_sync(0xffffffffu, v.lo, o)};
     return v;
