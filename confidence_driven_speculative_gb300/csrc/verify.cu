@@ -992,13 +992,44 @@ __device__ __forceinline__ float2 bonus_block(const VerifyArgs &a, int b, int i,
     return make_float2(m, s);
 }
 
+// A sampling draw's inputs, from the bonus row's slots or the residual
+// masses: the slot masses of blocks lane and lane + 32 in every lane
+// (blocks from 64 on are read again by slot_mass_at), the drawn row's
+// state, the kind of slot record, and what the commit needs.  Both draws
+// then share one tail (draw_tail), inlined once in the decider: its code is
+// cold beside the consumers' loop, and less of it makes the chain shorter.
+struct DrawPrep {
+    DecideState st;
+    float m[2][kCW];  // slot masses of blocks lane, lane + 32 (0 past the row)
+    float M;          // bonus: the reference of the slot masses
+    int kind;         // 0: bonus-row slots, 1: residual masses, 2: p masses
+    int r;            // packed target row drawn from
+    int acc;          // committed drafts
+    Drafts dr;
+};
+
+// Mass of slot w of block i of request b, read from the workspace (kind as
+// in DrawPrep).
+__device__ __forceinline__ float slot_mass_at(const VerifyArgs &a, int kind, int b, int i, int w,
+                                              float M) {
+    const size_t o = (size_t(b) * a.nblk + i) * kCW + w;
+    if (kind == 0) {
+        const float2 x = __ldcg(a.blkrec + o);
+        return x.y > 0.f ? x.y * exp2_approx((x.x - M) * a.scale) : 0.f;
+    }
+    const float2 x = __ldcg(a.zrec + o);
+    return kind == 1 ? x.x : x.y;
+}
+
 // The bonus draw of request b, every draft accepted: from p of row L_b
 // (sampling; block and slot masses from the row's per-warp slots), or the
-// argmax of row L_b (greedy; from its chunk records).
+// argmax of row L_b (greedy; from its chunk records).  Sampling prepares
+// the draw and returns true; greedy commits and returns false.
 template <typename T>
-__device__ void bonus_draw(const VerifyArgs &a, const StreamShape &sh, int b, int wpb, int lane) {
+__device__ bool prep_bonus(const VerifyArgs &a, const StreamShape &sh, int b, DrawPrep &p,
+                           int wpb, int lane) {
     const int Lb = verify_len(a, b), r = a.row_off[b] + Lb;
-    const Drafts dr = load_drafts(a, b, lane);
+    p.dr = load_drafts(a, b, lane);
     if (a.greedy) {
         float v = -INFINITY;
         int id = INT_MAX;
@@ -1008,82 +1039,51 @@ __device__ void bonus_draw(const VerifyArgs &a, const StreamShape &sh, int b, in
             am_combine(v, id, x.x, __float_as_int(x.y));
         }
         warp_am_reduce(v, id);
-        finish_request(a, b, Lb, id, dr, lane);
-        return;
+        finish_request(a, b, Lb, id, p.dr, lane);
+        return false;
     }
     const float scale = a.scale;
-    constexpr int kCache = 2;  // blocks per lane kept in registers (nblk <= 64)
-    float2 sl[kCache][kCW];
+    float2 sl[2][kCW];
 #pragma unroll
-    for (int q = 0; q < kCache; ++q) {
+    for (int q = 0; q < 2; ++q) {
         const int i = q * 32 + lane;
-        const float2 *p = a.blkrec + (size_t(b) * a.nblk + (i < a.nblk ? i : 0)) * kCW;
+        const float2 *x = a.blkrec + (size_t(b) * a.nblk + (i < a.nblk ? i : 0)) * kCW;
 #pragma unroll
         for (int w = 0; w < kCW; ++w)
-            sl[q][w] = i < a.nblk && w < wpb ? __ldcg(p + w) : make_float2(-INFINITY, 0.f);
+            sl[q][w] = i < a.nblk && w < wpb ? __ldcg(x + w) : make_float2(-INFINITY, 0.f);
     }
     float u, ub, ut;
     step_uniforms(a.seed, b, Lb, u, ub, ut);
     float mb = -INFINITY;
 #pragma unroll
-    for (int q = 0; q < kCache; ++q)
+    for (int q = 0; q < 2; ++q)
 #pragma unroll
         for (int w = 0; w < kCW; ++w)
             if (sl[q][w].y > 0.f) mb = fmaxf(mb, sl[q][w].x);
-    for (int i = kCache * 32 + lane; i < a.nblk; i += 32) {
+    for (int i = 64 + lane; i < a.nblk; i += 32) {
         const float2 x = bonus_block(a, b, i, wpb, scale);
         if (x.y > 0.f) mb = fmaxf(mb, x.x);
     }
     const float M = warp_max(mb);
     // slot mass in the units of 2^((z - M) s)
-    auto smass = [&](float2 x) { return x.y > 0.f ? x.y * exp2_approx((x.x - M) * scale) : 0.f; };
-    auto mass = [&](int i) {
-        const int q = i >> 5;
-        F2 m = f2(0.f);
-        if (q < kCache) {
 #pragma unroll
-            for (int c = 0; c < kCache; ++c)
-                if (q == c) {
-                    float v[kCW];
+    for (int q = 0; q < 2; ++q)
 #pragma unroll
-                    for (int w = 0; w < kCW; ++w) v[w] = smass(sl[c][w]);
-                    m = sum8_f2(v);
-                }
-        } else {
-            const float2 *p = a.blkrec + (size_t(b) * a.nblk + i) * kCW;
-            for (int w = 0; w < wpb; ++w) m = m + f2(smass(__ldcg(p + w)));
-        }
-        return m;
-    };
-    const int blk = choose_block(a.nblk, ub, mass, lane);
-    float slot_mass[kCW];
-    {
-        const int q = blk >> 5, owner = blk & 31;
-#pragma unroll
-        for (int w = 0; w < kCW; ++w) {
-            float m = 0.f;
-            if (q < kCache) {
-#pragma unroll
-                for (int c = 0; c < kCache; ++c)
-                    if (q == c) m = smass(sl[c][w]);
-                m = __shfl_sync(0xffffffffu, m, owner);
-            } else if (w < wpb) {
-                m = smass(__ldcg(a.blkrec + (size_t(b) * a.nblk + blk) * kCW + w));
-            }
-            slot_mass[w] = w < wpb ? m : 0.f;
-        }
-    }
-    DecideState st;
-    st.a = Lb;
-    st.mode = D_BONUS;
-    st.Mp = M;
-    st.Sp = 1.f;
-    st.Mq = 0.f;
-    st.Sq = 1.f;
-    st.u_blk = ub;
-    st.u_tok = ut;
-    const int token = block_pick<T>(a, st, b, r, blk, slot_mass, wpb, kSampleBlock / wpb, lane);
-    finish_request(a, b, Lb, token, dr, lane);
+        for (int w = 0; w < kCW; ++w)
+            p.m[q][w] = sl[q][w].y > 0.f ? sl[q][w].y * exp2_approx((sl[q][w].x - M) * scale) : 0.f;
+    p.M = M;
+    p.kind = 0;
+    p.r = r;
+    p.acc = Lb;
+    p.st.a = Lb;
+    p.st.mode = D_BONUS;
+    p.st.Mp = M;
+    p.st.Sp = 1.f;
+    p.st.Mq = 0.f;
+    p.st.Sq = 1.f;
+    p.st.u_blk = ub;
+    p.st.u_tok = ut;
+    return true;
 }
 
 // Request b's decision rows (k < L_b) are all in: accept tests and outputs
@@ -1095,7 +1095,7 @@ __device__ void bonus_draw(const VerifyArgs &a, const StreamShape &sh, int b, in
 // the streaming keeps L2 busy, and each dependent round trip costs
 // microseconds.
 template <typename T>
-__device__ void decide_request(const VerifyArgs &a, const StreamShape &sh, int b, int wpb,
+__device__ bool decide_request(const VerifyArgs &a, const StreamShape &sh, int b, int wpb,
                                int epoch, int lane) {
     // Round 1: lengths, offsets and draft tokens.
     const int Lb = verify_len(a, b), r0 = a.row_off[b], d0 = a.draft_off[b];
@@ -1200,7 +1200,7 @@ __device__ void decide_request(const VerifyArgs &a, const StreamShape &sh, int b
         if (lane == 0) st_relaxed(&a.rejflag[b], epoch);  // phase Q skips the bonus row
         if (a.greedy) {
             finish_request(a, b, acc, g_tok, dr, lane);
-            return;
+            return false;
         }
         DecideState st;
         st.a = acc;
@@ -1215,97 +1215,88 @@ __device__ void decide_request(const VerifyArgs &a, const StreamShape &sh, int b
             a.dstate[b] = st;
             push_resid_jobs(a, b, epoch);
         }
-        return;
+        return false;
     }
-    // Every draft accepted: the bonus draw, if the bonus row is in already.
+    // Every draft accepted: the bonus draw (true), if the bonus row is in
+    // already.
     int go = 0;
     if (lane == 0) {
         fence_acq_rel_gpu();
         go = atomicAdd(&a.join[b], 1) == 1;
     }
-    if (__shfl_sync(0xffffffffu, go, 0)) {
-        fence_acq_rel_gpu();
-        bonus_draw<T>(a, sh, b, wpb, lane);
-    }
+    const bool run = __shfl_sync(0xffffffffu, go, 0) != 0;
+    if (run) fence_acq_rel_gpu();
+    return run;
 }
 
-// Every residual slot of request b is in: choose the block from the masses,
-// then the slot, then the token.
+// Every residual slot of request b is in: the residual draw at packed row
+// r from the masses, or a draw from p of the same row when there is no
+// residual mass (or the window ends inside the accepted run).
 template <typename T>
-__device__ void finish_residual_at(const VerifyArgs &a, int b, int r, DecideState st, int wpb,
-                                   int lane) {
+__device__ void prep_residual(const VerifyArgs &a, int b, int r, DecideState st, DrawPrep &p,
+                              int wpb, int lane) {
     // One round of independent loads: drafts, masses.
-    const Drafts dr = load_drafts(a, b, lane);
+    p.dr = load_drafts(a, b, lane);
     const float2 *z = a.zrec + size_t(b) * a.nblk * kCW;
-    constexpr int kCache = 2;  // blocks per lane kept in registers (nblk <= 64)
-    float2 sl[kCache][kCW];
+    float2 sl[2][kCW];
 #pragma unroll
-    for (int q = 0; q < kCache; ++q) {
+    for (int q = 0; q < 2; ++q) {
         const int i = q * 32 + lane;
 #pragma unroll
         for (int w = 0; w < kCW; ++w)
             sl[q][w] = i < a.nblk && w < wpb ? __ldcg(z + size_t(i) * kCW + w) : make_float2(0.f, 0.f);
     }
-    auto mass = [&](int i, bool residual) {
-        const int q = i >> 5;
-        F2 m = f2(0.f);
-        if (q < kCache) {
+    // Residual mass anywhere in the row (masses are sums of non-negative
+    // terms: their total is positive exactly when one of them is).
+    bool pos = false;
 #pragma unroll
-            for (int c = 0; c < kCache; ++c)
-                if (q == c) {
-                    float v[kCW];
+    for (int q = 0; q < 2; ++q)
 #pragma unroll
-                    for (int w = 0; w < kCW; ++w) v[w] = residual ? sl[c][w].x : sl[c][w].y;
-                    m = sum8_f2(v);
-                }
-        } else {
-            for (int w = 0; w < wpb; ++w) {
-                const float2 x = __ldcg(z + size_t(i) * kCW + w);
-                m = m + f2(residual ? x.x : x.y);
-            }
-        }
-        return m;
-    };
-    F2 total = f2(0.f);
-    for (int t0 = 0; t0 < a.nblk; t0 += 32) {
-        const int i = t0 + lane;
-        total = total + warp_sum_f2(i < a.nblk ? mass(i, true) : f2(0.f));
-    }
-    const bool residual = st.mode == D_RESID && total.hi > 0.f;
+        for (int w = 0; w < kCW; ++w) pos |= sl[q][w].x > 0.f;
+    for (int i = 64 + lane; i < a.nblk; i += 32)
+        for (int w = 0; w < wpb; ++w) pos |= __ldcg(z + size_t(i) * kCW + w).x > 0.f;
+    const bool residual = st.mode == D_RESID && __any_sync(0xffffffffu, pos);
     if (!residual) {
-        // A draw from p (window cut inside the accepted run), or no residual
-        // mass: draw from p of the same row.
         st.mode = D_FALLBACK;
         st.Sp = 1.f;
     }
-    const int blk = choose_block(a.nblk, st.u_blk, [&](int i) { return mass(i, residual); }, lane);
-    float slot_mass[kCW];
-    {
-        const int q = blk >> 5, owner = blk & 31;
 #pragma unroll
-        for (int w = 0; w < kCW; ++w) {
-            float m = 0.f;
-            if (q < kCache) {
+    for (int q = 0; q < 2; ++q)
 #pragma unroll
-                for (int c = 0; c < kCache; ++c)
-                    if (q == c) m = residual ? sl[c][w].x : sl[c][w].y;
-                m = __shfl_sync(0xffffffffu, m, owner);
-            } else if (w < wpb) {
-                const float2 x = __ldcg(z + size_t(blk) * kCW + w);
-                m = residual ? x.x : x.y;
-            }
-            slot_mass[w] = w < wpb ? m : 0.f;
-        }
-    }
-    const int token = block_pick<T>(a, st, b, r, blk, slot_mass, wpb, kSampleBlock / wpb, lane);
-    finish_request(a, b, st.a, token, dr, lane);
+        for (int w = 0; w < kCW; ++w) p.m[q][w] = residual ? sl[q][w].x : sl[q][w].y;
+    p.M = 0.f;
+    p.kind = residual ? 1 : 2;
+    p.r = r;
+    p.acc = st.a;
+    p.st = st;
 }
 
-// The residual draw of request b from its state (the stream kernel's).
+// The end of every sampling draw of request b: the block by u' from the
+// block masses, the slot inside it, then the id by u''; the commit.
 template <typename T>
-__device__ void finish_residual(const VerifyArgs &a, int b, int wpb, int lane) {
-    const DecideState st = load_state(a, b);
-    finish_residual_at<T>(a, b, a.row_off[b] + st.a, st, wpb, lane);
+__device__ void draw_tail(const VerifyArgs &a, int b, const DrawPrep &p, int wpb, int lane) {
+    F2 bm[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) bm[q] = sum8_f2(p.m[q]);
+    // block i's mass, evaluated by the lane owning it
+    auto mass = [&](int i) {
+        if (i < 64) return i < 32 ? bm[0] : bm[1];
+        F2 m = f2(0.f);
+        for (int w = 0; w < wpb; ++w) m = m + f2(slot_mass_at(a, p.kind, b, i, w, p.M));
+        return m;
+    };
+    const int blk = choose_block(a.nblk, p.st.u_blk, mass, lane);
+    float slot_mass[kCW];
+    const int q = blk >> 5, owner = blk & 31;
+#pragma unroll
+    for (int w = 0; w < kCW; ++w) {
+        float m = 0.f;
+        if (q < 2) m = __shfl_sync(0xffffffffu, q == 0 ? p.m[0][w] : p.m[1][w], owner);
+        else if (w < wpb) m = slot_mass_at(a, p.kind, b, blk, w, p.M);
+        slot_mass[w] = w < wpb ? m : 0.f;
+    }
+    const int token = block_pick<T>(a, p.st, b, p.r, blk, slot_mass, wpb, kSampleBlock / wpb, lane);
+    finish_request(a, b, p.acc, token, p.dr, lane);
 }
 
 // ---------------------------------------------------------------------------
@@ -1503,9 +1494,22 @@ __device__ void decider(const VerifyArgs &a, VSmem &sm, const StreamShape &sh, i
         }
         b = __shfl_sync(0xffffffffu, b, 0);
         if (b < 0) return;  // the ready word was read with acquire: no fence needed
-        if (b & kFinishResidual) finish_residual<T>(a, b & ~kFinishResidual, wpb, lane);
-        else if (b & kBonusDraw) bonus_draw<T>(a, sh, b & ~kBonusDraw, wpb, lane);
-        else decide_request<T>(a, sh, b, wpb, epoch, lane);
+        // Every sampling draw goes through the one draw_tail below.
+        DrawPrep dp;
+        bool draw = false, bonus = false;
+        if (b & kFinishResidual) {
+            b &= ~kFinishResidual;
+            const DecideState st = load_state(a, b);
+            prep_residual<T>(a, b, a.row_off[b] + st.a, st, dp, wpb, lane);
+            draw = true;
+        } else if (b & kBonusDraw) {
+            b &= ~kBonusDraw;
+            bonus = true;
+        } else {
+            bonus = decide_request<T>(a, sh, b, wpb, epoch, lane);
+        }
+        if (bonus) draw = prep_bonus<T>(a, sh, b, dp, wpb, lane);
+        if (draw) draw_tail<T>(a, b, dp, wpb, lane);
     }
 }
 
@@ -1671,7 +1675,11 @@ __global__ void __launch_bounds__(kTailThreads) verify_tail_kernel(const VerifyA
             if (s_flag) __threadfence();  // and every other CTA's, before they are read
         }
         __syncthreads();
-        if (s_flag && warp == 0) finish_residual_at<T>(a, jb.x, jb.y, st, wpb, lane);
+        if (s_flag && warp == 0) {
+            DrawPrep dp;
+            prep_residual<T>(a, jb.x, jb.y, st, dp, wpb, lane);
+            draw_tail<T>(a, jb.x, dp, wpb, lane);
+        }
     }
     // The last CTA out resets the list for the next launch.
     __syncthreads();
